@@ -1,0 +1,358 @@
+// The cache-control kernel: one CTA runs the whole per-layer control step.
+//
+// FreeToken article, section "实现要点" (first bullet): the misses, the number
+// of fetches and the evicted slots change every step, and host-driven control
+// would cost a synchronisation at every MoE layer; so all routing-dependent
+// control runs on the GPU with fixed-shape work buffers and a device-resident
+// valid count, and one kernel does dedup, classification against the
+// residency table, the fetch count, victim choice and the logical-to-slot
+// rewrite.  Victim choice finds the K least-recently-used candidate slots in
+// a single pass whatever the miss count.  The fetch count follows the Decode
+// bullet of section "设计 1": q* ~ m*BP/BH, CPU-run experts leave residency
+// unchanged.
+//
+// Step (the clock `now` advances once per call; one cache serves all layers):
+//  1. count routes per local expert (shared-memory histogram);
+//  2. unique experts ascending; hit if slot_of[u] >= 0 (touch: last_use = now);
+//  3. q* = min(m, floor(m*r + 1/2)) in exact integer arithmetic,
+//     q = min(q*, K_max, #slots with last_use < now);
+//  4. the q smallest keys (last_use, slot) among slots with last_use < now:
+//     radix select on last_use (8-bit digits, only the bits where the
+//     eligible values differ), then the slots below the threshold are ranked
+//     and the ones at the threshold taken in slot order;
+//  5. fill i -> victim i: evict, install, last_use = now; the rest go to CPU;
+//  6. rewrite route ids to slot ids (-1 = CPU);
+//  7. group the routes by resident expert for the expert kernel (dispatch).
+#include "ft_internal.h"
+
+namespace ft {
+namespace {
+
+constexpr int NT = kControlThreads;
+constexpr int NW = NT / 32;
+
+struct Smem {
+  int ecount[kMaxExperts];   // routes per local expert
+  int emap[kMaxExperts];     // slot per local expert after the step (-1 none)
+  int gstart[kMaxExperts];   // first group_routes index of the expert's group
+  int cursor[kMaxExperts];   // scatter cursor per expert
+  int miss_local[kMaxExperts];
+  int victims[kMaxKmax];
+  int eqsel[kMaxKmax];
+  unsigned long long cand[kMaxKmax];  // (last_use << 32 | slot) below the threshold
+  unsigned hist[256];
+  int wsum[NW];
+  unsigned wmin[NW], wmax[NW];
+  int sc[16];  // scalars
+};
+
+// Exclusive block scan (NT threads); total returned through *total.
+__device__ __forceinline__ int block_scan(int v, int* wsum, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int s = lane < NW ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < NW) wsum[lane] = s;
+  }
+  __syncthreads();
+  int base = wid ? wsum[wid - 1] : 0;
+  *total = wsum[NW - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+__global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  Smem& sm = *reinterpret_cast<Smem*>(dyn);
+  unsigned* lu = reinterpret_cast<unsigned*>(dyn + sizeof(Smem));  // [S] last_use copy
+  const int tid = threadIdx.x;
+  const int E = a.E, S = a.S;
+  const int base_id = a.layer * E;
+
+  const unsigned now0 = *a.now;
+  const bool wrap = now0 == 0xFFFFFFFFu;
+  const unsigned now = now0 + 1u;
+
+  for (int e = tid; e < E; e += NT) {
+    sm.ecount[e] = 0;
+    sm.emap[e] = -1;
+    sm.cursor[e] = 0;
+  }
+  for (int s = tid; s < S; s += NT) lu[s] = a.last_use[s];
+  __syncthreads();
+
+  // 1. count routes
+  bool bad = false;
+  for (int r = tid; r < a.n_routes; r += NT) {
+    int e = a.ids[r];
+    if ((unsigned)e >= (unsigned)E)
+      bad = true;
+    else if (!wrap)
+      atomicAdd(&sm.ecount[e], 1);
+  }
+  if (__syncthreads_or(bad) && tid == 0) atomicOr(a.status, FT_ST_ROUTE_RANGE);
+  if (wrap) {
+    // The clock cannot advance: leave the table alone and send every route to the CPU.
+    if (tid == 0) atomicOr(a.status, FT_ST_CLOCK_WRAP);
+    for (int r = tid; r < a.n_routes; r += NT) a.slot_ids[r] = -1;
+    if (tid < kCountsLen) a.counts[tid] = 0;
+    if (tid == 0) a.group_off[0] = 0;
+    return;
+  }
+
+  // 2. dedup + classify (E <= NT: one expert per thread)
+  const int e = tid;
+  const bool present = e < E && sm.ecount[e] > 0;
+  int slot = -1;
+  if (present) slot = a.slot_of[base_id + e];
+  const bool hit = present && slot >= 0;
+  int tot;
+  int ex = block_scan(present ? (hit ? 1 : 0x10000) : 0, sm.wsum, &tot);
+  const int hits = tot & 0xFFFF, m = tot >> 16, n = hits + m;
+  const int hpos = ex & 0xFFFF, mpos = ex >> 16;
+  if (present) a.uniq[hpos + mpos] = base_id + e;
+  if (hit) {
+    if ((unsigned)slot >= (unsigned)S) {
+      atomicOr(a.status, FT_ST_BAD_SLOT);
+    } else {
+      a.hit_list[hpos] = base_id + e;
+      lu[slot] = now;
+      a.last_use[slot] = now;
+      sm.emap[e] = slot;
+    }
+  } else if (present) {
+    sm.miss_local[mpos] = e;
+  }
+  __syncthreads();
+
+  // 3. q*, q.  Each thread owns the contiguous slot range [s0, s1).
+  const int per = (S + NT - 1) / NT;
+  const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
+  int my_elig = 0;
+  unsigned my_min = 0xFFFFFFFFu, my_max = 0;
+  for (int s = s0; s < s1; ++s) {
+    unsigned v = lu[s];
+    if (v < now) {
+      ++my_elig;
+      my_min = min(my_min, v);
+      my_max = max(my_max, v);
+    }
+  }
+  int avail;
+  (void)block_scan(my_elig, sm.wsum, &avail);
+  long long qstar = (2LL * m * a.r_num + a.r_den) / (2LL * a.r_den);
+  if (qstar > m) qstar = m;
+  int q = (int)qstar;
+  if (q > a.K_max) q = a.K_max;
+  if (q > avail) q = avail;
+
+  // 4. victims: the q smallest (last_use, slot) among eligible slots
+  if (q > 0) {
+    const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      my_min = min(my_min, __shfl_xor_sync(0xffffffffu, my_min, o));
+      my_max = max(my_max, __shfl_xor_sync(0xffffffffu, my_max, o));
+    }
+    if (lane == 0) {
+      sm.wmin[wid] = my_min;
+      sm.wmax[wid] = my_max;
+    }
+    __syncthreads();
+    if (wid == 0) {
+      unsigned mn = sm.wmin[lane], mx = sm.wmax[lane];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      if (lane == 0) {
+        sm.sc[0] = (int)mn;
+        sm.sc[1] = (int)mx;
+      }
+    }
+    __syncthreads();
+    const unsigned vmin = (unsigned)sm.sc[0], range = (unsigned)sm.sc[1] - vmin;
+    const int bits = range ? 32 - __clz(range) : 0;
+    const int passes = (bits + 7) / 8;
+    unsigned prefix = 0;  // of key' = last_use - vmin, digits fixed so far
+    int need = q;         // how many still to take within the current prefix bucket
+    for (int p = passes - 1; p >= 0; --p) {
+      const int shift = 8 * p;
+      if (tid < 256) sm.hist[tid] = 0;
+      __syncthreads();
+      for (int s = s0; s < s1; ++s) {
+        unsigned v = lu[s];
+        if (v >= now) continue;
+        unsigned kk = v - vmin;
+        // higher digits must match the prefix (shift+8 may be 32: test in 64 bits)
+        if (((unsigned long long)kk >> (shift + 8)) != ((unsigned long long)prefix >> (shift + 8))) continue;
+        atomicAdd(&sm.hist[(kk >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (wid == 0) {
+        // lane owns bins [8*lane, 8*lane+8)
+        unsigned c[8], loc = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          c[i] = sm.hist[8 * lane + i];
+          loc += c[i];
+        }
+        unsigned incl = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        unsigned before = incl - loc;
+        // the lane whose range crosses `need`
+        bool mine = before < (unsigned)need && (unsigned)need <= incl;
+        if (mine) {
+          unsigned acc = before;
+          int d = 0;
+          for (; d < 8; ++d) {
+            if (acc + c[d] >= (unsigned)need) break;
+            acc += c[d];
+          }
+          sm.sc[2] = 8 * lane + d;
+          sm.sc[3] = need - (int)acc;
+        }
+      }
+      __syncthreads();
+      prefix |= (unsigned)sm.sc[2] << shift;
+      need = sm.sc[3];
+      __syncthreads();
+    }
+    const unsigned thr = vmin + prefix;  // last_use of the q-th smallest key
+    const int need_eq = need;             // slots with last_use == thr to take, lowest index first
+
+    int my_lt = 0, my_eq = 0;
+    for (int s = s0; s < s1; ++s) {
+      unsigned v = lu[s];
+      my_lt += v < thr;
+      my_eq += v == thr;
+    }
+    int tot2;
+    int ex2 = block_scan(my_lt | (my_eq << 16), sm.wsum, &tot2);
+    int lt_pos = ex2 & 0xFFFF, eq_pos = ex2 >> 16;
+    const int c_lt = tot2 & 0xFFFF;
+    for (int s = s0; s < s1; ++s) {
+      unsigned v = lu[s];
+      if (v < thr) {
+        sm.cand[lt_pos++] = ((unsigned long long)v << 32) | (unsigned)s;
+      } else if (v == thr) {
+        if (eq_pos < need_eq) sm.eqsel[eq_pos] = s;
+        ++eq_pos;
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < c_lt; i += NT) {
+      unsigned long long key = sm.cand[i];
+      int rank = 0;
+      for (int j = 0; j < c_lt; ++j) rank += sm.cand[j] < key;
+      sm.victims[rank] = (int)(key & 0xFFFFFFFFu);
+    }
+    for (int i = tid; i < need_eq; i += NT) sm.victims[c_lt + i] = sm.eqsel[i];
+    __syncthreads();
+  }
+
+  // 5. table update (fill i -> victim i) and CPU list
+  int my_evict = 0;
+  for (int i = tid; i < q; i += NT) {
+    int s = sm.victims[i];
+    int le = sm.miss_local[i];
+    int u = base_id + le;
+    int old = a.expert_of[s];
+    a.evicted[i] = old;
+    if (old >= 0) {
+      a.slot_of[old] = -1;
+      my_evict = 1;
+    }
+    a.slot_of[u] = s;
+    a.expert_of[s] = u;
+    a.last_use[s] = now;
+    a.fetch[i] = u;
+    a.victims[i] = s;
+    sm.emap[le] = s;
+  }
+  for (int i = q + tid; i < m; i += NT) a.cpu_list[i - q] = base_id + sm.miss_local[i];
+  const int evictions = __syncthreads_count(my_evict);
+
+  // 6. rewrite
+  for (int r = tid; r < a.n_routes; r += NT) {
+    int le = a.ids[r];
+    a.slot_ids[r] = ((unsigned)le < (unsigned)E) ? sm.emap[le] : -1;
+  }
+
+  // 7. groups of routes per resident expert, experts ascending
+  const bool resident = present && sm.emap[e] >= 0;
+  int tot3;
+  int ex3 = block_scan(resident ? (sm.ecount[e] | 0x10000) : 0, sm.wsum, &tot3);
+  const int n_groups = tot3 >> 16, n_grouped = tot3 & 0xFFFF;
+  if (resident) {
+    int gi = ex3 >> 16, off = ex3 & 0xFFFF;
+    a.group_slot[gi] = sm.emap[e];
+    a.group_off[gi] = off;
+    sm.gstart[e] = off;
+  }
+  if (tid == 0) a.group_off[n_groups] = n_grouped;
+  __syncthreads();
+  for (int r = tid; r < a.n_routes; r += NT) {
+    int le = a.ids[r];
+    if ((unsigned)le < (unsigned)E && sm.emap[le] >= 0) {
+      int pos = sm.gstart[le] + atomicAdd(&sm.cursor[le], 1);
+      a.group_routes[pos] = r;
+    }
+  }
+
+  if (tid == 0) {
+    a.counts[0] = n;
+    a.counts[1] = hits;
+    a.counts[2] = m;
+    a.counts[3] = q;
+    a.counts[4] = m - q;
+    a.counts[5] = n_groups;
+    a.counts[6] = (int)now;
+    a.counts[7] = 0;
+    *a.now = now;
+    a.counters[0] += (unsigned long long)hits;
+    a.counters[1] += (unsigned long long)m;
+    a.counters[2] += (unsigned long long)q;
+    a.counters[3] += (unsigned long long)(m - q);
+    a.counters[4] += (unsigned long long)evictions;
+    a.counters[5] += 1ull;
+  }
+}
+
+}  // namespace
+
+size_t control_smem_bytes(int S) { return sizeof(Smem) + sizeof(unsigned) * (size_t)S; }
+
+cudaError_t launch_control(const ControlArgs& a, cudaStream_t st) {
+  size_t smem = control_smem_bytes(a.S);
+  static thread_local int configured_for = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_for != dev) {
+    cudaError_t e = cudaFuncSetAttribute(control_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)control_smem_bytes(kMaxSlots));
+    if (e != cudaSuccess) return e;
+    configured_for = dev;
+  }
+  control_kernel<<<1, NT, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace ft

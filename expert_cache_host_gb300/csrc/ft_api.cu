@@ -1,0 +1,495 @@
+// C ABI: context, host-pool pinning, per-layer step buffers, streams, and the
+// order in which one MoE layer step's kernels are enqueued.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "ft_internal.h"
+#include "prefill.h"
+
+using namespace ft;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+#define CU(call)                                                                              \
+  do {                                                                                        \
+    cudaError_t e_ = (call);                                                                  \
+    if (e_ != cudaSuccess) return fail(FT_E_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+size_t expert_bytes(const ft_config& c) {
+  size_t df = (size_t)c.hidden * (size_t)c.inter;
+  return c.dtype == FT_DTYPE_BF16 ? 6 * df : 3 * df / 2 + 3 * df / 32;
+}
+
+}  // namespace
+
+struct ft_ctx {
+  ft_config cfg{};
+  int device = 0;
+  int sm_count = 0;
+  int S = 0;
+  int E_tot = 0;
+  size_t Bx = 0;
+  int epoch = 0;
+
+  void* host_pool = nullptr;
+  size_t pool_bytes = 0;
+  bool registered = false;
+  const uint8_t* pool_dev = nullptr;
+
+  uint8_t* arena = nullptr;
+  int32_t* slot_of = nullptr;
+  int32_t* expert_of = nullptr;
+  uint32_t* last_use = nullptr;
+  uint32_t* now = nullptr;
+  uint32_t* status = nullptr;
+  unsigned long long* counters = nullptr;
+
+  void* layer_mem = nullptr;
+  std::vector<LayerBufs> layers;
+  float* ypart = nullptr;
+  int n_chunks = 0;
+
+  cudaStream_t xfer = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+
+  // copy-engine fill mode: host copies of the step's fetch list
+  int32_t* h_counts = nullptr;
+  int32_t* h_fetch = nullptr;
+  int32_t* h_victims = nullptr;
+
+  PrefillState* prefill = nullptr;
+};
+
+namespace {
+
+int check_config(const ft_config& c) {
+  if (c.num_layers < 1) return fail(FT_E_ARG, "num_layers must be >= 1");
+  if (c.num_experts < 1 || c.num_experts > kMaxExperts) return fail(FT_E_ARG, "num_experts must be in [1, %d]", kMaxExperts);
+  if (c.top_k < 1 || c.top_k > kMaxTopK || c.top_k > c.num_experts) return fail(FT_E_ARG, "top_k must be in [1, min(32, E)]");
+  if (c.hidden < 256 || c.hidden % 256) return fail(FT_E_ARG, "hidden must be a positive multiple of 256");
+  if (c.inter < 128 || c.inter % 128) return fail(FT_E_ARG, "inter must be a positive multiple of 128");
+  if (c.dtype != FT_DTYPE_BF16 && c.dtype != FT_DTYPE_MXFP4) return fail(FT_E_ARG, "dtype must be BF16 or MXFP4");
+  if (c.num_slots < 1 || c.num_slots > kMaxSlots) return fail(FT_E_ARG, "num_slots must be in [1, %d]", kMaxSlots);
+  if (c.k_max < 1 || c.k_max > kMaxKmax) return fail(FT_E_ARG, "k_max must be in [1, %d]", kMaxKmax);
+  if (c.t_max < 1 || c.t_max > 1024 || c.t_max * c.top_k > 32768) return fail(FT_E_ARG, "t_max must be in [1, 1024] with t_max*k <= 32768");
+  if (c.r_num < 0 || c.r_den < 1) return fail(FT_E_ARG, "r = r_num/r_den needs r_num >= 0, r_den >= 1");
+  if (c.prefill_buffers < 0 || c.prefill_buffers > 2) return fail(FT_E_ARG, "prefill_buffers must be 0, 1 or 2");
+  if (c.prefill_buffers > 0 && (c.prefill_t_max < 1 || c.prefill_t_max > 65536))
+    return fail(FT_E_ARG, "prefill_t_max must be in [1, 65536] when prefill_buffers > 0");
+  if (c.fill_mode != FT_FILL_KERNEL && c.fill_mode != FT_FILL_COPY_ENGINE) return fail(FT_E_ARG, "bad fill_mode");
+  for (int i = 0; i < 4; ++i)
+    if (c.reserved[i]) return fail(FT_E_ARG, "reserved fields must be zero");
+  if ((long long)c.num_layers * c.num_experts > 0x7fffffffLL) return fail(FT_E_ARG, "too many experts");
+  return FT_OK;
+}
+
+int alloc_arena(ft_ctx* c, int S) {
+  c->S = 0;
+  size_t bytes = (size_t)S * c->Bx;
+  if (cudaMalloc(&c->arena, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    c->arena = nullptr;
+    return fail(FT_E_NOMEM, "slot arena of %d slots (%zu bytes) does not fit", S, bytes);
+  }
+  if (cudaMalloc(&c->expert_of, sizeof(int32_t) * S) != cudaSuccess ||
+      cudaMalloc(&c->last_use, sizeof(uint32_t) * S) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(FT_E_NOMEM, "residency table allocation failed");
+  }
+  c->S = S;
+  return FT_OK;
+}
+
+int reset_table(ft_ctx* c) {
+  CU(cudaMemset(c->slot_of, 0xFF, sizeof(int32_t) * c->E_tot));
+  CU(cudaMemset(c->expert_of, 0xFF, sizeof(int32_t) * c->S));
+  CU(cudaMemset(c->last_use, 0, sizeof(uint32_t) * c->S));
+  CU(cudaMemset(c->now, 0, sizeof(uint32_t)));
+  CU(cudaMemset(c->counters, 0, sizeof(unsigned long long) * kCountersPerLayer * c->cfg.num_layers));
+  for (auto& lb : c->layers) lb.last_T = -1;
+  return FT_OK;
+}
+
+void free_all(ft_ctx* c) {
+  if (c->prefill) prefill_destroy(c->prefill);
+  cudaFree(c->arena);
+  cudaFree(c->slot_of);
+  cudaFree(c->expert_of);
+  cudaFree(c->last_use);
+  cudaFree(c->now);
+  cudaFree(c->status);
+  cudaFree(c->counters);
+  cudaFree(c->layer_mem);
+  cudaFree(c->ypart);
+  if (c->h_counts) cudaFreeHost(c->h_counts);
+  if (c->h_fetch) cudaFreeHost(c->h_fetch);
+  if (c->h_victims) cudaFreeHost(c->h_victims);
+  if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+  if (c->ev_join) cudaEventDestroy(c->ev_join);
+  if (c->xfer) cudaStreamDestroy(c->xfer);
+  if (c->registered) cudaHostUnregister(c->host_pool);
+}
+
+int check_layer(ft_ctx* c, int layer) {
+  if (!c) return fail(FT_E_ARG, "null context");
+  if (layer < 0 || layer >= c->cfg.num_layers) return fail(FT_E_ARG, "layer %d outside [0, %d)", layer, c->cfg.num_layers);
+  if (c->S < 1) return fail(FT_E_STATE, "the cache has no slots (a rebuild failed)");
+  return FT_OK;
+}
+
+int enqueue_control(ft_ctx* c, int layer, const int32_t* ids, int T, cudaStream_t st) {
+  LayerBufs& lb = c->layers[layer];
+  ControlArgs a{};
+  a.layer = layer;
+  a.E = c->cfg.num_experts;
+  a.n_routes = T * c->cfg.top_k;
+  a.S = c->S;
+  a.K_max = c->cfg.k_max;
+  a.r_num = c->cfg.r_num;
+  a.r_den = c->cfg.r_den;
+  a.ids = ids;
+  a.slot_of = c->slot_of;
+  a.expert_of = c->expert_of;
+  a.last_use = c->last_use;
+  a.now = c->now;
+  a.status = c->status;
+  a.counters = c->counters + (size_t)kCountersPerLayer * layer;
+  a.slot_ids = lb.slot_ids;
+  a.uniq = lb.uniq;
+  a.hit_list = lb.hit_list;
+  a.fetch = lb.fetch;
+  a.victims = lb.victims;
+  a.evicted = lb.evicted;
+  a.cpu_list = lb.cpu_list;
+  a.counts = lb.counts;
+  a.group_slot = lb.group_slot;
+  a.group_off = lb.group_off;
+  a.group_routes = lb.group_routes;
+  CU(launch_control(a, st));
+  lb.last_T = T;
+  return FT_OK;
+}
+
+void fill_out(ft_ctx* c, int layer, ft_step_out* out) {
+  if (!out) return;
+  LayerBufs& lb = c->layers[layer];
+  out->ids = lb.ids;
+  out->weights = lb.w;
+  out->slot_ids = lb.slot_ids;
+  out->uniq = lb.uniq;
+  out->hit_list = lb.hit_list;
+  out->fetch = lb.fetch;
+  out->victims = lb.victims;
+  out->evicted = lb.evicted;
+  out->cpu_list = lb.cpu_list;
+  out->counts = lb.counts;
+}
+
+int enqueue_fill(ft_ctx* c, int layer, cudaStream_t st) {
+  LayerBufs& lb = c->layers[layer];
+  CU(cudaEventRecord(c->ev_fork, st));
+  CU(cudaStreamWaitEvent(c->xfer, c->ev_fork, 0));
+  if (c->cfg.fill_mode == FT_FILL_KERNEL) {
+    CU(launch_fill(c->pool_dev, c->arena, lb.counts, lb.fetch, lb.victims, c->Bx, c->S, c->E_tot, c->status,
+                   2 * c->sm_count, c->xfer));
+  } else {
+    // Copy-engine fills need the fetch list on the host: this reads it back.
+    CU(cudaMemcpyAsync(c->h_counts, lb.counts, sizeof(int32_t) * kCountsLen, cudaMemcpyDeviceToHost, c->xfer));
+    CU(cudaMemcpyAsync(c->h_fetch, lb.fetch, sizeof(int32_t) * c->cfg.k_max, cudaMemcpyDeviceToHost, c->xfer));
+    CU(cudaMemcpyAsync(c->h_victims, lb.victims, sizeof(int32_t) * c->cfg.k_max, cudaMemcpyDeviceToHost, c->xfer));
+    CU(cudaStreamSynchronize(c->xfer));
+    const int q = c->h_counts[3];
+    for (int i = 0; i < q; ++i) {
+      const int u = c->h_fetch[i], s = c->h_victims[i];
+      if (u < 0 || u >= c->E_tot || s < 0 || s >= c->S) return fail(FT_E_STATE, "corrupt fetch list entry %d", i);
+      CU(cudaMemcpyAsync(c->arena + (size_t)s * c->Bx, (const uint8_t*)c->host_pool + (size_t)u * c->Bx, c->Bx,
+                         cudaMemcpyHostToDevice, c->xfer));
+    }
+  }
+  CU(cudaEventRecord(c->ev_join, c->xfer));
+  CU(cudaStreamWaitEvent(st, c->ev_join, 0));
+  return FT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ft_last_error(void) { return g_err; }
+
+int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx** out) {
+  g_err[0] = 0;
+  if (!cfg || !out) return fail(FT_E_ARG, "null config or output pointer");
+  *out = nullptr;
+  int rc = check_config(*cfg);
+  if (rc) return rc;
+  if (!host_pool) return fail(FT_E_ARG, "null host pool");
+  ft_ctx* c = new (std::nothrow) ft_ctx();
+  if (!c) return fail(FT_E_NOMEM, "host allocation failed");
+  c->cfg = *cfg;
+  c->E_tot = cfg->num_layers * cfg->num_experts;
+  c->Bx = expert_bytes(*cfg);
+  c->host_pool = host_pool;
+  c->pool_bytes = pool_bytes;
+  if (pool_bytes < (size_t)c->E_tot * c->Bx) {
+    delete c;
+    return fail(FT_E_ARG, "pool_bytes %zu < L*E*B_x = %zu", pool_bytes, (size_t)c->E_tot * c->Bx);
+  }
+  auto bail = [&](int code) {
+    free_all(c);
+    delete c;
+    return code;
+  };
+  if (cudaGetDevice(&c->device) != cudaSuccess) return bail(fail(FT_E_CUDA, "no CUDA device"));
+  cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
+
+  // Pin after write: the caller has already written the final layout.
+  cudaPointerAttributes pa{};
+  if (cudaPointerGetAttributes(&pa, host_pool) == cudaSuccess && pa.type == cudaMemoryTypeHost) {
+    c->registered = false;
+  } else {
+    cudaGetLastError();
+    cudaError_t e = cudaHostRegister(host_pool, pool_bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return bail(fail(FT_E_PIN, "cudaHostRegister of %zu bytes failed: %s", pool_bytes, cudaGetErrorString(e)));
+    }
+    c->registered = true;
+  }
+  void* dp = nullptr;
+  if (cudaHostGetDevicePointer(&dp, host_pool, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return bail(fail(FT_E_PIN, "the host pool is pinned but not mapped into the device address space"));
+  }
+  c->pool_dev = static_cast<const uint8_t*>(dp);
+
+  if (cudaMalloc(&c->slot_of, sizeof(int32_t) * c->E_tot) != cudaSuccess ||
+      cudaMalloc(&c->now, sizeof(uint32_t)) != cudaSuccess || cudaMalloc(&c->status, sizeof(uint32_t)) != cudaSuccess ||
+      cudaMalloc(&c->counters, sizeof(unsigned long long) * kCountersPerLayer * cfg->num_layers) != cudaSuccess) {
+    cudaGetLastError();
+    return bail(fail(FT_E_NOMEM, "table allocation failed"));
+  }
+  if ((rc = alloc_arena(c, cfg->num_slots))) return bail(rc);
+
+  // per-layer step buffers, one allocation
+  const int E = cfg->num_experts, TK = cfg->t_max * cfg->top_k, K = cfg->k_max;
+  const size_t per_layer_words = (size_t)TK * 4 /*ids w slot_ids group_routes*/ + (size_t)E * 4 /*uniq hit cpu gslot*/ +
+                                 (E + 1) /*goff*/ + (size_t)K * 3 + kCountsLen;
+  const size_t per_layer = (per_layer_words * 4 + 255) / 256 * 256;
+  if (cudaMalloc(&c->layer_mem, per_layer * cfg->num_layers) != cudaSuccess) {
+    cudaGetLastError();
+    return bail(fail(FT_E_NOMEM, "step buffer allocation failed"));
+  }
+  c->layers.resize(cfg->num_layers);
+  for (int l = 0; l < cfg->num_layers; ++l) {
+    int32_t* p = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(c->layer_mem) + per_layer * l);
+    LayerBufs& lb = c->layers[l];
+    lb.ids = p; p += TK;
+    lb.w = reinterpret_cast<float*>(p); p += TK;
+    lb.slot_ids = p; p += TK;
+    lb.group_routes = p; p += TK;
+    lb.uniq = p; p += E;
+    lb.hit_list = p; p += E;
+    lb.cpu_list = p; p += E;
+    lb.group_slot = p; p += E;
+    lb.group_off = p; p += E + 1;
+    lb.fetch = p; p += K;
+    lb.victims = p; p += K;
+    lb.evicted = p; p += K;
+    lb.counts = p; p += kCountsLen;
+    lb.last_T = -1;
+  }
+  c->n_chunks = cfg->inter / kDecodeChunk;
+  if (cudaMalloc(&c->ypart, sizeof(float) * (size_t)TK * c->n_chunks * cfg->hidden) != cudaSuccess) {
+    cudaGetLastError();
+    return bail(fail(FT_E_NOMEM, "decode work buffer allocation failed"));
+  }
+  if (cudaMemset(c->layer_mem, 0, per_layer * cfg->num_layers) != cudaSuccess ||
+      cudaMemset(c->status, 0, sizeof(uint32_t)) != cudaSuccess)
+    return bail(fail(FT_E_CUDA, "memset failed"));
+  if ((rc = reset_table(c))) return bail(rc);
+
+  int lo = 0, hi = 0;
+  cudaDeviceGetStreamPriorityRange(&lo, &hi);
+  if (cudaStreamCreateWithPriority(&c->xfer, cudaStreamNonBlocking, hi) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming) != cudaSuccess)
+    return bail(fail(FT_E_CUDA, "stream/event creation failed"));
+  if (cfg->fill_mode == FT_FILL_COPY_ENGINE) {
+    if (cudaMallocHost(&c->h_counts, sizeof(int32_t) * kCountsLen) != cudaSuccess ||
+        cudaMallocHost(&c->h_fetch, sizeof(int32_t) * K) != cudaSuccess ||
+        cudaMallocHost(&c->h_victims, sizeof(int32_t) * K) != cudaSuccess)
+      return bail(fail(FT_E_NOMEM, "pinned host allocation failed"));
+  }
+  if (cfg->prefill_buffers > 0) {
+    PrefillConfig pc{cfg->num_layers, cfg->num_experts, cfg->top_k, cfg->hidden, cfg->inter, cfg->dtype,
+                     cfg->prefill_buffers, cfg->prefill_t_max, c->Bx, c->pool_dev, c->host_pool, c->status,
+                     c->sm_count};
+    char msg[256] = "";
+    c->prefill = prefill_create(pc, msg, sizeof(msg));
+    if (!c->prefill) return bail(fail(FT_E_NOMEM, "prefill buffers: %s", msg));
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) return bail(fail(FT_E_CUDA, "initialisation failed"));
+  *out = c;
+  return FT_OK;
+}
+
+int ft_moe_destroy(ft_ctx* c) {
+  if (!c) return FT_OK;
+  if (c->xfer) cudaStreamSynchronize(c->xfer);
+  cudaDeviceSynchronize();
+  free_all(c);
+  delete c;
+  return FT_OK;
+}
+
+int ft_cache_step(ft_ctx* c, int layer, const float* logits, int T, ft_step_out* out, void* stream) {
+  int rc = check_layer(c, layer);
+  if (rc) return rc;
+  if (T < 1 || T > c->cfg.t_max) return fail(FT_E_ARG, "T=%d outside [1, t_max=%d]", T, c->cfg.t_max);
+  if (!logits) return fail(FT_E_ARG, "null logits");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LayerBufs& lb = c->layers[layer];
+  CU(launch_route(logits, T, c->cfg.num_experts, c->cfg.top_k, lb.ids, lb.w, c->status, nullptr, st));
+  if ((rc = enqueue_control(c, layer, lb.ids, T, st))) return rc;
+  fill_out(c, layer, out);
+  return FT_OK;
+}
+
+int ft_cache_control(ft_ctx* c, int layer, const int32_t* ids, int T, ft_step_out* out, void* stream) {
+  int rc = check_layer(c, layer);
+  if (rc) return rc;
+  if (T < 1 || T > c->cfg.t_max) return fail(FT_E_ARG, "T=%d outside [1, t_max=%d]", T, c->cfg.t_max);
+  if (!ids) return fail(FT_E_ARG, "null ids");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LayerBufs& lb = c->layers[layer];
+  CU(cudaMemcpyAsync(lb.ids, ids, sizeof(int32_t) * T * c->cfg.top_k, cudaMemcpyDeviceToDevice, st));
+  if ((rc = enqueue_control(c, layer, lb.ids, T, st))) return rc;
+  fill_out(c, layer, out);
+  return FT_OK;
+}
+
+int ft_moe_forward(ft_ctx* c, int layer, int mode, const float* logits, const uint16_t* hidden, int T,
+                   const float* partial, float* out, void* stream) {
+  int rc = check_layer(c, layer);
+  if (rc) return rc;
+  if (!hidden || !out) return fail(FT_E_ARG, "null hidden or out");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (mode == FT_PREFILL_LAYER) {
+    if (!c->prefill) return fail(FT_E_STATE, "the context was created with prefill_buffers = 0");
+    if (!logits) return fail(FT_E_ARG, "prefill needs router logits");
+    if (T < 1 || T > c->cfg.prefill_t_max) return fail(FT_E_ARG, "T=%d outside [1, prefill_t_max]", T);
+    char msg[256] = "";
+    int r = prefill_forward(c->prefill, layer, logits, hidden, T, partial, out, st, msg, sizeof(msg));
+    if (r) return fail(r, "prefill: %s", msg);
+    return FT_OK;
+  }
+  if (mode != FT_DECODE_CACHED) return fail(FT_E_ARG, "unknown mode %d", mode);
+  LayerBufs& lb = c->layers[layer];
+  if (lb.last_T != T) return fail(FT_E_STATE, "decode forward of layer %d with T=%d needs a cache step with the same T", layer, T);
+  if ((rc = enqueue_fill(c, layer, st))) return rc;
+  DecodeArgs a{};
+  a.arena = c->arena;
+  a.Bx = c->Bx;
+  a.S = c->S;
+  a.d = c->cfg.hidden;
+  a.f = c->cfg.inter;
+  a.k = c->cfg.top_k;
+  a.dtype = c->cfg.dtype;
+  a.max_groups = T * c->cfg.top_k < c->cfg.num_experts ? T * c->cfg.top_k : c->cfg.num_experts;
+  a.counts = lb.counts;
+  a.group_slot = lb.group_slot;
+  a.group_off = lb.group_off;
+  a.group_routes = lb.group_routes;
+  a.hidden = hidden;
+  a.ypart = c->ypart;
+  a.status = c->status;
+  cudaError_t e = launch_decode_experts(a, st);
+  if (e == cudaErrorNotSupported) return fail(FT_E_UNSUPPORTED, "decode experts for this dtype are not built");
+  CU(e);
+  CU(launch_merge(c->ypart, c->n_chunks, lb.slot_ids, lb.w, partial, out, T, c->cfg.top_k, c->cfg.hidden, st));
+  return FT_OK;
+}
+
+int ft_cache_rebuild(ft_ctx* c, int new_slots) {
+  if (!c) return fail(FT_E_ARG, "null context");
+  if (new_slots < 1 || new_slots > kMaxSlots) return fail(FT_E_ARG, "new_slots must be in [1, %d]", kMaxSlots);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(c->xfer, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return fail(FT_E_STATE, "rebuild during stream capture");
+  CU(cudaDeviceSynchronize());
+  cudaFree(c->arena);
+  cudaFree(c->expert_of);
+  cudaFree(c->last_use);
+  c->arena = nullptr;
+  c->expert_of = nullptr;
+  c->last_use = nullptr;
+  c->S = 0;
+  ++c->epoch;
+  int rc = alloc_arena(c, new_slots);
+  if (rc) return rc;
+  if ((rc = reset_table(c))) return rc;
+  CU(cudaDeviceSynchronize());
+  return FT_OK;
+}
+
+int ft_get_status(ft_ctx* c, uint32_t* status, int clear) {
+  if (!c || !status) return fail(FT_E_ARG, "null argument");
+  CU(cudaDeviceSynchronize());
+  CU(cudaMemcpy(status, c->status, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  if (clear) CU(cudaMemset(c->status, 0, sizeof(uint32_t)));
+  return FT_OK;
+}
+
+int ft_get_counters(ft_ctx* c, uint64_t* counters) {
+  if (!c || !counters) return fail(FT_E_ARG, "null argument");
+  CU(cudaDeviceSynchronize());
+  CU(cudaMemcpy(counters, c->counters, sizeof(unsigned long long) * kCountersPerLayer * c->cfg.num_layers,
+                cudaMemcpyDeviceToHost));
+  return FT_OK;
+}
+
+int ft_get_table(ft_ctx* c, int32_t* slot_of, int32_t* expert_of, uint32_t* last_use, uint32_t* now) {
+  if (!c) return fail(FT_E_ARG, "null context");
+  CU(cudaDeviceSynchronize());
+  if (slot_of) CU(cudaMemcpy(slot_of, c->slot_of, sizeof(int32_t) * c->E_tot, cudaMemcpyDeviceToHost));
+  if (expert_of && c->S) CU(cudaMemcpy(expert_of, c->expert_of, sizeof(int32_t) * c->S, cudaMemcpyDeviceToHost));
+  if (last_use && c->S) CU(cudaMemcpy(last_use, c->last_use, sizeof(uint32_t) * c->S, cudaMemcpyDeviceToHost));
+  if (now) CU(cudaMemcpy(now, c->now, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  return FT_OK;
+}
+
+void* ft_slot_ptr(ft_ctx* c, int slot) {
+  if (!c || slot < 0 || slot >= c->S) return nullptr;
+  return c->arena + (size_t)slot * c->Bx;
+}
+
+int ft_get_epoch(ft_ctx* c) { return c ? c->epoch : fail(FT_E_ARG, "null context"); }
+
+int ft_num_slots(ft_ctx* c) { return c ? c->S : fail(FT_E_ARG, "null context"); }
+
+int ft_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, uint32_t* status, void* stream) {
+  if (!logits || !ids || !w) return fail(FT_E_ARG, "null pointer");
+  if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || k > kMaxTopK || k > E)
+    return fail(FT_E_ARG, "bad routing shape T=%d E=%d k=%d", T, E, k);
+  CU(launch_route(logits, T, E, k, ids, w, status, nullptr, static_cast<cudaStream_t>(stream)));
+  return FT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ft_moe.h"
+
+namespace ft {
+
+constexpr int kCountsLen = 8;     // n, hits, m, q, cpu, n_groups, now, 0
+constexpr int kCountersPerLayer = 6;  // hits, misses, fills, cpu, evictions, steps
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kMaxSlots = 32768;
+constexpr int kMaxKmax = 1024;
+constexpr int kControlThreads = 1024;
+
+// Rows of the intermediate dimension f handled by one decode GEMV work unit.
+constexpr int kDecodeChunk = 32;
+
+// Per-layer fixed-shape step buffers (device).
+struct LayerBufs {
+  int32_t* ids;
+  float* w;
+  int32_t* slot_ids;
+  int32_t* uniq;
+  int32_t* hit_list;
+  int32_t* fetch;
+  int32_t* victims;
+  int32_t* evicted;
+  int32_t* cpu_list;
+  int32_t* counts;
+  int32_t* group_slot;
+  int32_t* group_off;
+  int32_t* group_routes;
+  int last_T;  // T of the last step (host-side record, -1 = none)
+};
+
+struct ControlArgs {
+  int layer, E, n_routes, S, K_max;
+  long long r_num, r_den;
+  const int32_t* ids;
+  int32_t* slot_of;
+  int32_t* expert_of;
+  uint32_t* last_use;
+  uint32_t* now;
+  uint32_t* status;
+  unsigned long long* counters;  // this layer's row
+  int32_t* slot_ids;
+  int32_t* uniq;
+  int32_t* hit_list;
+  int32_t* fetch;
+  int32_t* victims;
+  int32_t* evicted;
+  int32_t* cpu_list;
+  int32_t* counts;
+  int32_t* group_slot;
+  int32_t* group_off;
+  int32_t* group_routes;
+};
+
+// Shared memory the control kernel needs for S slots.
+size_t control_smem_bytes(int S);
+cudaError_t launch_control(const ControlArgs& a, cudaStream_t st);
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, uint32_t* status,
+                         int32_t* hist, cudaStream_t st);
+
+// Fill: copy counts[3] experts fetch[i] (global ids, pool offset id*Bx) into
+// arena slot victims[i].
+cudaError_t launch_fill(const uint8_t* pool_dev, uint8_t* arena, const int32_t* counts, const int32_t* fetch,
+                        const int32_t* victims, size_t Bx, int S, int E_tot, uint32_t* status, int grid,
+                        cudaStream_t st);
+
+struct DecodeArgs {
+  const uint8_t* arena;  // slot s at arena + s*Bx
+  size_t Bx;
+  int S, d, f, k, dtype;
+  int max_groups;
+  const int32_t* counts;
+  const int32_t* group_slot;
+  const int32_t* group_off;
+  const int32_t* group_routes;
+  const uint16_t* hidden;  // [T, d] bf16
+  float* ypart;            // [T*k][f/kDecodeChunk][d]
+  uint32_t* status;
+};
+cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st);
+
+// out[t] = partial[t] + sum_j [slot_ids >= 0] w[t,j] * sum_c ypart[t*k+j][c]
+cudaError_t launch_merge(const float* ypart, int n_chunks, const int32_t* slot_ids, const float* w,
+                         const float* partial, float* out, int T, int k, int d, cudaStream_t st);
+
+}  // namespace ft

@@ -1,0 +1,209 @@
+/*
+ * ft_moe.h -- C ABI of the GB300 MoE expert-cache layer step.
+ *
+ * The operation is one MoE layer of FreeToken-style edge-native serving
+ * ("FreeToken: Efficient Edge-Native MoE Serving with Bandwidth-Adaptive
+ * Execution", summarised on theainews.cc, 2026-08-22-freetoken-edge-moe):
+ * the full expert pool lives in pinned host memory and is the source of
+ * truth; one device-resident cache of expert slots is shared by every MoE
+ * layer (section "设计：三大机制", intro).  Per layer step:
+ *
+ *   routes     top-k of E routed experts per token (section "为什么个人跑 MoE
+ *              这么难"; routing stays exact, section "与相关工作").
+ *   control    dedup, classify hits/misses against a device residency table,
+ *              split the m misses by q* ~ m*BP/BH between GPU fill and an
+ *              external (CPU) partial sum, pick K least-recently-used victim
+ *              slots in one scan, rewrite logical expert ids to slot ids --
+ *              one kernel with fixed-shape buffers and device-resident counts
+ *              so the step can be captured in a CUDA graph (section "实现要点",
+ *              first bullet; "设计 1" Decode bullet).
+ *   fill       copy the q fetched experts from the host pool into their slots
+ *              on a side stream (Decode bullet).
+ *   prefill    full-layer double buffer: while layer l computes, a transfer
+ *              stream uploads all experts of layer l+1 (Prefill bullet).
+ *   experts    routed SwiGLU FFNs, weighted and summed per token, plus an exact
+ *              merge of a caller-supplied partial sum (Decode bullet: CPU and
+ *              GPU partial sums merge exactly).
+ *
+ * Conventions
+ *  - Every call returns FT_OK (0) or a negative FT_E_* code; ft_last_error()
+ *    returns the calling thread's last message.  Argument errors are found on
+ *    the host before anything is launched.  Faults found on the device (a
+ *    route id outside [0, E), a NaN logit, the step clock about to wrap) set
+ *    bits in a device status word read by ft_get_status(); the step still
+ *    completes with the offending route treated as absent.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *    Calls enqueue work and never synchronise unless stated.
+ *  - Device pointers (suffix _dev) are owned by the caller unless stated.
+ *    Pointers returned in ft_step_out are owned by the context.
+ *  - bf16 values are passed as their 16-bit patterns (uint16_t).
+ *
+ * Canonical host pool layout (the "final runtime layout" the page has the
+ * loader write before pinning, section "设计 3" fast start):
+ *  expert (l, e) starts at byte (l*E + e) * B_x;
+ *  bf16   expert: [W_gate f x d | W_up f x d | W_down d x f], row-major,
+ *         B_x = 6*d*f;
+ *  mxfp4  expert: [codes gate f*d/2 | codes up | codes down d*f/2 |
+ *         scales gate f*d/32 | scales up | scales down d*f/32];
+ *         two e2m1 codes per byte, element 2i in the low nibble; one e8m0
+ *         scale byte per 32 consecutive elements of a row (OCP MX v1.0).
+ *         B_x = 3*d*f/2 + 3*d*f/32.
+ */
+#ifndef FT_MOE_H
+#define FT_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define FT_OK 0
+#define FT_E_ARG -1         /* bad argument (checked on the host) */
+#define FT_E_PIN -2         /* the host pool could not be pinned/mapped */
+#define FT_E_NOMEM -3       /* device allocation failed */
+#define FT_E_CUDA -4        /* a CUDA runtime call failed */
+#define FT_E_STATE -5       /* call not allowed now (e.g. during stream capture) */
+#define FT_E_UNSUPPORTED -6 /* shape or mode not built into this library */
+
+/* device status bits (ft_get_status) */
+#define FT_ST_ROUTE_RANGE 1u /* a route id was outside [0, E) */
+#define FT_ST_NAN 2u         /* a router logit was NaN */
+#define FT_ST_CLOCK_WRAP 4u  /* the LRU step clock reached 2^32 - 1 */
+#define FT_ST_BAD_SLOT 8u    /* a slot id outside [0, S) reached a kernel */
+
+#define FT_DTYPE_BF16 0
+#define FT_DTYPE_MXFP4 1
+
+#define FT_DECODE_CACHED 0 /* experts from the shared cache, after ft_cache_step */
+#define FT_PREFILL_LAYER 1 /* experts from the full-layer buffers */
+
+#define FT_FILL_KERNEL 0      /* SM copy from the mapped pool; graph capturable */
+#define FT_FILL_COPY_ENGINE 1 /* cudaMemcpyAsync per expert; reads the fetch list back (host sync) */
+
+typedef struct ft_config {
+  int32_t num_layers;    /* L: MoE layers sharing the cache */
+  int32_t num_experts;   /* E: routed experts per layer (<= 1024) */
+  int32_t top_k;         /* k: experts per token (<= 32, <= E) */
+  int32_t hidden;        /* d (multiple of 256) */
+  int32_t inter;         /* f: expert intermediate size (multiple of 128) */
+  int32_t dtype;         /* FT_DTYPE_BF16 or FT_DTYPE_MXFP4 */
+  int32_t num_slots;     /* S: cache slots (<= 32768) */
+  int32_t k_max;         /* K_max: fixed victim-buffer size (1..1024) */
+  int32_t t_max;         /* tokens per decode/control step (1..1024) */
+  int32_t r_num, r_den;  /* r = BP/BH as a rational, r_num >= 0, r_den >= 1 */
+  int32_t prefill_buffers; /* 0: no prefill; 1: one layer buffer (no overlap); 2: double buffer */
+  int32_t prefill_t_max; /* tokens per prefill chunk (0 if no prefill) */
+  int32_t fill_mode;     /* FT_FILL_KERNEL or FT_FILL_COPY_ENGINE */
+  int32_t reserved[4];   /* must be zero */
+} ft_config;
+
+/* Per-layer results of ft_cache_step / ft_cache_control.  All pointers are
+ * device memory owned by the context and stay valid (and unchanged) until the
+ * next step of the same layer or ft_cache_rebuild.  Sizes are fixed
+ * capacities; the valid lengths are in counts. */
+typedef struct ft_step_out {
+  int32_t* ids;       /* [T, k] local expert ids, logit-descending per token */
+  float* weights;     /* [T, k] routing weights (softmax renormalised over the k) */
+  int32_t* slot_ids;  /* [T, k] cache slot of each route, -1 = CPU route */
+  int32_t* uniq;      /* [E] unique global expert ids (layer*E + e), ascending */
+  int32_t* hit_list;  /* [E] unique ids that hit, ascending */
+  int32_t* fetch;     /* [K_max] filled global expert ids, ascending */
+  int32_t* victims;   /* [K_max] slot receiving fetch[i] */
+  int32_t* evicted;   /* [K_max] expert that victims[i] held before, -1 if empty */
+  int32_t* cpu_list;  /* [E] misses left to the CPU, ascending */
+  int32_t* counts;    /* [8] n, hits, m, q, cpu, n_groups, now, 0 */
+} ft_step_out;
+
+typedef struct ft_ctx ft_ctx;
+
+/* Create a context on the current device.  host_pool holds num_layers *
+ * num_experts experts in the canonical layout, already written by the caller
+ * (pool_bytes >= L*E*B_x); the library registers it as mapped pinned memory
+ * (pin after write) and unregisters it in ft_moe_destroy -- the caller keeps
+ * ownership and must keep it alive.  If the range is already pinned it is
+ * used as is.  Allocates the slot arena (S*B_x bytes), the residency table,
+ * fixed-shape work buffers and, if prefill_buffers > 0, the layer buffers.
+ * The cache starts cold: every slot empty, clock 0.
+ * Errors: FT_E_ARG, FT_E_PIN (no fallback), FT_E_NOMEM, FT_E_CUDA. */
+int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx** out);
+
+/* Free everything the context allocated and unregister the pool.  Waits for
+ * the context's streams.  NULL is accepted. */
+int ft_moe_destroy(ft_ctx* ctx);
+
+/* Routing + cache control for one decode step of `layer`: logits_dev is
+ * [T, E] float32 row-major, 1 <= T <= t_max.  Enqueues the routing kernel and
+ * the control kernel on `stream`; no host synchronisation, so the call can be
+ * captured in a CUDA graph (shapes are fixed by T).  The step clock advances
+ * by one per call.  `out` (may be NULL) receives the context's buffers. */
+int ft_cache_step(ft_ctx* ctx, int layer, const float* logits_dev, int T, ft_step_out* out, void* stream);
+
+/* The control kernel alone, on routes the caller supplies: ids_dev is [T, k]
+ * local expert ids (each token's ids distinct).  Weights are left untouched. */
+int ft_cache_control(ft_ctx* ctx, int layer, const int32_t* ids_dev, int T, ft_step_out* out, void* stream);
+
+/* Expert FFNs of one layer.
+ *  mode FT_DECODE_CACHED: uses the last ft_cache_step of `layer` (same T);
+ *    fills the q fetched experts into their slots on the context's transfer
+ *    stream, joined back into `stream`, then runs the routed SwiGLU experts
+ *    of every route with a slot and merges:
+ *      out[t] = partial[t] + sum_j w[t,j] * y_{ids[t,j]}(hidden[t])   (slot >= 0)
+ *    logits_dev is ignored.
+ *  mode FT_PREFILL_LAYER: routes logits_dev itself (no cache access; the
+ *    residency table is untouched), waits for layer `layer` in its layer
+ *    buffer (uploading it first if it is not there), runs all routes, and --
+ *    with prefill_buffers == 2 -- starts the upload of layer+1 into the other
+ *    buffer before returning.  T <= prefill_t_max.
+ *  hidden_dev [T, d] bf16; partial_dev [T, d] float32 or NULL (= 0);
+ *  out_dev [T, d] float32, written (not accumulated).
+ * Never synchronises (except FT_FILL_COPY_ENGINE, which reads the fetch list
+ * back and so cannot be captured). */
+int ft_moe_forward(ft_ctx* ctx, int layer, int mode, const float* logits_dev, const uint16_t* hidden_dev,
+                   int T, const float* partial_dev, float* out_dev, void* stream);
+
+/* Rebuild the cache with new_slots slots under a revised memory budget
+ * ("设计 3" runtime cache rebuild): only at a safe point -- the caller's
+ * streams idle, no capture in progress (FT_E_STATE otherwise).  Frees and
+ * reallocates the slot arena and resets the residency table to cold; the
+ * host pool stays pinned.  CUDA graphs captured earlier must be recaptured:
+ * the epoch (ft_get_epoch) increases by one.  Synchronises the device. */
+int ft_cache_rebuild(ft_ctx* ctx, int new_slots);
+
+/* Read (and clear, if clear != 0) the device status word; synchronises the
+ * context's streams. */
+int ft_get_status(ft_ctx* ctx, uint32_t* status, int clear);
+
+/* Per-layer counters since init/rebuild, summed over steps, copied to the
+ * host array counters[L][6] = {hits, misses, fills, cpu routes, evictions,
+ * steps}.  Synchronises. */
+int ft_get_counters(ft_ctx* ctx, uint64_t* counters);
+
+/* Copy the residency table to host arrays (any may be NULL): slot_of[L*E],
+ * expert_of[S], last_use[S], now[1].  Synchronises.  For tests and tools. */
+int ft_get_table(ft_ctx* ctx, int32_t* slot_of, int32_t* expert_of, uint32_t* last_use, uint32_t* now);
+
+/* Device pointer of slot s's bytes in the arena (for tests), or NULL. */
+void* ft_slot_ptr(ft_ctx* ctx, int slot);
+
+/* Cache epoch: starts at 0, +1 per ft_cache_rebuild. */
+int ft_get_epoch(ft_ctx* ctx);
+
+/* Current slot count S. */
+int ft_num_slots(ft_ctx* ctx);
+
+/* Standalone routing kernel (no context): logits_dev [T, E] float32 ->
+ * ids_dev [T, k] int32 and w_dev [T, k] float32; status_dev (may be NULL) is
+ * a device uint32 that receives FT_ST_NAN bits.  E <= 1024, k <= 32. */
+int ft_route(const float* logits_dev, int T, int E, int k, int32_t* ids_dev, float* w_dev, uint32_t* status_dev,
+             void* stream);
+
+/* Message of the calling thread's last error ("" if none). */
+const char* ft_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FT_MOE_H */

@@ -1,0 +1,227 @@
+"""GPU parity of the decode path against the oracle, through the C ABI.
+
+Control state (routes, unique/hit/miss lists, fetch set, victims, evicted
+experts, rewritten slot ids, the whole residency table and clock) must match
+bit for bit after every step; expert outputs within max relative error 2e-2
+and normwise 5e-3 of the fp64 oracle.
+"""
+import numpy as np
+import pytest
+
+import ftsynth
+import oracle
+from harness import (check_output, compare_step, compare_table, dev_view, make_model, step_to_host)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def ft():
+    from expert_cache_host_gb300 import build as ftbuild
+    ftbuild.build()
+    import expert_cache_host_gb300 as lib
+    lib.load()
+    return lib
+
+
+# ------------------------------------------------------------------ routing
+
+@pytest.mark.parametrize("T,E,k", [(1, 16, 2), (64, 128, 8), (100, 256, 6), (33, 1000, 32), (5, 7, 7)])
+def test_route_parity(ft, T, E, k):
+    rng = np.random.default_rng(T * 7 + E)
+    lg = ftsynth.test_logits(11, E, T, E)
+    # plant ties and signed zeros
+    lg[:, ::3] = np.round(lg[:, ::3] * 2) / 2
+    lg[0, :min(E, 4)] = 0.0
+    if E > 5:
+        lg[0, 5] = -0.0
+    ref_ids, ref_w = oracle.route(lg, k)
+    d_lg = torch.from_numpy(lg).cuda()
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ft.ft_route(d_lg.data_ptr(), T, E, k, ids.data_ptr(), w.data_ptr(), st.data_ptr())
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-7)
+    assert int(st.item()) == 0
+
+
+def test_route_nan_sets_status(ft):
+    lg = np.zeros((3, 16), dtype=np.float32)
+    lg[1, 4] = np.nan
+    d_lg = torch.from_numpy(lg).cuda()
+    ids = torch.empty((3, 2), dtype=torch.int32, device="cuda")
+    w = torch.empty((3, 2), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ft.ft_route(d_lg.data_ptr(), 3, 16, 2, ids.data_ptr(), w.data_ptr(), st.data_ptr())
+    torch.cuda.synchronize()
+    assert int(st.item()) & ft.FT_ST_NAN
+
+
+# ------------------------------------------------------------------ decode steps
+
+def run_decode(ft, model, S, K_max, r, steps, T=1, fill_mode=0, check_every=1, out_tokens=None, rho=0.9,
+               rebuild_at=None, graph=False):
+    """Decode `steps` steps over all layers through the library and the oracle
+    side by side; compare control state every step and outputs every
+    `check_every` steps."""
+    L, E, k, d, f = model.L, model.E, model.k, model.d, model.f
+    cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, dtype=model.dtype, num_slots=S,
+                         k_max=K_max, t_max=T, r_num=r[0], r_den=r[1], fill_mode=fill_mode)
+    ctx = ft.ft_moe_init(cfg, model.pool.ctypes.data, model.pool.nbytes)
+    try:
+        cache = oracle.Cache(L * E, S)
+        hid = np.stack([np.stack([ftsynth.ar1_hidden(model.seed, l, b, steps, d, rho) for b in range(T)], axis=1)
+                        for l in range(L)], axis=1)  # [steps, L, T, d]
+        logits = np.stack([ftsynth.router_logits(hid[:, l], model.wr[l]) for l in range(L)], axis=1)  # [steps,L,T,E]
+        d_hid = torch.from_numpy(hid.view(np.int16)).cuda()
+        d_lg = torch.from_numpy(logits).cuda()
+        out = torch.empty((T, d), dtype=torch.float32, device="cuda")
+        partial = torch.empty((T, d), dtype=torch.float32, device="cuda")
+        stream = torch.cuda.current_stream().cuda_stream
+        worst = (0.0, 0.0)
+        for s in range(steps):
+            if rebuild_at is not None and s == rebuild_at[0]:
+                ft.ft_cache_rebuild(ctx, rebuild_at[1])
+                cache = oracle.Cache(L * E, rebuild_at[1])
+                S = rebuild_at[1]
+            for l in range(L):
+                res = ft.ft_cache_step(ctx, l, d_lg[s, l].data_ptr(), T, stream)
+                ref_ids, ref_w = oracle.route(logits[s, l], k)
+                ref = cache.step(l, E, ref_ids, r[0], r[1], K_max)
+                torch.cuda.synchronize()
+                g = step_to_host(res, T, k, E, K_max)
+                where = f"step {s} layer {l}"
+                assert np.array_equal(g["ids"], ref_ids), where
+                np.testing.assert_allclose(g["w"], ref_w, rtol=2e-6, atol=1e-7)
+                compare_step(g, ref, where)
+                check = (s % check_every == 0)
+                if check:
+                    full, gpu_part, cpu_part = oracle.moe_forward(model.layer_pool(l), model.bx, model.dtype, d, f,
+                                                                  ref_ids, ref_w, hid[s, l],
+                                                                  slot_ids=ref.slot_ids.reshape(T, k))
+                    partial.copy_(torch.from_numpy(cpu_part.astype(np.float32)))
+                else:
+                    partial.zero_()
+                ft.ft_moe_forward(ctx, l, ft.FT_DECODE_CACHED, 0, d_hid[s, l].data_ptr(), T, partial.data_ptr(),
+                                  out.data_ptr(), stream)
+                torch.cuda.synchronize()
+                if check:
+                    y = out.cpu().numpy().astype(np.float64)
+                    mr, nw = check_output(y, full, where)
+                    worst = (max(worst[0], mr), max(worst[1], nw))
+            compare_table(ft, ctx, cache, f"after step {s}")
+        assert ft.ft_get_status(ctx) == 0
+        return ctx, cache, worst
+    except Exception:
+        ft.ft_moe_destroy(ctx)
+        raise
+
+
+def test_tiny_decode_all_fill(ft):
+    """1 layer, d=256, E=16, top-2, f=128, 8 slots, BP/BH = 1, 32 steps."""
+    model = make_model(1, 16, 2, 256, 128, seed=0)
+    ctx, cache, worst = run_decode(ft, model, S=8, K_max=16, r=(1, 1), steps=32)
+    cnt = ft.ft_get_counters(ctx, 1)
+    assert cnt[0, 5] == 32 and cnt[0, 3] == 0  # all misses filled at r = 1
+    ft.ft_moe_destroy(ctx)
+
+
+@pytest.mark.parametrize("r,K_max", [((1, 2), 16), ((1, 1), 1), ((0, 1), 4)])
+def test_tiny_decode_cpu_split(ft, r, K_max):
+    """Misses left to the CPU arrive as an external partial sum and merge exactly."""
+    model = make_model(2, 16, 2, 256, 128, seed=1)
+    ctx, cache, worst = run_decode(ft, model, S=6, K_max=K_max, r=r, steps=20)
+    cnt = ft.ft_get_counters(ctx, 2)
+    assert cnt[:, 3].sum() > 0  # some routes did go to the CPU
+    ft.ft_moe_destroy(ctx)
+
+
+def test_tiny_decode_copy_engine_fill(ft):
+    model = make_model(2, 16, 2, 256, 128, seed=2)
+    ctx, _, _ = run_decode(ft, model, S=5, K_max=16, r=(1, 1), steps=12, fill_mode=ft.FT_FILL_COPY_ENGINE)
+    ft.ft_moe_destroy(ctx)
+
+
+def test_batch16_decode_groups(ft):
+    """16 tokens per step: tokens share experts, so groups hold several routes."""
+    model = make_model(2, 16, 4, 256, 256, seed=3)
+    ctx, _, _ = run_decode(ft, model, S=12, K_max=8, r=(1, 1), steps=6, T=16)
+    ft.ft_moe_destroy(ctx)
+
+
+def test_rebuild_mid_run(ft):
+    """A rebuild at a safe point resets the cache cold at the new size; the
+    results stay equal to a fresh oracle cache of that size."""
+    model = make_model(2, 16, 2, 256, 128, seed=4)
+    ctx, cache, _ = run_decode(ft, model, S=8, K_max=16, r=(1, 1), steps=10, rebuild_at=(5, 3))
+    assert ft.ft_get_epoch(ctx) == 1 and ft.ft_num_slots(ctx) == 3
+    ft.ft_moe_destroy(ctx)
+
+
+def test_ragged_shapes_and_larger_model(ft):
+    """d=2048, f=768 (24 chunks), E=128, top-8: the A3B expert shape, 3 layers."""
+    model = make_model(3, 128, 8, 2048, 768, seed=5)
+    ctx, _, worst = run_decode(ft, model, S=20, K_max=128, r=(1, 2), steps=4)
+    ft.ft_moe_destroy(ctx)
+
+
+# ------------------------------------------------------------------ control alone
+
+@pytest.mark.parametrize("S,K_max,r,s_zipf", [(64, 64, (1, 1), 1.2), (40, 8, (1, 2), 0.6), (300, 512, (1, 1), 0.6),
+                                                (6144, 128, (1, 1), 1.2)])
+def test_control_zipf_stress_small(ft, S, K_max, r, s_zipf):
+    """The control kernel alone on Zipf route streams: 64 tokens x top-8 x E=128."""
+    L, E, k, T, steps = 4, 128, 8, 64, 25
+    d, f = 256, 128  # the control path never reads expert bytes: smallest legal expert shape
+    bx = ftsynth.expert_bytes(d, f, 0)
+    pool = np.zeros(L * E * bx, dtype=np.uint8)
+    cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, num_slots=S, k_max=K_max,
+                         t_max=T, r_num=r[0], r_den=r[1])
+    ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
+    routes = np.stack([ftsynth.zipf_routes(0, l, E, T, k, s_zipf, 0, steps, threads=4) for l in range(L)], axis=1)
+    d_routes = torch.from_numpy(routes).cuda()
+    cache = oracle.Cache(L * E, S)
+    stream = torch.cuda.current_stream().cuda_stream
+    for s in range(steps):
+        for l in range(L):
+            res = ft.ft_cache_control(ctx, l, d_routes[s, l].data_ptr(), T, stream)
+            ref = cache.step(l, E, routes[s, l], r[0], r[1], K_max)
+            torch.cuda.synchronize()
+            compare_step(step_to_host(res, T, k, E, K_max), ref, f"step {s} layer {l}")
+        compare_table(ft, ctx, cache, f"after step {s}")
+    assert ft.ft_get_status(ctx) == 0
+    ft.ft_moe_destroy(ctx)
+
+
+def test_control_out_of_range_route_sets_status(ft):
+    L, E, k, T, S = 1, 16, 2, 2, 4
+    d, f = 256, 128
+    pool = np.zeros(L * E * ftsynth.expert_bytes(d, f, 0), dtype=np.uint8)
+    cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, num_slots=S, t_max=T)
+    ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
+    ids = torch.tensor([[1, 99], [2, 3]], dtype=torch.int32, device="cuda")
+    res = ft.ft_cache_control(ctx, 0, ids.data_ptr(), T, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    g = step_to_host(res, T, k, E, 16)
+    assert ft.ft_get_status(ctx, clear=True) & ft.FT_ST_ROUTE_RANGE
+    assert g["slot_ids"][0, 1] == -1 and g["counts"][0] == 3  # the bad route is treated as absent
+    assert ft.ft_get_status(ctx) == 0
+    ft.ft_moe_destroy(ctx)
+
+
+def test_forward_without_step_is_rejected(ft):
+    model = make_model(1, 16, 2, 256, 128, seed=6)
+    cfg = ft.make_config(num_layers=1, num_experts=16, top_k=2, hidden=256, inter=128, num_slots=4)
+    ctx = ft.ft_moe_init(cfg, model.pool.ctypes.data, model.pool.nbytes)
+    out = torch.empty((1, 256), dtype=torch.float32, device="cuda")
+    hid = torch.zeros((1, 256), dtype=torch.int16, device="cuda")
+    with pytest.raises(ft.FtError) as ei:
+        ft.ft_moe_forward(ctx, 0, ft.FT_DECODE_CACHED, 0, hid.data_ptr(), 1, 0, out.data_ptr())
+    assert ei.value.code == ft.FT_E_STATE
+    with pytest.raises(ft.FtError):
+        ft.ft_cache_step(ctx, 3, hid.data_ptr(), 1)  # bad layer
+    ft.ft_moe_destroy(ctx)
