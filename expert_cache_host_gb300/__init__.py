@@ -28,8 +28,10 @@ COUNTS = ("n", "hits", "m", "q", "cpu", "n_groups", "now")
 EXPORTS = (
     "ft_moe_init", "ft_moe_destroy", "ft_cache_step", "ft_cache_control", "ft_moe_forward", "ft_cache_rebuild",
     "ft_get_status", "ft_get_counters", "ft_get_table", "ft_slot_ptr", "ft_get_epoch", "ft_num_slots", "ft_route",
-    "ft_last_error",
+    "ft_profile_enable", "ft_profile_read", "ft_last_error",
 )
+FT_K_ROUTE, FT_K_CONTROL, FT_K_FILL, FT_K_EXPERTS, FT_K_MERGE, FT_K_UPLOAD, FT_K_PREFILL, FT_K_COUNT = 0, 1, 2, 3, 4, 5, 6, 8
+KERNEL_CLASSES = ("route", "control", "fill", "experts", "merge", "upload", "prefill")
 
 
 class FtError(RuntimeError):
@@ -82,6 +84,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "ft_get_epoch": ([vp], i32),
             "ft_num_slots": ([vp], i32),
             "ft_route": ([vp, i32, i32, i32, vp, vp, vp, vp], i32),
+            "ft_profile_enable": ([vp, i32], i32),
+            "ft_profile_read": ([vp, vp, vp, i32], i32),
             "ft_last_error": ([], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -184,6 +188,18 @@ def ft_route(logits_ptr: int, T: int, E: int, k: int, ids_ptr: int, w_ptr: int, 
              stream: int = 0) -> None:
     _chk(load().ft_route(ctypes.c_void_p(logits_ptr), T, E, k, ctypes.c_void_p(ids_ptr), ctypes.c_void_p(w_ptr),
                          ctypes.c_void_p(status_ptr or None), ctypes.c_void_p(stream)))
+
+
+def ft_profile_enable(ctx: int, on: bool = True) -> None:
+    _chk(load().ft_profile_enable(ctypes.c_void_p(ctx), int(on)))
+
+
+def ft_profile_read(ctx: int, reset: bool = True) -> dict:
+    """{class name: (total ms, launches)} recorded since the last reset."""
+    ms = (ctypes.c_double * FT_K_COUNT)()
+    n = (ctypes.c_uint64 * FT_K_COUNT)()
+    _chk(load().ft_profile_read(ctypes.c_void_p(ctx), ms, n, int(reset)))
+    return {name: (ms[i], int(n[i])) for i, name in enumerate(KERNEL_CLASSES)}
 
 
 def ft_last_error() -> str:

@@ -1,42 +1,48 @@
 // Decode expert kernel: routed SwiGLU experts for a few tokens, HBM-bound.
 //
 // For every resident expert of the step (a "group": the routes that chose it,
-// built by the control kernel) and every chunk c of kDecodeChunk rows of the
+// built by the control kernel) and every chunk c of FC = 32 rows of the
 // intermediate dimension f, one CTA computes
 //     h[t, i] = silu(W_gate[i] . x_t) * (W_up[i] . x_t)        i in chunk c
 //     ypart[route(t), c, :] = W_down[:, chunk c] . h[t, chunk c]
 // with fp32 accumulation.  Splitting f this way needs no grid-wide barrier
-// between the gate/up and down projections; the per-chunk partial sums are
+// between the gate/up and the down projection; the per-chunk partial sums are
 // reduced in a fixed order by the merge kernel, so results are deterministic.
-// Weights are read once per step with 16-byte coalesced loads (gate/up rows
-// are d-contiguous; a down chunk is 2*kDecodeChunk contiguous bytes per row).
-// The page's activation is not named; SwiGLU is the one of the served models
-// (FreeToken article, section "核心亮点": Qwen3.6-35B-A3B, DeepSeek-V4-Flash).
+//
+// Data movement (warp-specialised): a producer warp streams the CTA's weights
+// through a ring of NS 16 KB shared-memory stages with the Tensor Memory
+// Accelerator, each stage guarded by a "full" mbarrier (TMA transaction
+// bytes) and an "empty" mbarrier (one arrival per consumer warp).
+//  - gate/up tiles: 32 rows x 256 columns boxes of a 4-D tensor map over the
+//    arena (d, f, {gate, up}, slot); a consumer thread owns one row and 16
+//    columns of every column block, so it accumulates its row over all blocks
+//    in registers and one 16-lane reduction per row finishes the dot product;
+//  - down tiles: 256 rows x 32 columns boxes of a 3-D map (f, d, slot).
+// The ring runs from the gate/up tiles straight into the down tiles.  Every
+// mbarrier wait is bounded; a wait that runs out records FT_ST_TIMEOUT and
+// the kernel carries on to a bounded drain, so it always terminates.
+// The page's activation is not named; SwiGLU is the one of the served model
+// families (FreeToken article, section "核心亮点").
 #include <math.h>
 
 #include "ft_internal.h"
+#include "tma.h"
 
 namespace ft {
 namespace {
 
-constexpr int FC = kDecodeChunk;        // 32 rows of f per CTA
-constexpr int kThreads = 256;           // 8 warps
-constexpr int kRowsPerWarp = FC / 8;    // 4
-constexpr int kTokBatch = 4;            // tokens per pass over the weights
-
-__device__ __forceinline__ int4 ldg_stream(const void* p) {
-  int4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
+constexpr int FC = kDecodeChunk;           // 32 rows of f per CTA
+constexpr int kConsumers = 512;            // 16 consumer warps
+constexpr int kThreads = kConsumers + 32;  // + 1 producer warp
+constexpr int kTokBatch = 4;               // tokens per pass over the weights
+constexpr int NS = 5;                      // ring stages
+constexpr int kTile = 16384;               // bytes per stage
 
 __device__ __forceinline__ float bf_lo(unsigned v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(unsigned v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-__device__ __forceinline__ float dot8(const int4 w, const int4 x) {
-  float s = bf_lo(w.x) * bf_lo(x.x);
+__device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float s) {
+  s = fmaf(bf_lo(w.x), bf_lo(x.x), s);
   s = fmaf(bf_hi(w.x), bf_hi(x.x), s);
   s = fmaf(bf_lo(w.y), bf_lo(x.y), s);
   s = fmaf(bf_hi(w.y), bf_hi(x.y), s);
@@ -47,142 +53,242 @@ __device__ __forceinline__ float dot8(const int4 w, const int4 x) {
   return s;
 }
 
-__device__ __forceinline__ float dot8h(const int4 w, const float* h) {
-  float s = bf_lo(w.x) * h[0];
-  s = fmaf(bf_hi(w.x), h[1], s);
-  s = fmaf(bf_lo(w.y), h[2], s);
-  s = fmaf(bf_hi(w.y), h[3], s);
-  s = fmaf(bf_lo(w.z), h[4], s);
-  s = fmaf(bf_hi(w.z), h[5], s);
-  s = fmaf(bf_lo(w.w), h[6], s);
-  s = fmaf(bf_hi(w.w), h[7], s);
+__device__ __forceinline__ float dot8h(const uint4 w, const float4 h0, const float4 h1, float s) {
+  s = fmaf(bf_lo(w.x), h0.x, s);
+  s = fmaf(bf_hi(w.x), h0.y, s);
+  s = fmaf(bf_lo(w.y), h0.z, s);
+  s = fmaf(bf_hi(w.y), h0.w, s);
+  s = fmaf(bf_lo(w.z), h1.x, s);
+  s = fmaf(bf_hi(w.z), h1.y, s);
+  s = fmaf(bf_lo(w.w), h1.z, s);
+  s = fmaf(bf_hi(w.w), h1.w, s);
   return s;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads) decode_bf16_kernel(DecodeArgs a) {
-  extern __shared__ __align__(16) unsigned char dyn[];
-  const int d = a.d, f = a.f;
-  uint16_t* xs = reinterpret_cast<uint16_t*>(dyn);                        // [kTokBatch][d]
-  float* hs = reinterpret_cast<float*>(dyn + (size_t)kTokBatch * d * 2);  // [kTokBatch][FC]
-  int* rs = reinterpret_cast<int*>(hs + kTokBatch * FC);                  // [kTokBatch] routes
+struct Layout {
+  size_t ring, full, empty, xs, gu, hs, rs, total;
+};
 
-  const int c = blockIdx.x, g = blockIdx.y;
+__host__ __device__ inline Layout smem_layout(int d) {
+  Layout L{};
+  L.ring = 0;
+  L.full = L.ring + (size_t)NS * kTile;
+  L.empty = L.full + 8 * NS;
+  L.xs = (L.empty + 8 * NS + 15) / 16 * 16;
+  L.gu = L.xs + (size_t)kTokBatch * d * 2;           // [2][FC][kTokBatch] row sums
+  L.hs = L.gu + sizeof(float) * 2 * FC * kTokBatch;  // [kTokBatch][FC]
+  L.rs = L.hs + sizeof(float) * kTokBatch * FC;      // [kTokBatch]
+  L.total = L.rs + sizeof(int) * kTokBatch;
+  return L;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_bf16_kernel(const __grid_constant__ CUtensorMap tmap_gu, const __grid_constant__ CUtensorMap tmap_wd,
+                       DecodeArgs a) {
+  extern __shared__ __align__(1024) unsigned char dyn[];
+  const int d = a.d, f = a.f;
+  const Layout Ly = smem_layout(d);
+  unsigned char* ring = dyn + Ly.ring;
+  uint64_t* full = reinterpret_cast<uint64_t*>(dyn + Ly.full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(dyn + Ly.empty);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(dyn + Ly.xs);  // [kTokBatch][d]
+  float* gu = reinterpret_cast<float*>(dyn + Ly.gu);        // [2][FC][kTokBatch]
+  float* hs = reinterpret_cast<float*>(dyn + Ly.hs);        // [kTokBatch][FC]
+  int* rs = reinterpret_cast<int*>(dyn + Ly.rs);            // [kTokBatch]
+
+  const int c = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
   if (g >= a.counts[5]) return;
   const int slot = a.group_slot[g];
   if ((unsigned)slot >= (unsigned)a.S) {
-    if (threadIdx.x == 0) atomicOr(a.status, FT_ST_BAD_SLOT);
+    if (tid == 0) atomicOr(a.status, FT_ST_BAD_SLOT);
     return;
   }
   const int r0 = a.group_off[g], r1 = a.group_off[g + 1];
-  const size_t df = (size_t)d * f;
-  const uint16_t* Wg = reinterpret_cast<const uint16_t*>(a.arena + (size_t)slot * a.Bx);
-  const uint16_t* Wu = Wg + df;
-  const uint16_t* Wd = Wg + 2 * df;
-  const int n_chunks = f / FC;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int nit = d / 256;
+  const int n_batches = (r1 - r0 + kTokBatch - 1) / kTokBatch;
+  const int cb_n = d / 256;           // column blocks per gate (or up) matrix
+  const int P1 = 2 * cb_n;            // gate/up tiles per batch
+  const int NTL = P1 + d / 256;       // + down tiles (256 rows each)
+  const int total = n_batches * NTL;  // tiles over all token batches
 
-  for (int tb = r0; tb < r1; tb += kTokBatch) {
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers / 32);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (tid >= kConsumers) {
+    // ---------------- producer warp ----------------
+    if (tid == kConsumers) {
+      bool late = false;
+      int s = 0;
+      uint32_t ph = 0;
+      for (int n = 0, i = 0; n < total; ++n) {
+        if (n >= NS && !mbar_wait(&empty[s], ph ^ 1u)) late = true;
+        unsigned char* dst = ring + s * kTile;
+        mbar_expect_tx(&full[s], kTile);
+        if (i < P1) {
+          const int m = i < cb_n ? 0 : 1, cb = i - m * cb_n;
+          tensor_g2s_4d(dst, &tmap_gu, cb * 256, c * FC, m, slot, &full[s]);
+        } else {
+          tensor_g2s_3d(dst, &tmap_wd, c * FC, (i - P1) * 256, slot, &full[s]);
+        }
+        if (++i == NTL) i = 0;
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      // drain: the last use of every stage must have landed before the CTA exits
+      for (int k = 0; k < NS && k < total; ++k) {
+        const int n = total - 1 - k;
+        if (!mbar_wait(&full[n % NS], (uint32_t)((n / NS) & 1))) late = true;
+      }
+      if (late) atomicOr(a.status, FT_ST_TIMEOUT);
+    }
+    return;
+  }
+
+  // ---------------- consumer warps ----------------
+  const int lane = tid & 31;
+  // gate/up tile (32 rows x 512 B): thread = row rl, columns 8cq..8cq+7 and 128+8cq..
+  // down tile (256 rows x 64 B): thread = quarter q of rows tid/4 and 128 + tid/4
+  // (lanes of a quarter-warp read 128 contiguous bytes: no bank conflicts)
+  const int rl = tid >> 4, cq = tid & 15;
+  const int rowq = tid >> 2, q = tid & 3;
+  const int n_chunks = f / FC;
+  bool late = false;
+  int s = 0;
+  uint32_t ph = 0;
+  auto release = [&]() {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (++s == NS) {
+      s = 0;
+      ph ^= 1u;
+    }
+  };
+
+  for (int b = 0; b < n_batches; ++b) {
+    const int tb = r0 + b * kTokBatch;
     const int nt = min(kTokBatch, r1 - tb);
-    __syncthreads();  // xs/hs reuse
-    if (threadIdx.x < nt) rs[threadIdx.x] = a.group_routes[tb + threadIdx.x];
+    consumer_sync();  // previous batch done with xs / rs / hs
+    if (tid < nt) rs[tid] = a.group_routes[tb + tid];
     for (int t = 0; t < nt; ++t) {
       const int tok = a.group_routes[tb + t] / a.k;
-      const int4* src = reinterpret_cast<const int4*>(a.hidden + (size_t)tok * d);
-      int4* dst = reinterpret_cast<int4*>(xs + (size_t)t * d);
-      for (int i = threadIdx.x; i < d / 8; i += kThreads) dst[i] = src[i];
+      const uint4* src = reinterpret_cast<const uint4*>(a.hidden + (size_t)tok * d);
+      uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)t * d);
+      for (int i = tid; i < d / 8; i += kConsumers) dst[i] = src[i];
     }
-    __syncthreads();
+    consumer_sync();
 
-    // gate/up rows of this chunk: warp wid owns rows wid + 8*rr
-    float ag[kRowsPerWarp][kTokBatch], au[kRowsPerWarp][kTokBatch];
+    float acc[2][kTokBatch];
 #pragma unroll
-    for (int rr = 0; rr < kRowsPerWarp; ++rr)
+    for (int m = 0; m < 2; ++m)
 #pragma unroll
-      for (int t = 0; t < kTokBatch; ++t) ag[rr][t] = au[rr][t] = 0.f;
-    const size_t row0 = (size_t)c * FC + wid;
-    for (int it = 0; it < nit; ++it) {
-      const int col = it * 256 + lane * 8;
-      int4 wg[kRowsPerWarp], wu[kRowsPerWarp];
+      for (int t = 0; t < kTokBatch; ++t) acc[m][t] = 0.f;
+
+    // gate (m = 0) then up (m = 1) column blocks
 #pragma unroll
-      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-        wg[rr] = ldg_stream(Wg + (row0 + 8 * rr) * d + col);
-        wu[rr] = ldg_stream(Wu + (row0 + 8 * rr) * d + col);
-      }
+    for (int m = 0; m < 2; ++m) {
+#pragma unroll 1
+      for (int cb = 0; cb < cb_n; ++cb) {
+        if (!mbar_wait(&full[s], ph)) late = true;
+        const unsigned char* buf = ring + s * kTile + rl * 512 + cq * 16;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(buf);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(buf + 256);
+        release();
+        const uint16_t* xp = xs + cb * 256 + cq * 8;
 #pragma unroll
-      for (int t = 0; t < kTokBatch; ++t) {
-        if (t < nt) {
-          const int4 x = *reinterpret_cast<const int4*>(xs + (size_t)t * d + col);
-#pragma unroll
-          for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-            ag[rr][t] += dot8(wg[rr], x);
-            au[rr][t] += dot8(wu[rr], x);
+        for (int t = 0; t < kTokBatch; ++t) {
+          if (t < nt) {
+            const uint4 x0 = *reinterpret_cast<const uint4*>(xp + (size_t)t * d);
+            const uint4 x1 = *reinterpret_cast<const uint4*>(xp + (size_t)t * d + 128);
+            acc[m][t] = dot8(w1, x1, dot8(w0, x0, acc[m][t]));
           }
         }
       }
     }
+    // row sums: 16 lanes per row
 #pragma unroll
-    for (int rr = 0; rr < kRowsPerWarp; ++rr)
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int t = 0; t < kTokBatch; ++t) {
+        float v = acc[m][t];
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        if (cq == 0 && t < nt) gu[(m * FC + rl) * kTokBatch + t] = v;
+      }
+    consumer_sync();
+    if (tid < FC * kTokBatch) {
+      const int row = tid % FC, t = tid / FC;
+      if (t < nt) {
+        const float gs = gu[(0 * FC + row) * kTokBatch + t], us = gu[(1 * FC + row) * kTokBatch + t];
+        hs[t * FC + row] = gs / (1.f + expf(-gs)) * us;
+      }
+    }
+    consumer_sync();
+
+    // down projection: 256 rows per tile, 4 threads per row, 2 rows per thread
+#pragma unroll 1
+    for (int j = 0; j < d / 256; ++j) {
+      if (!mbar_wait(&full[s], ph)) late = true;
+      const unsigned char* buf = ring + s * kTile + tid * 16;
+      const uint4 w0 = *reinterpret_cast<const uint4*>(buf);
+      const uint4 w1 = *reinterpret_cast<const uint4*>(buf + 8192);
+      release();
 #pragma unroll
       for (int t = 0; t < kTokBatch; ++t) {
         if (t < nt) {
-          float gs = warp_sum(ag[rr][t]);
-          float us = warp_sum(au[rr][t]);
-          if (lane == 0) hs[t * FC + wid + 8 * rr] = gs / (1.f + expf(-gs)) * us;
-        }
-      }
-    __syncthreads();
-
-    // down projection of this chunk: 4 threads per row of W_down, 64 rows per pass
-    const int quad = threadIdx.x & 3, rowq = threadIdx.x >> 2;
-    float hq[kTokBatch][8];
-#pragma unroll
-    for (int t = 0; t < kTokBatch; ++t)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) hq[t][i] = t < nt ? hs[t * FC + quad * 8 + i] : 0.f;
-    const uint16_t* wdc = Wd + (size_t)c * FC + quad * 8;
-    constexpr int kUnroll = 8;
-    for (int rb = 0; rb < d; rb += 64 * kUnroll) {
-      int4 w[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int r = rb + u * 64 + rowq;
-        w[u] = r < d ? ldg_stream(wdc + (size_t)r * f) : make_int4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int r = rb + u * 64 + rowq;
-#pragma unroll
-        for (int t = 0; t < kTokBatch; ++t) {
-          if (t < nt) {
-            float p = dot8h(w[u], hq[t]);
-            p += __shfl_xor_sync(0xffffffffu, p, 1);
-            p += __shfl_xor_sync(0xffffffffu, p, 2);
-            if (quad == 0 && r < d) a.ypart[((size_t)rs[t] * n_chunks + c) * d + r] = p;
+          const float4* hp = reinterpret_cast<const float4*>(hs + t * FC + q * 8);
+          const float4 h0 = hp[0], h1 = hp[1];
+          float v0 = dot8h(w0, h0, h1, 0.f), v1 = dot8h(w1, h0, h1, 0.f);
+          v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+          v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+          v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+          v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+          if (q == 0) {
+            float* yp = a.ypart + ((size_t)rs[t] * n_chunks + c) * d + j * 256 + rowq;
+            yp[0] = v0;
+            yp[128] = v1;
           }
         }
       }
     }
   }
+  if (late) atomicOr(a.status, FT_ST_TIMEOUT);
 }
 
 }  // namespace
 
+size_t decode_bf16_smem_bytes(int d) { return smem_layout(d).total; }
+
 cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st) {
   if (a.dtype != FT_DTYPE_BF16) return cudaErrorNotSupported;
+  if (a.d > 8192 || a.d % 256 || a.f % FC || !a.tmap_wd || !a.tmap_gu) return cudaErrorInvalidValue;
   dim3 grid(a.f / FC, a.max_groups), block(kThreads);
-  size_t smem = (size_t)kTokBatch * a.d * 2 + kTokBatch * FC * 4 + kTokBatch * 4;
-  if (smem > 48 * 1024) {
+  const size_t smem = decode_bf16_smem_bytes(a.d);
+  static thread_local int configured_dev = -1;
+  static thread_local size_t configured_smem = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev || configured_smem < smem) {
     cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    configured_dev = dev;
+    configured_smem = smem;
   }
-  decode_bf16_kernel<<<grid, block, smem, st>>>(a);
+  decode_bf16_kernel<<<grid, block, smem, st>>>(*a.tmap_gu, *a.tmap_wd, a);
   return cudaGetLastError();
 }
 

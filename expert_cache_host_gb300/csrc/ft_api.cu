@@ -10,6 +10,7 @@
 
 #include "ft_internal.h"
 #include "prefill.h"
+#include "tma.h"
 
 using namespace ft;
 
@@ -53,6 +54,8 @@ struct ft_ctx {
   const uint8_t* pool_dev = nullptr;
 
   uint8_t* arena = nullptr;
+  CUtensorMap tmap_wd{};  // (f, d, slot) view of every slot's W_down, for the decode expert kernel
+  CUtensorMap tmap_gu{};  // (d, f, {gate, up}, slot) view of every slot's W_gate / W_up
   int32_t* slot_of = nullptr;
   int32_t* expert_of = nullptr;
   uint32_t* last_use = nullptr;
@@ -74,6 +77,7 @@ struct ft_ctx {
   int32_t* h_victims = nullptr;
 
   PrefillState* prefill = nullptr;
+  Profiler prof;
 };
 
 namespace {
@@ -112,6 +116,22 @@ int alloc_arena(ft_ctx* c, int S) {
     cudaGetLastError();
     return fail(FT_E_NOMEM, "residency table allocation failed");
   }
+  if (c->cfg.dtype == FT_DTYPE_BF16) {
+    const uint64_t d = c->cfg.hidden, f = c->cfg.inter;
+    const uint64_t dims[3] = {f, d, (uint64_t)S};
+    const uint64_t strides[2] = {f * 2, c->Bx};
+    const uint32_t box[3] = {(uint32_t)kDecodeChunk, 256, 1};
+    char msg[160] = "";
+    if (!encode_tensor_map(&c->tmap_wd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c->arena + 4 * d * f, dims, strides, box,
+                           msg, sizeof(msg)))
+      return fail(FT_E_CUDA, "tensor map of the slot arena: %s", msg);
+    const uint64_t dims4[4] = {d, f, 2, (uint64_t)S};
+    const uint64_t strides4[3] = {d * 2, d * f * 2, c->Bx};
+    const uint32_t box4[4] = {256, (uint32_t)kDecodeChunk, 1, 1};
+    if (!encode_tensor_map(&c->tmap_gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, c->arena, dims4, strides4, box4, msg,
+                           sizeof(msg)))
+      return fail(FT_E_CUDA, "tensor map of the slot arena: %s", msg);
+  }
   c->S = S;
   return FT_OK;
 }
@@ -128,6 +148,7 @@ int reset_table(ft_ctx* c) {
 
 void free_all(ft_ctx* c) {
   if (c->prefill) prefill_destroy(c->prefill);
+  c->prof.destroy();
   cudaFree(c->arena);
   cudaFree(c->slot_of);
   cudaFree(c->expert_of);
@@ -181,7 +202,9 @@ int enqueue_control(ft_ctx* c, int layer, const int32_t* ids, int T, cudaStream_
   a.group_slot = lb.group_slot;
   a.group_off = lb.group_off;
   a.group_routes = lb.group_routes;
+  cudaEvent_t pb = c->prof.begin(st);
   CU(launch_control(a, st));
+  c->prof.end(st, FT_K_CONTROL, pb);
   lb.last_T = T;
   return FT_OK;
 }
@@ -205,7 +228,9 @@ int enqueue_fill(ft_ctx* c, int layer, cudaStream_t st) {
   LayerBufs& lb = c->layers[layer];
   CU(cudaEventRecord(c->ev_fork, st));
   CU(cudaStreamWaitEvent(c->xfer, c->ev_fork, 0));
+  cudaEvent_t pb = nullptr;
   if (c->cfg.fill_mode == FT_FILL_KERNEL) {
+    pb = c->prof.begin(c->xfer);
     CU(launch_fill(c->pool_dev, c->arena, lb.counts, lb.fetch, lb.victims, c->Bx, c->S, c->E_tot, c->status,
                    2 * c->sm_count, c->xfer));
   } else {
@@ -214,6 +239,7 @@ int enqueue_fill(ft_ctx* c, int layer, cudaStream_t st) {
     CU(cudaMemcpyAsync(c->h_fetch, lb.fetch, sizeof(int32_t) * c->cfg.k_max, cudaMemcpyDeviceToHost, c->xfer));
     CU(cudaMemcpyAsync(c->h_victims, lb.victims, sizeof(int32_t) * c->cfg.k_max, cudaMemcpyDeviceToHost, c->xfer));
     CU(cudaStreamSynchronize(c->xfer));
+    pb = c->prof.begin(c->xfer);
     const int q = c->h_counts[3];
     for (int i = 0; i < q; ++i) {
       const int u = c->h_fetch[i], s = c->h_victims[i];
@@ -222,6 +248,7 @@ int enqueue_fill(ft_ctx* c, int layer, cudaStream_t st) {
                          cudaMemcpyHostToDevice, c->xfer));
     }
   }
+  c->prof.end(c->xfer, FT_K_FILL, pb);
   CU(cudaEventRecord(c->ev_join, c->xfer));
   CU(cudaStreamWaitEvent(st, c->ev_join, 0));
   return FT_OK;
@@ -366,7 +393,9 @@ int ft_cache_step(ft_ctx* c, int layer, const float* logits, int T, ft_step_out*
   if (!logits) return fail(FT_E_ARG, "null logits");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   LayerBufs& lb = c->layers[layer];
+  cudaEvent_t pb = c->prof.begin(st);
   CU(launch_route(logits, T, c->cfg.num_experts, c->cfg.top_k, lb.ids, lb.w, c->status, nullptr, st));
+  c->prof.end(st, FT_K_ROUTE, pb);
   if ((rc = enqueue_control(c, layer, lb.ids, T, st))) return rc;
   fill_out(c, layer, out);
   return FT_OK;
@@ -396,7 +425,7 @@ int ft_moe_forward(ft_ctx* c, int layer, int mode, const float* logits, const ui
     if (!logits) return fail(FT_E_ARG, "prefill needs router logits");
     if (T < 1 || T > c->cfg.prefill_t_max) return fail(FT_E_ARG, "T=%d outside [1, prefill_t_max]", T);
     char msg[256] = "";
-    int r = prefill_forward(c->prefill, layer, logits, hidden, T, partial, out, st, msg, sizeof(msg));
+    int r = prefill_forward(c->prefill, layer, logits, hidden, T, partial, out, st, &c->prof, msg, sizeof(msg));
     if (r) return fail(r, "prefill: %s", msg);
     return FT_OK;
   }
@@ -420,10 +449,17 @@ int ft_moe_forward(ft_ctx* c, int layer, int mode, const float* logits, const ui
   a.hidden = hidden;
   a.ypart = c->ypart;
   a.status = c->status;
+  a.tmap_wd = &c->tmap_wd;
+  a.tmap_gu = &c->tmap_gu;
+  cudaEvent_t pb = c->prof.begin(st);
   cudaError_t e = launch_decode_experts(a, st);
   if (e == cudaErrorNotSupported) return fail(FT_E_UNSUPPORTED, "decode experts for this dtype are not built");
+  if (e == cudaErrorInvalidValue) return fail(FT_E_UNSUPPORTED, "decode experts need d <= 8192 (multiple of 256)");
   CU(e);
+  c->prof.end(st, FT_K_EXPERTS, pb);
+  pb = c->prof.begin(st);
   CU(launch_merge(c->ypart, c->n_chunks, lb.slot_ids, lb.w, partial, out, T, c->cfg.top_k, c->cfg.hidden, st));
+  c->prof.end(st, FT_K_MERGE, pb);
   return FT_OK;
 }
 
@@ -483,6 +519,29 @@ void* ft_slot_ptr(ft_ctx* c, int slot) {
 int ft_get_epoch(ft_ctx* c) { return c ? c->epoch : fail(FT_E_ARG, "null context"); }
 
 int ft_num_slots(ft_ctx* c) { return c ? c->S : fail(FT_E_ARG, "null context"); }
+
+int ft_profile_enable(ft_ctx* c, int on) {
+  if (!c) return fail(FT_E_ARG, "null context");
+  c->prof.on = on != 0;
+  return FT_OK;
+}
+
+int ft_profile_read(ft_ctx* c, double* total_ms, uint64_t* launches, int reset) {
+  if (!c) return fail(FT_E_ARG, "null context");
+  CU(cudaDeviceSynchronize());
+  for (int k = 0; k < FT_K_COUNT; ++k) {
+    double ms = 0.0;
+    for (auto& p : c->prof.rec[k]) {
+      float x = 0.f;
+      CU(cudaEventElapsedTime(&x, p.first, p.second));
+      ms += x;
+    }
+    if (total_ms) total_ms[k] = ms;
+    if (launches) launches[k] = c->prof.rec[k].size();
+  }
+  if (reset) c->prof.reset();
+  return FT_OK;
+}
 
 int ft_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, uint32_t* status, void* stream) {
   if (!logits || !ids || !w) return fail(FT_E_ARG, "null pointer");

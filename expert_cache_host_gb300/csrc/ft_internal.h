@@ -5,7 +5,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+#include <vector>
+
 #include "../../include/ft_moe.h"
+
+struct CUtensorMap_st;
 
 namespace ft {
 
@@ -86,11 +91,62 @@ struct DecodeArgs {
   const uint16_t* hidden;  // [T, d] bf16
   float* ypart;            // [T*k][f/kDecodeChunk][d]
   uint32_t* status;
+  const CUtensorMap_st* tmap_wd;  // 3-D map (f, d, slot) over the arena's down projections
+  const CUtensorMap_st* tmap_gu;  // 4-D map (d, f, {gate, up}, slot) over the arena's gate/up projections
 };
 cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st);
 
 // out[t] = partial[t] + sum_j [slot_ids >= 0] w[t,j] * sum_c ypart[t*k+j][c]
 cudaError_t launch_merge(const float* ypart, int n_chunks, const int32_t* slot_ids, const float* w,
                          const float* partial, float* out, int T, int k, int d, cudaStream_t st);
+
+// Event pairs around launches, for ft_profile_read.  Records nothing while
+// the stream is being captured.
+struct Profiler {
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> rec[FT_K_COUNT];
+
+  cudaEvent_t get() {
+    cudaEvent_t e = nullptr;
+    if (!pool.empty()) {
+      e = pool.back();
+      pool.pop_back();
+    } else if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+    }
+    return e;
+  }
+  // Returns the start event, or nullptr when not recording.
+  cudaEvent_t begin(cudaStream_t st) {
+    if (!on) return nullptr;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+    cudaEvent_t b = get();
+    if (b) cudaEventRecord(b, st);
+    return b;
+  }
+  void end(cudaStream_t st, int kind, cudaEvent_t b) {
+    if (!b) return;
+    cudaEvent_t e = get();
+    if (!e) return;
+    cudaEventRecord(e, st);
+    rec[kind].push_back({b, e});
+  }
+  void reset() {
+    for (auto& v : rec) {
+      for (auto& p : v) {
+        pool.push_back(p.first);
+        pool.push_back(p.second);
+      }
+      v.clear();
+    }
+  }
+  void destroy() {
+    reset();
+    for (auto e : pool) cudaEventDestroy(e);
+    pool.clear();
+  }
+};
 
 }  // namespace ft

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "ft_internal.h"
+
 namespace ft {
 
 struct PrefillConfig {
@@ -23,6 +25,7 @@ struct PrefillState;
 PrefillState* prefill_create(const PrefillConfig& cfg, char* msg, size_t msg_len);
 void prefill_destroy(PrefillState* p);
 int prefill_forward(PrefillState* p, int layer, const float* logits, const uint16_t* hidden, int T,
-                    const float* partial, float* out, cudaStream_t st, char* msg, size_t msg_len);
+                    const float* partial, float* out, cudaStream_t st, Profiler* prof, char* msg,
+                    size_t msg_len);
 
 }  // namespace ft

@@ -73,6 +73,7 @@ extern "C" {
 #define FT_ST_NAN 2u         /* a router logit was NaN */
 #define FT_ST_CLOCK_WRAP 4u  /* the LRU step clock reached 2^32 - 1 */
 #define FT_ST_BAD_SLOT 8u    /* a slot id outside [0, S) reached a kernel */
+#define FT_ST_TIMEOUT 16u    /* a bounded wait for an asynchronous copy ran out; the kernel exited early */
 
 #define FT_DTYPE_BF16 0
 #define FT_DTYPE_MXFP4 1
@@ -199,6 +200,27 @@ int ft_num_slots(ft_ctx* ctx);
  * a device uint32 that receives FT_ST_NAN bits.  E <= 1024, k <= 32. */
 int ft_route(const float* logits_dev, int T, int E, int k, int32_t* ids_dev, float* w_dev, uint32_t* status_dev,
              void* stream);
+
+/* Kernel classes of ft_profile_read. */
+#define FT_K_ROUTE 0   /* routing kernel */
+#define FT_K_CONTROL 1 /* cache-control kernel */
+#define FT_K_FILL 2    /* decode fill (kernel or copy-engine copies), transfer stream */
+#define FT_K_EXPERTS 3 /* decode expert kernel */
+#define FT_K_MERGE 4   /* merge kernel */
+#define FT_K_UPLOAD 5  /* prefill full-layer upload, transfer stream */
+#define FT_K_PREFILL 6 /* prefill routing, dispatch and grouped GEMMs */
+#define FT_K_COUNT 8
+
+/* Per-kernel timing for measurement.  While on, every kernel or copy the
+ * context enqueues outside a stream capture is bracketed by CUDA events
+ * recorded on the stream it is launched on (nothing is recorded during a
+ * capture).  Costs two event records per launch. */
+int ft_profile_enable(ft_ctx* ctx, int on);
+
+/* Synchronise, then return per class (arrays of FT_K_COUNT) the summed
+ * elapsed milliseconds and the number of launches recorded since the last
+ * reset; reset != 0 clears the records. */
+int ft_profile_read(ft_ctx* ctx, double* total_ms, uint64_t* launches, int reset);
 
 /* Message of the calling thread's last error ("" if none). */
 const char* ft_last_error(void);

@@ -63,6 +63,8 @@ def _l():
             lib.or_expert_ffn.argtypes = [vp, i32, i32, i32, vp, vp]
             lib.or_moe_forward.argtypes = [vp, u64, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp]
             lib.or_dense_moe.argtypes = [vp, u64, i32, i32, i32, i32, i32, vp, vp, vp]
+            lib.or_threads.argtypes = []
+            lib.or_threads.restype = i32
             for fn in ("or_route", "or_cache_step", "or_expert_ffn", "or_moe_forward", "or_dense_moe"):
                 getattr(lib, fn).restype = i32
             _lib = lib
@@ -83,6 +85,11 @@ class OracleError(RuntimeError):
 def _check(rc, what):
     if rc != OR_OK:
         raise OracleError(f"{what} returned {rc}")
+
+
+def threads() -> int:
+    """Threads the oracle's expert evaluations may use."""
+    return int(_l().or_threads())
 
 
 # ------------------------------------------------------------------ routing

@@ -27,6 +27,9 @@
  */
 #include <math.h>
 #include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdlib.h>
 #include <string.h>
 
@@ -35,6 +38,15 @@
 #define OR_ENAN -2
 #define OR_ERANGE -3
 #define OR_EWRAP -4
+
+/* Threads the expert evaluations may use (1 without OpenMP). */
+int or_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------ routing */
 
