@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       int s = 0;
       uint32_t ph = 0;
       for (int n = 0, i = 0; n < total; ++n) {
-        if (n >= NS && !mbar_wait(&empty[s], ph ^ 1u)) late = true;
+        if (n >= NS && !mbar_wait(&empty[s], ph ^ 1u, late)) late = true;
         unsigned char* dst = ring + s * kTile;
         mbar_expect_tx(&full[s], kTile);
         if (i < P1) {
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       // drain: the last use of every stage must have landed before the CTA exits
       for (int k = 0; k < NS && k < total; ++k) {
         const int n = total - 1 - k;
-        if (!mbar_wait(&full[n % NS], (uint32_t)((n / NS) & 1))) late = true;
+        if (!mbar_wait(&full[n % NS], (uint32_t)((n / NS) & 1), late)) late = true;
       }
       if (late) atomicOr(a.status, FT_ST_TIMEOUT);
     }
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int m = 0; m < 2; ++m) {
 #pragma unroll 1
       for (int cb = 0; cb < cb_n; ++cb) {
-        if (!mbar_wait(&full[s], ph)) late = true;
+        if (!mbar_wait(&full[s], ph, late)) late = true;
         const unsigned char* buf = ring + s * kTile + rl * 512 + cq * 16;
         const uint4 w0 = *reinterpret_cast<const uint4*>(buf);
         const uint4 w1 = *reinterpret_cast<const uint4*>(buf + 256);
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // down projection: 256 rows per tile, 4 threads per row, 2 rows per thread
 #pragma unroll 1
     for (int j = 0; j < d / 256; ++j) {
-      if (!mbar_wait(&full[s], ph)) late = true;
+      if (!mbar_wait(&full[s], ph, late)) late = true;
       const unsigned char* buf = ring + s * kTile + tid * 16;
       const uint4 w0 = *reinterpret_cast<const uint4*>(buf);
       const uint4 w1 = *reinterpret_cast<const uint4*>(buf + 8192);

@@ -232,7 +232,7 @@ int enqueue_fill(ft_ctx* c, int layer, cudaStream_t st) {
   if (c->cfg.fill_mode == FT_FILL_KERNEL) {
     pb = c->prof.begin(c->xfer);
     CU(launch_fill(c->pool_dev, c->arena, lb.counts, lb.fetch, lb.victims, c->Bx, c->S, c->E_tot, c->status,
-                   2 * c->sm_count, c->xfer));
+                   4 * c->sm_count, c->xfer));
   } else {
     // Copy-engine fills need the fetch list on the host: this reads it back.
     CU(cudaMemcpyAsync(c->h_counts, lb.counts, sizeof(int32_t) * kCountsLen, cudaMemcpyDeviceToHost, c->xfer));

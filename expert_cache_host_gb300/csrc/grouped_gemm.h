@@ -1,0 +1,34 @@
+// Grouped expert GEMMs (tcgen05) for the prefill path.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ft_internal.h"
+
+namespace ft {
+
+struct GemmArgs {
+  const int32_t* n_mtiles;     // device: number of valid M tiles
+  const int32_t* tile_expert;  // [max_mtiles] expert of each M tile
+  const int32_t* tile_row0;    // [max_mtiles] first sorted row of each M tile
+  const int32_t* seg_start;    // [E + 1] first sorted row of each expert's segment
+  void* out;                   // mode 1: H bf16 [rows, f]; mode 2: Y fp32 [rows, d]
+  int out_ld;                  // elements per output row
+  int K;                       // reduction length: d (mode 1) or f (mode 2)
+  uint32_t* status;
+};
+
+// H[rows, f] = silu(X W_gate^T) * (X W_up^T) per expert segment.
+// map_x: 2-D (d, rows) bf16, box 64 x 128, 128-byte swizzle.
+// map_w1: 4-D (d, f, {gate, up}, expert) bf16, box 64 x 128 x 1 x 1, 128-byte swizzle.
+cudaError_t launch_gemm_gateup(const CUtensorMap* map_x, const CUtensorMap* map_w1, const GemmArgs& a, int max_mtiles,
+                               int f, cudaStream_t st);
+
+// Y[rows, d] = H W_down^T per expert segment.
+// map_h: 2-D (f, rows) bf16, box 64 x 128; map_w2: 3-D (f, d, expert), box 64 x 256; both 128-byte swizzle.
+cudaError_t launch_gemm_down(const CUtensorMap* map_h, const CUtensorMap* map_w2, const GemmArgs& a, int max_mtiles,
+                             int d, cudaStream_t st);
+
+}  // namespace ft

@@ -24,7 +24,8 @@ EncodeFn encoder() {
 }  // namespace
 
 bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, void* base, const uint64_t* dims,
-                       const uint64_t* strides_bytes, const uint32_t* box, char* msg, size_t msg_len) {
+                       const uint64_t* strides_bytes, const uint32_t* box, char* msg, size_t msg_len,
+                       bool swizzle128) {
   EncodeFn fn = encoder();
   if (!fn) {
     snprintf(msg, msg_len, "cuTensorMapEncodeTiled is not available from the driver");
@@ -38,8 +39,9 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t ran
     es[i] = 1;
     if (i + 1 < rank) gs[i] = strides_bytes[i];
   }
-  CUresult r = fn(map, dtype, rank, base, gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(map, dtype, rank, base, gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed with %d", (int)r);
     return false;

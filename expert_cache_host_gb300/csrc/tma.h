@@ -9,12 +9,19 @@
 
 namespace ft {
 
-// Iterations of mbarrier.try_wait before a wait is declared failed.  Each
-// try_wait may suspend the thread for a short hardware-defined interval, so
-// the bound is well under a second of wall time on a healthy GPU.
-constexpr uint32_t kWaitLimit = 1u << 22;
+// Wall-clock bound of one mbarrier wait: a wait that has not completed after
+// this long is declared failed (the caller records FT_ST_TIMEOUT and winds
+// down).  Once a thread has seen a failed wait it passes give_up = true so
+// later waits try once and return, keeping the kernel's exit prompt.
+constexpr uint64_t kWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -32,19 +39,26 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Bounded wait for the phase with parity `parity` to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, bool give_up = false) {
   const uint32_t a = smem_u32(bar);
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(done)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (done) return true;
+  if (mbar_try(a, parity)) return true;
+  if (give_up) return false;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try(a, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
   }
-  return false;
 }
 
 // 1-D bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned).
@@ -53,6 +67,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                    smem_u32(dst)),
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
+}
+
+// 2-D tiled tensor copy of one box at coordinates (x, y).
+__device__ __forceinline__ void tensor_g2s_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // 3-D tiled tensor copy of one box at coordinates (x, y, z).
@@ -75,7 +98,9 @@ __device__ __forceinline__ void tensor_g2s_4d(void* dst, const CUtensorMap* map,
 }
 
 // Host: encode a tiled tensor map (returns false if the driver refuses it).
+// swizzle128 selects the 128-byte swizzle layout (inner box extent must then be 128 bytes).
 bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, void* base, const uint64_t* dims,
-                       const uint64_t* strides_bytes, const uint32_t* box, char* msg, size_t msg_len);
+                       const uint64_t* strides_bytes, const uint32_t* box, char* msg, size_t msg_len,
+                       bool swizzle128 = false);
 
 }  // namespace ft
