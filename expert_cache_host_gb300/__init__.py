@@ -28,7 +28,7 @@ COUNTS = ("n", "hits", "m", "q", "cpu", "n_groups", "now")
 EXPORTS = (
     "ft_moe_init", "ft_moe_destroy", "ft_cache_step", "ft_cache_control", "ft_moe_forward", "ft_cache_rebuild",
     "ft_get_status", "ft_get_counters", "ft_get_table", "ft_slot_ptr", "ft_get_epoch", "ft_num_slots", "ft_route",
-    "ft_profile_enable", "ft_profile_read", "ft_last_error",
+    "ft_profile_enable", "ft_profile_read", "ft_decode_experts_noalloc", "ft_last_error",
 )
 FT_K_ROUTE, FT_K_CONTROL, FT_K_FILL, FT_K_EXPERTS, FT_K_MERGE, FT_K_UPLOAD, FT_K_PREFILL, FT_K_COUNT = 0, 1, 2, 3, 4, 5, 6, 8
 KERNEL_CLASSES = ("route", "control", "fill", "experts", "merge", "upload", "prefill")
@@ -86,6 +86,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "ft_route": ([vp, i32, i32, i32, vp, vp, vp, vp], i32),
             "ft_profile_enable": ([vp, i32], i32),
             "ft_profile_read": ([vp, vp, vp, i32], i32),
+            "ft_decode_experts_noalloc": ([vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp], i32),
             "ft_last_error": ([], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -200,6 +201,17 @@ def ft_profile_read(ctx: int, reset: bool = True) -> dict:
     n = (ctypes.c_uint64 * FT_K_COUNT)()
     _chk(load().ft_profile_read(ctypes.c_void_p(ctx), ms, n, int(reset)))
     return {name: (ms[i], int(n[i])) for i, name in enumerate(KERNEL_CLASSES)}
+
+
+def ft_decode_experts_noalloc(arena_ptr: int, num_slots: int, hidden: int, inter: int, top_k: int, T: int,
+                              slot_ids_ptr: int, weights_ptr: int, hidden_ptr: int, partial_ptr: int, out_ptr: int,
+                              status_ptr: int = 0, stream: int = 0) -> None:
+    """Decode experts + merge with no device allocation (scratch is a fixed
+    array inside the library; see include/ft_moe.h for the limits)."""
+    v = ctypes.c_void_p
+    _chk(load().ft_decode_experts_noalloc(v(arena_ptr), num_slots, hidden, inter, top_k, T, v(slot_ids_ptr),
+                                          v(weights_ptr), v(hidden_ptr), v(partial_ptr or None), v(out_ptr),
+                                          v(status_ptr or None), v(stream)))
 
 
 def ft_last_error() -> str:

@@ -39,6 +39,14 @@ size_t expert_bytes(const ft_config& c) {
 
 }  // namespace
 
+int ft::record_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
 struct ft_ctx {
   ft_config cfg{};
   int device = 0;

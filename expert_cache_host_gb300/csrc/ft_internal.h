@@ -100,6 +100,10 @@ cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_merge(const float* ypart, int n_chunks, const int32_t* slot_ids, const float* w,
                          const float* partial, float* out, int T, int k, int d, cudaStream_t st);
 
+// Record the calling thread's error message (read back by ft_last_error) and
+// return `code`.
+int record_error(int code, const char* fmt, ...);
+
 // Event pairs around launches, for ft_profile_read.  Records nothing while
 // the stream is being captured.
 struct Profiler {

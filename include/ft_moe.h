@@ -222,6 +222,33 @@ int ft_profile_enable(ft_ctx* ctx, int on);
  * reset; reset != 0 clears the records. */
 int ft_profile_read(ft_ctx* ctx, double* total_ms, uint64_t* launches, int reset);
 
+/* Decode experts + merge without any allocation, for callers that cannot
+ * allocate device memory when they run the step (a runtime that fixes its
+ * memory budget at start-up and forbids allocation afterwards, a framework
+ * that owns every device buffer through its own pool, or code inside a
+ * stream capture in global mode, where cudaMalloc is not permitted).  The
+ * paper has no counterpart: this is an interface for such callers.
+ *
+ * Computes, for T tokens and bf16 experts in the canonical layout held in
+ * `arena_dev` (num_slots slots of 6*hidden*inter bytes, 16-byte aligned):
+ *   out[t] = partial[t] + sum_j [slot_ids[t,j] >= 0] weights[t,j] *
+ *            SwiGLU expert in slot slot_ids[t,j] applied to hidden[t]
+ * -- the same arithmetic as ft_moe_forward(FT_DECODE_CACHED) after the fills,
+ * with every route its own group.  slot_ids_dev [T, top_k] int32,
+ * weights_dev [T, top_k] float32, hidden_dev [T, hidden] bf16, partial_dev
+ * [T, hidden] float32 or NULL, out_dev [T, hidden] float32 (written);
+ * status_dev: a device uint32 that receives FT_ST_* bits, or NULL.
+ * Scratch lives in a fixed 8 MiB device array inside the library (held by
+ * every GPU that loads it until exit); T*top_k*(inter/32)*hidden*4 bytes of
+ * partial sums plus small route lists must fit, else FT_E_ARG.  The first call
+ * on a device looks the array up (cudaGetSymbolAddress) and should come before
+ * any stream capture.  All calls share the array, which keeps the last call's
+ * contents; calls that overlap on the GPU race on it.  Enqueues on `stream`,
+ * never synchronises, calls no allocating routine. */
+int ft_decode_experts_noalloc(const void* arena_dev, int num_slots, int hidden, int inter, int top_k, int T,
+                              const int32_t* slot_ids_dev, const float* weights_dev, const uint16_t* hidden_dev,
+                              const float* partial_dev, float* out_dev, uint32_t* status_dev, void* stream);
+
 /* Message of the calling thread's last error ("" if none). */
 const char* ft_last_error(void);
 
