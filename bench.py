@@ -1,19 +1,22 @@
 #!/usr/bin/env python
 """Benchmark of the MoE expert-cache layer step on GB300.
 
-Default workload (one line of JSON on stdout): A3B-style decode, 48 MoE layers,
-d=2048, E=128 routed experts, top-8, SwiGLU f=768, bf16 weights N(0, 0.02) in a
-57.98 GB pinned host pool, batch 1, AR(1) hidden states (rho = 0.9), a shared
-LRU cache of 1536 slots (25% of 48x128), BP/BH = 1, K_max = 128.  One step is
-one decode token through all 48 layers: routing, cache control, fills from the
-host pool, expert FFNs and merge, replayed as one CUDA graph per token.
+One JSON line on stdout.  The headline (value) is A3B-style decode: 48 MoE
+layers, d=2048, E=128 routed experts, top-8, SwiGLU f=768, bf16 weights
+N(0, 0.02) in a 57.98 GB pinned host pool, batch 1, AR(1) hidden states
+(rho = 0.9), a shared LRU cache of 1536 slots (25% of 48x128), BP/BH = 1,
+K_max = 128.  One step is one decode token through all 48 layers -- routing,
+cache control, fills from the host pool, expert FFNs and merge -- replayed as
+one CUDA graph per token.  The same run adds, as components, the 8192-token
+prefill chunk of the same model (full-layer double buffer on and off, grouped
+GEMM throughput with weights resident) and the cache-control stress workload
+(48 layers x 64 tokens x top-8, 6144 slots, Zipf routes).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload a3b_decode|tiny_decode|v4_decode|a3b_prefill|control_stress]
 
-Under torchrun (N > 1) every rank runs an independent replica of the workload
-on its own GPU (the path has no exchange step); rank 0 prints the line with
-value = units of all ranks / the slowest rank's time.
+Under torchrun (N > 1) every rank runs an independent replica of the decode
+workload on its own GPU (the path has no exchange step); rank 0 prints the
+line with value = tokens of all ranks / the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -34,24 +37,22 @@ if ROOT not in sys.path:
 
 import ftsynth  # noqa: E402
 
-WORKLOADS = {
-    "a3b_decode": dict(L=48, E=128, k=8, d=2048, f=768, dtype=0, S=1536, K_max=128, T=1, rho=0.9, r=(1, 1),
-                       steps=512,
-                       desc="A3B-style decode: 48 layers, d=2048, E=128, top-8, f=768, bf16, batch 1, "
-                            "S=1536 (25% of 6144), BP/BH=1, K_max=128, AR(1) rho=0.9"),
-    "tiny_decode": dict(L=1, E=16, k=2, d=256, f=128, dtype=0, S=8, K_max=16, T=1, rho=0.9, r=(1, 1), steps=32,
-                        desc="tiny: 1 layer, d=256, E=16, top-2, f=128, S=8, BP/BH=1"),
-}
+METRIC = "MoE decode tok/s (A3B-style, batch 1, GPU side; CPU-routed experts arrive as a partial sum)"
+A3B = dict(L=48, E=128, k=8, d=2048, f=768, dtype=0, S=1536, K_max=128, T=1, rho=0.9, r=(1, 1),
+           desc="A3B-style decode: 48 layers, d=2048, E=128, top-8, f=768, bf16, batch 1, "
+                "S=1536 (25% of 6144), BP/BH=1, K_max=128, AR(1) rho=0.9")
 L2_BYTES = 129 * 2 ** 20
+
+# DRAM bytes per launch from ncu captures (profiles/); None once the kernel changed.
+NCU_TRAFFIC = {
+    "decode_experts": 75_544_832 + 1_589_248,  # profiles/decode_experts_a3b.md, one A3B layer, 8 experts
+}
 
 
 # ----------------------------------------------------------------------------- helpers
 
 def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
 def replica_reduce(elapsed_s: float, units: float, world_size: int):
@@ -87,9 +88,7 @@ class ClockSampler:
          "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = None
+        self.gpu, self.proc, self.path = gpu_index, None, None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(prefix="ftclk", suffix=".csv")
@@ -116,22 +115,18 @@ class ClockSampler:
         rows = []
         if self.path and os.path.exists(self.path):
             with open(self.path) as fh:
-                for line in fh:
-                    parts = [x.strip() for x in line.split(",")]
-                    if len(parts) >= 9:
-                        rows.append(parts)
+                rows = [p for p in ([x.strip() for x in line.split(",")] for line in fh) if len(p) >= 9]
             os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        num = lambda s: s.replace(".", "", 1).isdigit()
+        sm = [float(r[1]) for r in rows if num(r[1])]
+        mx = [float(r[2]) for r in rows if num(r[2])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows)}
 
-
-# ----------------------------------------------------------------------------- decode workload
 
 def decode_inputs(w, n_steps, seed=0):
     """AR(1) hidden [steps, L, T, d] bf16 and logits [steps, L, T, E] float32."""
@@ -145,19 +140,40 @@ def decode_inputs(w, n_steps, seed=0):
     return hid, np.ascontiguousarray(lg)
 
 
-def run_ours_decode(args, w, world, rank, local, pool, hid, lg, t_gen):
+def timed(stream, fn, reps=1):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def link_peak_gbs(pool, nbytes):
+    """Best of three host->device copies of `nbytes` of the pinned pool (copy engine)."""
+    import torch
+    src = torch.from_numpy(pool[:nbytes])
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    best = min(timed(s, lambda: dst.copy_(src, non_blocking=True)) for _ in range(3))
+    del dst
+    return nbytes / best / 1e9
+
+
+# ----------------------------------------------------------------------------- decode (headline)
+
+def run_decode_leg(args, w, world, local, pool, hid, lg):
     import torch
 
     import expert_cache_host_gb300 as ft
-    from expert_cache_host_gb300 import build as ftbuild
 
-    ftbuild.build()
-    torch.cuda.set_device(local)
     L, E, k, d, f, T = w["L"], w["E"], w["k"], w["d"], w["f"], w["T"]
     bx = ftsynth.expert_bytes(d, f, w["dtype"])
     W, K = args.warmup, args.steps
-    P = min(K, args.profile_steps)
-    E2E = min(K, args.e2e_steps)
+    P, E2E = min(K, args.profile_steps), min(K, args.e2e_steps)
     cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, dtype=w["dtype"],
                          num_slots=w["S"], k_max=w["K_max"], t_max=T, r_num=w["r"][0], r_den=w["r"][1])
     t0 = time.time()
@@ -181,118 +197,201 @@ def run_ours_decode(args, w, world, rank, local, pool, hid, lg, t_gen):
 
         with torch.cuda.stream(stream):
             st = stream.cuda_stream
-            # one eager token (step 0) to set up kernel attributes, then capture
             cur_hid.copy_(d_hid[0])
             cur_lg.copy_(d_lg[0])
-            token(st)
+            token(st)  # one eager token (step 0): kernel attributes are set outside the capture
             stream.synchronize()
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
                 token(torch.cuda.current_stream().cuda_stream)
             s = 1
+
+            def step():
+                nonlocal s
+                cur_hid.copy_(d_hid[s])
+                cur_lg.copy_(d_lg[s])
+                graph.replay()
+                s += 1
+
             for _ in range(W - 1):
-                cur_hid.copy_(d_hid[s]); cur_lg.copy_(d_lg[s]); graph.replay(); s += 1
+                step()
             stream.synchronize()
             if world > 1:
                 torch.distributed.barrier()
             c0 = ft.ft_get_counters(ctx, L)
-            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with ClockSampler(local) as clk:
-                stream.synchronize()
-                ev0.record(stream)
-                for _ in range(K):
-                    cur_hid.copy_(d_hid[s]); cur_lg.copy_(d_lg[s]); graph.replay(); s += 1
-                ev1.record(stream)
-                ev1.synchronize()
-            elapsed = ev0.elapsed_time(ev1) / 1e3
+                elapsed = timed(stream, step, K)
             if world > 1:
                 torch.distributed.barrier()
             c1 = ft.ft_get_counters(ctx, L)
             clocks = clk.summary()
 
-            # per-kernel durations: the same steps run eagerly with event timing
+            # per-kernel durations: the following steps run eagerly with event timing
             ft.ft_profile_enable(ctx, True)
             ft.ft_profile_read(ctx, reset=True)
             cp0 = ft.ft_get_counters(ctx, L)
             for _ in range(P):
-                cur_hid.copy_(d_hid[s]); cur_lg.copy_(d_lg[s]); token(st); s += 1
+                cur_hid.copy_(d_hid[s])
+                cur_lg.copy_(d_lg[s])
+                token(st)
+                s += 1
             prof = ft.ft_profile_read(ctx, reset=True)
             cp1 = ft.ft_get_counters(ctx, L)
             ft.ft_profile_enable(ctx, False)
 
-            # end to end: pinned host inputs in, layer outputs back, per token
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            stream.synchronize()
-            e0.record(stream)
-            for _ in range(E2E):
+            # end to end: pinned host inputs in, every layer's output back, per token
+            def e2e_step():
+                nonlocal s
                 cur_hid.copy_(h_hid[s], non_blocking=True)
                 cur_lg.copy_(h_lg[s], non_blocking=True)
                 graph.replay()
                 h_out.copy_(out, non_blocking=True)
                 s += 1
-            e1.record(stream)
-            e1.synchronize()
-            e2e_elapsed = e0.elapsed_time(e1) / 1e3
+
+            e2e_elapsed = timed(stream, e2e_step, E2E)
         status = ft.ft_get_status(ctx)
     finally:
         ft.ft_moe_destroy(ctx)
 
     dc = (c1 - c0).astype(np.float64)
-    hits, misses, fills, cpu = dc[:, 0].sum(), dc[:, 1].sum(), dc[:, 2].sum(), dc[:, 3].sum()
+    hits, misses, fills, cpu = (dc[:, i].sum() for i in range(4))
     elapsed_max, units = replica_reduce(elapsed, K * T, world)
-    value = units / elapsed_max
-    peaks = measured_peaks()
     dp = (cp1 - cp0).astype(np.float64)
-    groups_p = dp[:, 0].sum() + dp[:, 2].sum()
-    fills_p = dp[:, 2].sum()
+    groups_p, fills_p = dp[:, 0].sum() + dp[:, 2].sum(), dp[:, 2].sum()
     tot_ms = sum(v[0] for v in prof.values())
-    shares = {kname: (round(v[0] / tot_ms, 4) if tot_ms else 0.0) for kname, v in prof.items() if v[1]}
     ex_ms, ex_n = prof["experts"]
     fill_ms, fill_n = prof["fill"]
-    ex_bytes = groups_p * bx  # algorithmic: each executed expert's weights read once
-    ex_gbs = ex_bytes / (ex_ms / 1e3) / 1e9 if ex_ms else 0.0
-    fill_gbs = fills_p * bx / (fill_ms / 1e3) / 1e9 if fill_ms else 0.0
-    per_launch_bytes = ex_bytes / ex_n if ex_n else 0.0
-    h2d = (lg[0].nbytes + hid[0].nbytes)
-    d2h = L * T * d * 4
-    line = {
-        "metric": "MoE decode tok/s (A3B-style, batch 1, GPU side; CPU-routed experts arrive as a partial sum)",
-        "value": round(value, 3),
-        "unit": "tok/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": W,
-        "ms_per_step": round(elapsed_max / K * 1e3, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": w["desc"], "graph": "one CUDA graph per token", "batch": T,
-                   "l2": "inputs larger than L2: %.2f GB of expert weights read per token" % (L * k * bx / 1e9),
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
-        "roofline": {"bound": "hbm", "kernel": "decode experts", "achieved": round(ex_gbs, 1),
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ex_gbs / peaks["hbm_gbs"], 4),
-                     "traffic": None, "peak_source": peaks["source"],
-                     "bytes_per_launch": round(per_launch_bytes), "avg_launch_us": round(ex_ms / ex_n * 1e3, 2) if ex_n else None},
-        "components": {
-            "kernel_share": shares,
-            "kernel_ms_per_token": {kname: round(v[0] / P, 4) for kname, v in prof.items() if v[1]},
-            "fill_link_gbs": round(fill_gbs, 1),
-            "control_us_per_layer_step": round(prof["control"][0] / max(1, prof["control"][1]) * 1e3, 3),
-            "hit_rate": round(hits / max(1.0, hits + misses), 4),
-            "fills_per_token": round(fills / K, 3),
-            "cpu_routes_per_token": round(cpu / K, 3),
-            "eager_ms_per_token_profiled": round(tot_ms / P, 4) if P else None,
-            "setup_s": {"generate": round(t_gen, 1), "init_pin": round(t_init, 1)},
-            "device_status": status,
-        },
-        "clocks": clocks,
-        "e2e": {"value": round(E2E * T / e2e_elapsed, 3), "unit": "tok/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": int(K * L * (5 if w["dtype"] == 0 else 5)),
-    }
-    return line
+    return dict(
+        value=units / elapsed_max, elapsed=elapsed_max, K=K, W=W, T=T, clocks=clocks, status=status,
+        t_init=t_init, hits=hits, misses=misses, fills=fills, cpu=cpu, P=P,
+        shares={n: round(v[0] / tot_ms, 4) for n, v in prof.items() if v[1]},
+        ms_per_token={n: round(v[0] / P, 4) for n, v in prof.items() if v[1]},
+        launches={n: v[1] for n, v in prof.items() if v[1]},
+        ex_bytes=groups_p * bx, ex_ms=ex_ms, ex_n=ex_n, fill_bytes=fills_p * bx, fill_ms=fill_ms, fill_n=fill_n,
+        control_us=prof["control"][0] / max(1, prof["control"][1]) * 1e3,
+        route_us=prof["route"][0] / max(1, prof["route"][1]) * 1e3,
+        eager_ms=tot_ms / P if P else None,
+        e2e=E2E * T / e2e_elapsed, h2d=int(lg[0].nbytes + hid[0].nbytes), d2h=int(L * T * d * 4),
+    )
+
+
+# ----------------------------------------------------------------------------- prefill chunk
+
+def run_prefill_leg(args, w, pool):
+    import torch
+
+    import expert_cache_host_gb300 as ft
+
+    L = args.prefill_layers or w["L"]
+    E, k, d, f, T = w["E"], w["k"], w["d"], w["f"], args.prefill_tokens
+    bx = ftsynth.expert_bytes(d, f, 0)
+    wr = ftsynth.router_weights(0, L, E, d)
+    hid = np.stack([ftsynth.prefill_hidden(0, l, T, d) for l in range(L)])
+    lg = np.stack([ftsynth.router_logits(hid[l], wr[l]) for l in range(L)])
+    d_hid = torch.from_numpy(hid.view(np.int16)).cuda()
+    d_lg = torch.from_numpy(lg).cuda()
+    del hid, lg
+    out = torch.empty((T, d), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    res = {}
+    for buffers in (2, 1):
+        cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, num_slots=1, k_max=1, t_max=1,
+                             prefill_buffers=buffers, prefill_t_max=T)
+        ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
+        try:
+            with torch.cuda.stream(stream):
+                st = stream.cuda_stream
+
+                def chunk():
+                    for l in range(L):
+                        ft.ft_moe_forward(ctx, l, ft.FT_PREFILL_LAYER, d_lg[l].data_ptr(), d_hid[l].data_ptr(), T, 0,
+                                          out.data_ptr(), st)
+
+                chunk()  # warm-up chunk (each chunk re-uploads the whole pool: layer 0 is not resident)
+                times = [timed(stream, chunk) for _ in range(2)]
+                res[buffers] = min(times)
+                if buffers == 2:
+                    # upload rate and grouped-GEMM throughput, weights resident (layer 0 twice in a row)
+                    ft.ft_profile_enable(ctx, True)
+                    ft.ft_profile_read(ctx, reset=True)
+                    chunk()
+                    prof_chunk = ft.ft_profile_read(ctx, reset=True)
+                    for _ in range(3):
+                        ft.ft_moe_forward(ctx, 0, ft.FT_PREFILL_LAYER, d_lg[0].data_ptr(), d_hid[0].data_ptr(), T, 0,
+                                          out.data_ptr(), st)
+                    ft.ft_moe_forward(ctx, 0, ft.FT_PREFILL_LAYER, d_lg[0].data_ptr(), d_hid[0].data_ptr(), T, 0,
+                                      out.data_ptr(), st)
+                    prof_res = ft.ft_profile_read(ctx, reset=True)
+                    ft.ft_profile_enable(ctx, False)
+            status = ft.ft_get_status(ctx)
+        finally:
+            ft.ft_moe_destroy(ctx)
+    pool_bytes = L * E * bx
+    up_ms, up_n = prof_chunk["upload"]
+    gemm_ms, gemm_n = prof_res["gemm"]
+    flops_layer = T * k * 3 * d * f * 2  # 3 matrices of d*f MACs per (token, expert), 2 flops per MAC
+    gemm_tflops = flops_layer / (gemm_ms / gemm_n / 1e3) / 1e12 if gemm_n else 0.0
+    upload_gbs = up_n * E * bx / (up_ms / 1e3) / 1e9 if up_n else 0.0
+    return dict(L=L, T=T, chunk_s=res[2], chunk_s_single_buffer=res[1], pool_bytes=pool_bytes,
+                link_gbs=pool_bytes / res[2] / 1e9, upload_gbs=upload_gbs, gemm_tflops=gemm_tflops,
+                gemm_ms_per_layer=gemm_ms / max(1, gemm_n), status=status,
+                overlap_loss_without_double_buffer=1.0 - res[2] / res[1])
+
+
+# ----------------------------------------------------------------------------- control stress
+
+def run_control_leg(args):
+    import torch
+
+    import expert_cache_host_gb300 as ft
+
+    L, E, k, T, steps = 48, 128, 8, 64, args.control_steps
+    d, f = 256, 128  # the control kernel never reads expert bytes: smallest legal expert shape
+    pool = np.zeros(L * E * ftsynth.expert_bytes(d, f, 0), dtype=np.uint8)
+    stream = torch.cuda.Stream()
+    cases = [(6144, km, s) for s in (0.6, 1.2) for km in (8, 64, 128, 512)] + \
+            [(S, 128, s) for S in (1536, 512) for s in (0.6, 1.2)]
+    routes = {}
+    for s in (0.6, 1.2):
+        r = np.stack([ftsynth.zipf_routes(0, l, E, T, k, s, 0, steps) for l in range(L)], axis=1)
+        routes[s] = torch.from_numpy(r).cuda()  # [steps, L, T, k]
+    out = []
+    for S, km, s in cases:
+        cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, num_slots=S, k_max=km, t_max=T)
+        ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
+        try:
+            cur = torch.empty((L, T, k), dtype=torch.int32, device="cuda")
+            with torch.cuda.stream(stream):
+                cur.copy_(routes[s][0])
+                for l in range(L):
+                    ft.ft_cache_control(ctx, l, cur[l].data_ptr(), T, stream.cuda_stream)
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for l in range(L):
+                        ft.ft_cache_control(ctx, l, cur[l].data_ptr(), T, torch.cuda.current_stream().cuda_stream)
+                i = 1
+
+                def step():
+                    nonlocal i
+                    cur.copy_(routes[s][i])
+                    g.replay()
+                    i += 1
+
+                warm = min(100, steps // 4)
+                for _ in range(warm):
+                    step()
+                c0 = ft.ft_get_counters(ctx, L)
+                el = timed(stream, step, steps - 1 - warm)
+                c1 = ft.ft_get_counters(ctx, L)
+            dc = (c1 - c0).astype(np.float64)
+            n_ls = (steps - 1 - warm) * L
+            out.append(dict(S=S, K_max=km, zipf_s=s, us_per_layer_step=round(el / n_ls * 1e6, 3),
+                            miss_rate=round(dc[:, 1].sum() / max(1.0, dc[:, 0].sum() + dc[:, 1].sum()), 4),
+                            fills_per_layer_step=round(dc[:, 2].sum() / n_ls, 3), status=ft.ft_get_status(ctx)))
+        finally:
+            ft.ft_moe_destroy(ctx)
+    return out
 
 
 # ----------------------------------------------------------------------------- oracle (CPU baseline / reference arm)
@@ -324,20 +423,16 @@ def oracle_decode_rate(w, pool, hid, lg, budget_s, min_tokens=1, max_tokens=None
 
 
 def run_reference(args, w):
-    """The oracle as the reference arm: same metric and unit, CPU cores."""
-    budget = args.ref_budget_s
+    """The oracle as the reference arm: same metric and unit, host cores."""
     pool = ftsynth.make_pool(0, w["L"], w["E"], w["d"], w["f"], w["dtype"], 0.02)
     hid, lg = decode_inputs(w, max(2, min(args.steps, 64)))
-    rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, budget, min_tokens=max(1, min(args.steps, 2)),
+    rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, args.ref_budget_s, min_tokens=max(1, min(args.steps, 2)),
                                               max_tokens=max(1, args.steps))
     sample = f"{n} decode tokens x {w['L']} layers from a cold cache ({t:.1f} s of oracle work)"
     return {
-        "impl": "reference",
-        "metric": "MoE decode tok/s (A3B-style, batch 1, GPU side; CPU-routed experts arrive as a partial sum)",
-        "value": round(rate, 5), "unit": "tok/s", "n_gpus": 1, "steps": n, "warmup": 0,
-        "ms_per_step": round(t / max(1, n) * 1e3, 2), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w["desc"]},
+        "impl": "reference", "metric": METRIC, "value": round(rate, 5), "unit": "tok/s", "n_gpus": 1, "steps": n,
+        "warmup": 0, "ms_per_step": round(t / max(1, n) * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": w["desc"]},
         "cpu_baseline": {"value": round(rate, 5), "unit": "tok/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(rate, 5), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -345,29 +440,90 @@ def run_reference(args, w):
 
 # ----------------------------------------------------------------------------- main
 
+def build_line(args, w, world, dec, link_gbs, pre, ctl, peaks):
+    ex_gbs = dec["ex_bytes"] / (dec["ex_ms"] / 1e3) / 1e9 if dec["ex_ms"] else 0.0
+    fill_gbs = dec["fill_bytes"] / (dec["fill_ms"] / 1e3) / 1e9 if dec["fill_ms"] else 0.0
+    bx = ftsynth.expert_bytes(w["d"], w["f"], w["dtype"])
+    line = {
+        "metric": METRIC, "value": round(dec["value"], 3), "unit": "tok/s", "n_gpus": world, "steps": dec["K"],
+        "warmup": dec["W"], "ms_per_step": round(dec["elapsed"] / dec["K"] * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w["desc"], "graph": "one CUDA graph per token", "batch": dec["T"],
+                   "l2": "inputs larger than L2: %.2f GB of expert weights per token" % (w["L"] * w["k"] * bx / 1e9),
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        # the dominant kernel by time is the fill: host-link bound
+        "roofline": {"bound": "host_link", "kernel": "decode fill (host pool -> slots)", "achieved": round(fill_gbs, 1),
+                     "peak": round(link_gbs, 1), "unit": "GB/s", "frac": round(fill_gbs / link_gbs, 4) if link_gbs else None,
+                     "traffic": None, "peak_source": "measured in this run: 1.21 GB pinned H2D cudaMemcpyAsync, best of 3",
+                     "share": dec["shares"].get("fill")},
+        "roofline_experts": {"bound": "hbm", "kernel": "decode experts", "achieved": round(ex_gbs, 1),
+                             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ex_gbs / peaks["hbm_gbs"], 4),
+                             "traffic": NCU_TRAFFIC["decode_experts"], "peak_source": peaks["source"],
+                             "bytes_per_launch": round(dec["ex_bytes"] / max(1, dec["ex_n"])),
+                             "avg_launch_us": round(dec["ex_ms"] / max(1, dec["ex_n"]) * 1e3, 2),
+                             "share": dec["shares"].get("experts")},
+        "components": {
+            "kernel_share": dec["shares"], "kernel_ms_per_token": dec["ms_per_token"],
+            "control_us_per_layer_step": round(dec["control_us"], 3), "route_us_per_layer_step": round(dec["route_us"], 3),
+            "hit_rate": round(dec["hits"] / max(1.0, dec["hits"] + dec["misses"]), 4),
+            "fills_per_token": round(dec["fills"] / dec["K"], 3), "cpu_routes_per_token": round(dec["cpu"] / dec["K"], 3),
+            "eager_ms_per_token_profiled": round(dec["eager_ms"], 4) if dec["eager_ms"] else None,
+            "init_pin_s": round(dec["t_init"], 2), "device_status": dec["status"],
+        },
+        "clocks": dec["clocks"],
+        "e2e": {"value": round(dec["e2e"], 3), "unit": "tok/s", "h2d_bytes_per_step": dec["h2d"],
+                "d2h_bytes_per_step": dec["d2h"]},
+        "gpu_launches": int(dec["K"] * w["L"] * 5),
+    }
+    if pre:
+        line["prefill"] = {
+            "workload": f"{pre['T']}-token chunk, A3B-style, {pre['L']} layers, full-layer double buffer",
+            "chunk_s": round(pre["chunk_s"], 4), "chunk_s_single_buffer": round(pre["chunk_s_single_buffer"], 4),
+            "loss_without_double_buffer": round(pre["overlap_loss_without_double_buffer"], 4),
+            "tok_s": round(pre["T"] / pre["chunk_s"], 1), "pool_gb": round(pre["pool_bytes"] / 1e9, 2),
+            "link_gbs_effective": round(pre["link_gbs"], 1), "upload_gbs": round(pre["upload_gbs"], 1),
+            "link_frac": round(pre["link_gbs"] / link_gbs, 4) if link_gbs else None,
+            "device_status": pre["status"],
+            "roofline_gemm": {"bound": "tensor", "kernel": "grouped SwiGLU GEMMs (tcgen05), weights resident",
+                              "achieved": round(pre["gemm_tflops"], 1), "peak": peaks["bf16_tflops"],
+                              "unit": "TFLOP/s", "frac": round(pre["gemm_tflops"] / peaks["bf16_tflops"], 4),
+                              "ms_per_layer": round(pre["gemm_ms_per_layer"], 3), "traffic": None,
+                              "peak_source": peaks["source"] + " (burst bf16)"},
+        }
+    if ctl:
+        line["control_stress"] = {
+            "workload": "control kernel alone, 48 layers x 64 tokens x top-8, E=128, Zipf routes, graph replay",
+            "steps": args.control_steps, "cases": ctl,
+        }
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=448)
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="a3b_decode")
     ap.add_argument("--profile-steps", type=int, default=32)
     ap.add_argument("--e2e-steps", type=int, default=128)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--ref-budget-s", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-control", action="store_true")
+    ap.add_argument("--prefill-tokens", type=int, default=8192)
+    ap.add_argument("--prefill-layers", type=int, default=0)
+    ap.add_argument("--control-steps", type=int, default=10000)
     ap.add_argument("--layers", type=int, default=0, help="override L (small profiling cases, not a bench line)")
     ap.add_argument("--slots", type=int, default=0, help="override S (small profiling cases, not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
-    w = dict(WORKLOADS[args.workload])
+    w = dict(A3B)
     if args.layers or args.slots:
-        w["L"] = args.layers or w["L"]
-        w["S"] = args.slots or w["S"]
-        w["desc"] = w["desc"] + f" [profiling case: L={w['L']}, S={w['S']}]"
+        w["L"], w["S"] = args.layers or w["L"], args.slots or w["S"]
+        w["desc"] += f" [profiling case: L={w['L']}, S={w['S']}]"
 
     if world > 1:
         import torch
@@ -384,18 +540,44 @@ def main():
             dist.destroy_process_group()
         return
 
-    t0 = time.time()
-    pool = ftsynth.make_pool(0, w["L"], w["E"], w["d"], w["f"], w["dtype"], 0.02)
+    import torch
+
+    from expert_cache_host_gb300 import build as ftbuild
+    ftbuild.build()
+    torch.cuda.set_device(local)
+    # The pool is written into memory that is already pinned (cudaHostAlloc through
+    # torch): over NVLink-C2C it streams ~5-15% faster than malloc'd pages pinned
+    # after the write, and much faster on first touch than huge-page-advised pages.
+    pool_t = torch.empty(w["L"] * w["E"] * ftsynth.expert_bytes(w["d"], w["f"], w["dtype"]), dtype=torch.uint8,
+                         pin_memory=True)
+    pool = ftsynth.make_pool(0, w["L"], w["E"], w["d"], w["f"], w["dtype"], 0.02, out=pool_t.numpy())
     hid, lg = decode_inputs(w, args.warmup + args.steps + min(args.steps, args.profile_steps)
                             + min(args.steps, args.e2e_steps))
-    t_gen = time.time() - t0
-    line = run_ours_decode(args, w, world, rank, local, pool, hid, lg, t_gen)
-    if rank == 0 and not args.no_cpu_baseline:
-        rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, args.cpu_budget_s)
-        line["cpu_baseline"] = {"value": round(rate, 5), "unit": "tok/s", "cores": threads, "kind": "oracle",
-                                "sample": f"{n} decode tokens x {w['L']} layers from a cold cache, "
-                                          f"{t:.1f} s of oracle work"}
+    dec = run_decode_leg(args, w, world, local, pool, hid, lg)
+    pre = ctl = None
+    link = 0.0
     if rank == 0:
+        import expert_cache_host_gb300 as ft
+        # the pool is registered (pinned, mapped) for the measurement below by a throwaway context
+        cfg = ft.make_config(num_layers=w["L"], num_experts=w["E"], top_k=w["k"], hidden=w["d"], inter=w["f"],
+                             num_slots=1, k_max=1, t_max=1)
+        ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
+        try:
+            link = link_peak_gbs(pool, w["E"] * ftsynth.expert_bytes(w["d"], w["f"], 0))
+        finally:
+            ft.ft_moe_destroy(ctx)
+        if not args.no_prefill and not args.layers:
+            pre = run_prefill_leg(args, w, pool)
+        if not args.no_control and not args.layers:
+            ctl = run_control_leg(args)
+    peaks = measured_peaks()
+    if rank == 0:
+        line = build_line(args, w, world, dec, link, pre, ctl, peaks)
+        if not args.no_cpu_baseline:
+            rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, args.cpu_budget_s)
+            line["cpu_baseline"] = {"value": round(rate, 5), "unit": "tok/s", "cores": threads, "kind": "oracle",
+                                    "sample": f"{n} decode tokens x {w['L']} layers from a cold cache, "
+                                              f"{t:.1f} s of oracle work"}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -30,8 +30,9 @@ EXPORTS = (
     "ft_get_status", "ft_get_counters", "ft_get_table", "ft_slot_ptr", "ft_get_epoch", "ft_num_slots", "ft_route",
     "ft_profile_enable", "ft_profile_read", "ft_decode_experts_noalloc", "ft_last_error",
 )
-FT_K_ROUTE, FT_K_CONTROL, FT_K_FILL, FT_K_EXPERTS, FT_K_MERGE, FT_K_UPLOAD, FT_K_PREFILL, FT_K_COUNT = 0, 1, 2, 3, 4, 5, 6, 8
-KERNEL_CLASSES = ("route", "control", "fill", "experts", "merge", "upload", "prefill")
+FT_K_ROUTE, FT_K_CONTROL, FT_K_FILL, FT_K_EXPERTS, FT_K_MERGE, FT_K_UPLOAD, FT_K_PREFILL, FT_K_GEMM = range(8)
+FT_K_COUNT = 8
+KERNEL_CLASSES = ("route", "control", "fill", "experts", "merge", "upload", "prefill", "gemm")
 
 
 class FtError(RuntimeError):

@@ -1,0 +1,322 @@
+// Decode expert kernel for MXFP4 experts (e2m1 codes, one e8m0 scale per 32
+// consecutive elements of a row; OCP Microscaling v1.0), HBM-bound.
+//
+// Same work split and data movement as the bf16 decode kernel: one CTA per
+// (resident expert, chunk of FC = 64 rows of f), a producer warp streaming
+// 16 KB TMA tiles through a ring with full/empty mbarriers, 16 consumer warps.
+//  - gate/up codes: 64 rows x 256 bytes boxes of a 4-D map (d/2, f, {g,u}, slot);
+//    the chunk's gate/up scales (64 rows x d/32 bytes each) arrive once by
+//    two 1-D bulk copies;
+//  - down codes: 256 rows x 32 bytes boxes of a 3-D map (f/2, d, slot), two per
+//    stage; the two down scales of each row for this chunk are read directly
+//    (the 32 chunks of one expert share those sectors in L2).
+// Arithmetic: a 16-byte piece of a row is 32 elements = exactly one scale
+// group.  cvt.rn.f16x2.e2m1x2 turns each code byte into two exact f16 values;
+// the group's products with the f16 activations accumulate in two chains of
+// eight HFMA2, the group sum is widened to fp32 and multiplied by the exact
+// power of two 2^(E-127), and groups accumulate in fp32.  The intermediate h
+// is held in f16 for the down projection.  (The page keeps DSV4's experts in
+// native MXFP4, "bit-identical" to the checkpoint: section "评估结果".)
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "ft_internal.h"
+#include "tma.h"
+
+namespace ft {
+namespace {
+
+constexpr int FC = kDecodeChunkFp4;        // 64 rows of f per CTA
+constexpr int kConsumers = 512;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kTile = 16384;
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+// Exact 2^(E-127) for an e8m0 byte (E = 255 is NaN, E = 0 the subnormal 2^-127).
+__device__ __forceinline__ float e8m0(unsigned e) {
+  return e == 255u ? __int_as_float(0x7FC00000) : (e ? __int_as_float((int)(e << 23)) : __int_as_float(0x00400000));
+}
+
+// Four code bytes -> four f16x2 pairs (low nibble -> low half).
+__device__ __forceinline__ void e2m1x8(unsigned w, unsigned& p0, unsigned& p1, unsigned& p2, unsigned& p3) {
+  asm("{ .reg .b8 a0, a1, a2, a3; mov.b32 {a0, a1, a2, a3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, a0; cvt.rn.f16x2.e2m1x2 %1, a1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, a2; cvt.rn.f16x2.e2m1x2 %3, a3; }"
+      : "=r"(p0), "=r"(p1), "=r"(p2), "=r"(p3)
+      : "r"(w));
+}
+
+__device__ __forceinline__ __half2 h2(unsigned v) { return *reinterpret_cast<__half2*>(&v); }
+
+// Sum over one 32-element group: 16 code bytes (w) against 16 f16x2 activation
+// pairs (x[0..3] as four uint4), returned in fp32 (unscaled).
+__device__ __forceinline__ float group_dot(const uint4 w, const uint4* x) {
+  __half2 a0 = __float2half2_rn(0.f), a1 = __float2half2_rn(0.f);
+  const unsigned ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    unsigned p0, p1, p2, p3;
+    e2m1x8(ww[i], p0, p1, p2, p3);
+    const uint4 xv = x[i];
+    if (i < 2) {
+      a0 = __hfma2(h2(p0), h2(xv.x), a0);
+      a0 = __hfma2(h2(p1), h2(xv.y), a0);
+      a0 = __hfma2(h2(p2), h2(xv.z), a0);
+      a0 = __hfma2(h2(p3), h2(xv.w), a0);
+    } else {
+      a1 = __hfma2(h2(p0), h2(xv.x), a1);
+      a1 = __hfma2(h2(p1), h2(xv.y), a1);
+      a1 = __hfma2(h2(p2), h2(xv.z), a1);
+      a1 = __hfma2(h2(p3), h2(xv.w), a1);
+    }
+  }
+  const float2 f0 = __half22float2(a0), f1 = __half22float2(a1);
+  return (f0.x + f0.y) + (f1.x + f1.y);
+}
+
+struct Layout {
+  size_t ring, full, empty, scbar, sc, xs, gu, hs, rs, total;
+};
+
+template <int TB, int NS>
+__host__ __device__ inline Layout smem_layout(int d) {
+  Layout L{};
+  L.ring = 0;
+  L.full = L.ring + (size_t)NS * kTile;
+  L.empty = L.full + 8 * NS;
+  L.scbar = L.empty + 8 * NS;
+  L.sc = (L.scbar + 8 + 127) / 128 * 128;                   // [2][FC][d/32] scale bytes
+  L.xs = L.sc + (size_t)2 * FC * (d / 32);                  // [TB][d/2] f16x2 pairs
+  L.gu = L.xs + (size_t)TB * (d / 2) * 4;                   // [2][FC][TB] fp32 row sums
+  L.hs = L.gu + sizeof(float) * 2 * FC * TB;                // [TB][FC/2] f16x2
+  L.rs = L.hs + (size_t)TB * (FC / 2) * 4;                  // [TB]
+  L.total = L.rs + sizeof(int) * TB;
+  return L;
+}
+
+template <int TB, int NS>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tmap_gu, const __grid_constant__ CUtensorMap tmap_wd,
+                        DecodeArgs a) {
+  extern __shared__ __align__(1024) unsigned char dyn[];
+  const int d = a.d, f = a.f;
+  const Layout Ly = smem_layout<TB, NS>(d);
+  unsigned char* ring = dyn + Ly.ring;
+  uint64_t* full = reinterpret_cast<uint64_t*>(dyn + Ly.full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(dyn + Ly.empty);
+  uint64_t* scbar = reinterpret_cast<uint64_t*>(dyn + Ly.scbar);
+  const unsigned char* sc = dyn + Ly.sc;
+  unsigned* xs = reinterpret_cast<unsigned*>(dyn + Ly.xs);
+  float* gu = reinterpret_cast<float*>(dyn + Ly.gu);
+  unsigned* hs = reinterpret_cast<unsigned*>(dyn + Ly.hs);
+  int* rs = reinterpret_cast<int*>(dyn + Ly.rs);
+
+  const int c = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
+  if (g >= a.counts[5]) return;
+  const int slot = a.group_slot[g];
+  if ((unsigned)slot >= (unsigned)a.S) {
+    if (tid == 0) atomicOr(a.status, FT_ST_BAD_SLOT);
+    return;
+  }
+  const size_t df = (size_t)d * f;
+  const unsigned char* ex = a.arena + (size_t)slot * a.Bx;
+  const unsigned char* sc_gate = ex + 3 * (df / 2);                 // [f][d/32]
+  const unsigned char* sc_down = sc_gate + 2 * (df / 32);           // [d][f/32]
+  const int r0 = a.group_off[g], r1 = a.group_off[g + 1];
+  const int n_batches = (r1 - r0 + TB - 1) / TB;
+  const int cb_n = d / 512;            // 256-byte column blocks per gate/up row
+  const int P1 = 2 * cb_n;
+  const int NTL = P1 + d / 512;        // down stages: 512 rows (two 256-row boxes) each
+  const int total = n_batches * NTL;
+  const int sc_row = d / 32;           // scale bytes per gate/up row
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers / 32);
+    }
+    mbar_init(scbar, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (tid >= kConsumers) {
+    if (tid == kConsumers) {
+      bool late = false;
+      const uint32_t scb = FC * sc_row;
+      mbar_expect_tx(scbar, 2 * scb);
+      bulk_g2s(dyn + Ly.sc, sc_gate + (size_t)c * FC * sc_row, scb, scbar);
+      bulk_g2s(dyn + Ly.sc + scb, sc_gate + df / 32 + (size_t)c * FC * sc_row, scb, scbar);
+      int s = 0;
+      uint32_t ph = 0;
+      for (int n = 0, i = 0; n < total; ++n) {
+        if (n >= NS && !mbar_wait(&empty[s], ph ^ 1u, late)) late = true;
+        unsigned char* dst = ring + s * kTile;
+        mbar_expect_tx(&full[s], kTile);
+        if (i < P1) {
+          const int m = i < cb_n ? 0 : 1, cb = i - m * cb_n;
+          tensor_g2s_4d(dst, &tmap_gu, cb * 256, c * FC, m, slot, &full[s]);
+        } else {
+          const int j = i - P1;
+          tensor_g2s_3d(dst, &tmap_wd, c * (FC / 2), j * 512, slot, &full[s]);
+          tensor_g2s_3d(dst + kTile / 2, &tmap_wd, c * (FC / 2), j * 512 + 256, slot, &full[s]);
+        }
+        if (++i == NTL) i = 0;
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      for (int k = 0; k < NS && k < total; ++k) {
+        const int n = total - 1 - k;
+        if (!mbar_wait(&full[n % NS], (uint32_t)((n / NS) & 1), late)) late = true;
+      }
+      if (!mbar_wait(scbar, 0, late)) late = true;
+      if (late) atomicOr(a.status, FT_ST_TIMEOUT);
+    }
+    return;
+  }
+
+  const int lane = tid & 31;
+  const int rl = tid >> 3, cq = tid & 7;      // gate/up: row, 16-byte column within a 128-byte half block
+  const int rowq = tid >> 1, q = tid & 1;     // down: row within a 256-row box, scale group of the chunk
+  const int n_chunks = f / FC;
+  bool late = false;
+  int s = 0;
+  uint32_t ph = 0;
+  auto release = [&]() {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (++s == NS) {
+      s = 0;
+      ph ^= 1u;
+    }
+  };
+
+  for (int b = 0; b < n_batches; ++b) {
+    const int tb = r0 + b * TB;
+    const int nt = min(TB, r1 - tb);
+    consumer_sync();
+    if (tid < nt) rs[tid] = a.group_routes[tb + tid];
+    for (int t = 0; t < nt; ++t) {
+      const int tok = a.group_routes[tb + t] / a.k;
+      const unsigned* src = reinterpret_cast<const unsigned*>(a.hidden + (size_t)tok * d);  // bf16 pairs
+      for (int i = tid; i < d / 2; i += kConsumers) {
+        const unsigned v = src[i];
+        const __half2 hv = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+        xs[(size_t)t * (d / 2) + i] = *reinterpret_cast<const unsigned*>(&hv);
+      }
+    }
+    consumer_sync();
+    if (b == 0 && !mbar_wait(scbar, 0, late)) late = true;
+
+    float acc[2][TB];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int t = 0; t < TB; ++t) acc[m][t] = 0.f;
+
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+#pragma unroll 1
+      for (int cb = 0; cb < cb_n; ++cb) {
+        if (!mbar_wait(&full[s], ph, late)) late = true;
+        const unsigned char* buf = ring + s * kTile + rl * 256 + cq * 16;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(buf);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(buf + 128);
+        release();
+        const int g0 = cb * 16 + cq;  // scale group of piece 0; piece 1 is g0 + 8
+        const float s0 = e8m0(sc[(m * FC + rl) * sc_row + g0]);
+        const float s1 = e8m0(sc[(m * FC + rl) * sc_row + g0 + 8]);
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+          if (t < nt) {
+            const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)t * (d / 2) + cb * 256 + cq * 16);
+            acc[m][t] = fmaf(group_dot(w0, xp), s0, acc[m][t]);
+            acc[m][t] = fmaf(group_dot(w1, xp + 32), s1, acc[m][t]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        float v = acc[m][t];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        if (cq == 0 && t < nt) gu[(m * FC + rl) * TB + t] = v;
+      }
+    consumer_sync();
+    if (tid < (FC / 2) * TB) {
+      const int pr = tid % (FC / 2), t = tid / (FC / 2);
+      if (t < nt) {
+        const float g0 = gu[(0 * FC + 2 * pr) * TB + t], u0 = gu[(1 * FC + 2 * pr) * TB + t];
+        const float g1 = gu[(0 * FC + 2 * pr + 1) * TB + t], u1 = gu[(1 * FC + 2 * pr + 1) * TB + t];
+        const __half2 hv = __floats2half2_rn(g0 / (1.f + expf(-g0)) * u0, g1 / (1.f + expf(-g1)) * u1);
+        hs[t * (FC / 2) + pr] = *reinterpret_cast<const unsigned*>(&hv);
+      }
+    }
+    consumer_sync();
+
+#pragma unroll 1
+    for (int j = 0; j < d / 512; ++j) {
+      const int row0 = j * 512 + rowq, row1 = row0 + 256;
+      const float s0 = e8m0(__ldg(sc_down + (size_t)row0 * (f / 32) + c * 2 + q));
+      const float s1 = e8m0(__ldg(sc_down + (size_t)row1 * (f / 32) + c * 2 + q));
+      if (!mbar_wait(&full[s], ph, late)) late = true;
+      const unsigned char* buf = ring + s * kTile + tid * 16;
+      const uint4 w0 = *reinterpret_cast<const uint4*>(buf);
+      const uint4 w1 = *reinterpret_cast<const uint4*>(buf + kTile / 2);
+      release();
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        if (t < nt) {
+          const uint4* hp = reinterpret_cast<const uint4*>(hs + t * (FC / 2) + q * 16);
+          float v0 = group_dot(w0, hp) * s0, v1 = group_dot(w1, hp) * s1;
+          v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+          v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+          if (q == 0) {
+            float* yp = a.ypart + ((size_t)rs[t] * n_chunks + c) * d;
+            yp[row0] = v0;
+            yp[row1] = v1;
+          }
+        }
+      }
+    }
+  }
+  if (late) atomicOr(a.status, FT_ST_TIMEOUT);
+}
+
+template <int TB, int NS>
+cudaError_t launch(const DecodeArgs& a, cudaStream_t st) {
+  const size_t smem = smem_layout<TB, NS>(a.d).total;
+  static thread_local int configured_dev = -1;
+  static thread_local size_t configured_smem = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev || configured_smem < smem) {
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_mxfp4_kernel<TB, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+    configured_smem = smem;
+  }
+  dim3 grid(a.f / FC, a.max_groups);
+  decode_mxfp4_kernel<TB, NS><<<grid, kThreads, smem, st>>>(*a.tmap_gu, *a.tmap_wd, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_experts_mxfp4(const DecodeArgs& a, int tokens, cudaStream_t st) {
+  if (a.d % 512 || a.d > 16384 || a.f % FC || !a.tmap_wd || !a.tmap_gu) return cudaErrorInvalidValue;
+  return tokens == 1 ? launch<1, 5>(a, st) : launch<4, 3>(a, st);
+}
+
+}  // namespace ft

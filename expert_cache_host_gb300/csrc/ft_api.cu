@@ -139,6 +139,22 @@ int alloc_arena(ft_ctx* c, int S) {
     if (!encode_tensor_map(&c->tmap_gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, c->arena, dims4, strides4, box4, msg,
                            sizeof(msg)))
       return fail(FT_E_CUDA, "tensor map of the slot arena: %s", msg);
+  } else {
+    // MXFP4: byte views of the codes -- gate/up (d/2, f, {g, u}, slot), down (f/2, d, slot)
+    const uint64_t d = c->cfg.hidden, f = c->cfg.inter;
+    const uint64_t dims[3] = {f / 2, d, (uint64_t)S};
+    const uint64_t strides[2] = {f / 2, c->Bx};
+    const uint32_t box[3] = {(uint32_t)kDecodeChunkFp4 / 2, 256, 1};
+    char msg[160] = "";
+    if (!encode_tensor_map(&c->tmap_wd, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c->arena + d * f, dims, strides, box, msg,
+                           sizeof(msg)))
+      return fail(FT_E_CUDA, "tensor map of the slot arena: %s", msg);
+    const uint64_t dims4[4] = {d / 2, f, 2, (uint64_t)S};
+    const uint64_t strides4[3] = {d / 2, d * f / 2, c->Bx};
+    const uint32_t box4[4] = {256, (uint32_t)kDecodeChunkFp4, 1, 1};
+    if (!encode_tensor_map(&c->tmap_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, c->arena, dims4, strides4, box4, msg,
+                           sizeof(msg)))
+      return fail(FT_E_CUDA, "tensor map of the slot arena: %s", msg);
   }
   c->S = S;
   return FT_OK;
@@ -350,7 +366,7 @@ int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx
     lb.counts = p; p += kCountsLen;
     lb.last_T = -1;
   }
-  c->n_chunks = cfg->inter / kDecodeChunk;
+  c->n_chunks = cfg->inter / (cfg->dtype == FT_DTYPE_BF16 ? kDecodeChunk : kDecodeChunkFp4);
   if (cudaMalloc(&c->ypart, sizeof(float) * (size_t)TK * c->n_chunks * cfg->hidden) != cudaSuccess) {
     cudaGetLastError();
     return bail(fail(FT_E_NOMEM, "decode work buffer allocation failed"));
@@ -415,10 +431,9 @@ int ft_cache_control(ft_ctx* c, int layer, const int32_t* ids, int T, ft_step_ou
   if (T < 1 || T > c->cfg.t_max) return fail(FT_E_ARG, "T=%d outside [1, t_max=%d]", T, c->cfg.t_max);
   if (!ids) return fail(FT_E_ARG, "null ids");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  LayerBufs& lb = c->layers[layer];
-  CU(cudaMemcpyAsync(lb.ids, ids, sizeof(int32_t) * T * c->cfg.top_k, cudaMemcpyDeviceToDevice, st));
-  if ((rc = enqueue_control(c, layer, lb.ids, T, st))) return rc;
+  if ((rc = enqueue_control(c, layer, ids, T, st))) return rc;
   fill_out(c, layer, out);
+  if (out) out->ids = const_cast<int32_t*>(ids);  // the control kernel read the caller's routes in place
   return FT_OK;
 }
 
@@ -460,9 +475,10 @@ int ft_moe_forward(ft_ctx* c, int layer, int mode, const float* logits, const ui
   a.tmap_wd = &c->tmap_wd;
   a.tmap_gu = &c->tmap_gu;
   cudaEvent_t pb = c->prof.begin(st);
-  cudaError_t e = launch_decode_experts(a, st);
+  cudaError_t e = c->cfg.dtype == FT_DTYPE_BF16 ? launch_decode_experts(a, st) : launch_decode_experts_mxfp4(a, T, st);
   if (e == cudaErrorNotSupported) return fail(FT_E_UNSUPPORTED, "decode experts for this dtype are not built");
-  if (e == cudaErrorInvalidValue) return fail(FT_E_UNSUPPORTED, "decode experts need d <= 8192 (multiple of 256)");
+  if (e == cudaErrorInvalidValue)
+    return fail(FT_E_UNSUPPORTED, "decode experts need d <= 8192 (bf16) or d a multiple of 512 (MXFP4)");
   CU(e);
   c->prof.end(st, FT_K_EXPERTS, pb);
   pb = c->prof.begin(st);

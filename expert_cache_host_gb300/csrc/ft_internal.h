@@ -22,8 +22,10 @@ constexpr int kMaxSlots = 32768;
 constexpr int kMaxKmax = 1024;
 constexpr int kControlThreads = 1024;
 
-// Rows of the intermediate dimension f handled by one decode GEMV work unit.
+// Rows of the intermediate dimension f handled by one decode work unit
+// (bf16 experts / MXFP4 experts).
 constexpr int kDecodeChunk = 32;
+constexpr int kDecodeChunkFp4 = 64;
 
 // Per-layer fixed-shape step buffers (device).
 struct LayerBufs {
@@ -95,6 +97,8 @@ struct DecodeArgs {
   const CUtensorMap_st* tmap_gu;  // 4-D map (d, f, {gate, up}, slot) over the arena's gate/up projections
 };
 cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st);
+// MXFP4 experts; ypart is [T*k][f/kDecodeChunkFp4][d]; tokens = T of the step.
+cudaError_t launch_decode_experts_mxfp4(const DecodeArgs& a, int tokens, cudaStream_t st);
 
 // out[t] = partial[t] + sum_j [slot_ids >= 0] w[t,j] * sum_c ypart[t*k+j][c]
 cudaError_t launch_merge(const float* ypart, int n_chunks, const int32_t* slot_ids, const float* w,

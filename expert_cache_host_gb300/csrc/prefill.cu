@@ -299,6 +299,8 @@ int prefill_forward(PrefillState* p, int layer, const float* logits, const uint1
   ga.seg_start = p->seg_start;
   ga.status = c.status;
   const int max_mt = (n_routes + 127) / 128 + c.E;
+  if (prof) prof->end(st, FT_K_PREFILL, pb);
+  pb = prof ? prof->begin(st) : nullptr;
   if (e == cudaSuccess) {
     ga.out = p->hbuf;
     ga.out_ld = c.f;
@@ -311,6 +313,8 @@ int prefill_forward(PrefillState* p, int layer, const float* logits, const uint1
     ga.K = c.f;
     e = launch_gemm_down(&p->map_h, &p->map_w2[b], ga, max_mt, c.d, st);
   }
+  if (prof) prof->end(st, FT_K_GEMM, pb);
+  pb = prof ? prof->begin(st) : nullptr;
   if (e == cudaSuccess && cudaEventRecord(p->ev_free[b], st) == cudaSuccess) p->free_recorded[b] = true;
   if (e == cudaSuccess) {
     const int d4 = c.d / 4;

@@ -145,24 +145,11 @@ def fill_pool(pool: np.ndarray, seed: int, L: int, E: int, d: int, f: int, dtype
     return pool
 
 
-def host_alloc(nbytes: int) -> np.ndarray:
-    """Anonymous host memory advised for transparent huge pages, as a uint8 array.
-
-    Huge pages let the GPU stream a pinned, mapped pool over the host link at a
-    higher rate (fewer translations per expert copy); the pages are first touched
-    by whoever writes the pool, before it is pinned."""
-    import mmap
-    m = mmap.mmap(-1, max(1, nbytes), flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
-    if hasattr(mmap, "MADV_HUGEPAGE"):
-        try:
-            m.madvise(mmap.MADV_HUGEPAGE)
-        except OSError:
-            pass
-    return np.frombuffer(m, dtype=np.uint8, count=nbytes)
-
-
-def make_pool(seed, L, E, d, f, dtype, std=0.02, threads=None) -> np.ndarray:
-    pool = host_alloc(L * E * expert_bytes(d, f, dtype))
+def make_pool(seed, L, E, d, f, dtype, std=0.02, threads=None, out: np.ndarray | None = None) -> np.ndarray:
+    """Generate the pool into `out` (a uint8 array of at least L*E*B_x bytes,
+    e.g. a view of pinned host memory) or into a new pageable array."""
+    n = L * E * expert_bytes(d, f, dtype)
+    pool = np.empty(n, dtype=np.uint8) if out is None else out[:n]
     return fill_pool(pool, seed, L, E, d, f, dtype, std, 0, threads)
 
 

@@ -143,7 +143,9 @@ int ft_moe_destroy(ft_ctx* ctx);
 int ft_cache_step(ft_ctx* ctx, int layer, const float* logits_dev, int T, ft_step_out* out, void* stream);
 
 /* The control kernel alone, on routes the caller supplies: ids_dev is [T, k]
- * local expert ids (each token's ids distinct).  Weights are left untouched. */
+ * local expert ids (each token's ids distinct), read in place -- keep it
+ * unchanged until the step's kernels have run (out->ids points to it).
+ * Weights are left untouched. */
 int ft_cache_control(ft_ctx* ctx, int layer, const int32_t* ids_dev, int T, ft_step_out* out, void* stream);
 
 /* Expert FFNs of one layer.
@@ -208,7 +210,8 @@ int ft_route(const float* logits_dev, int T, int E, int k, int32_t* ids_dev, flo
 #define FT_K_EXPERTS 3 /* decode expert kernel */
 #define FT_K_MERGE 4   /* merge kernel */
 #define FT_K_UPLOAD 5  /* prefill full-layer upload, transfer stream */
-#define FT_K_PREFILL 6 /* prefill routing, dispatch and grouped GEMMs */
+#define FT_K_PREFILL 6 /* prefill routing, dispatch, gather and combine */
+#define FT_K_GEMM 7    /* prefill grouped GEMMs (gate/up + down) */
 #define FT_K_COUNT 8
 
 /* Per-kernel timing for measurement.  While on, every kernel or copy the

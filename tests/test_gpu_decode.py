@@ -225,3 +225,26 @@ def test_forward_without_step_is_rejected(ft):
     with pytest.raises(ft.FtError):
         ft.ft_cache_step(ctx, 3, hid.data_ptr(), 1)  # bad layer
     ft.ft_moe_destroy(ctx)
+
+
+# ------------------------------------------------------------------ MXFP4 experts
+
+def test_mxfp4_decode_small(ft):
+    """MXFP4 experts (e2m1 codes uniform over all 16 values, e8m0 scales 119..121)."""
+    model = make_model(2, 16, 2, 512, 128, dtype=1, seed=21)
+    ctx, _, worst = run_decode(ft, model, S=6, K_max=16, r=(1, 1), steps=10)
+    ft.ft_moe_destroy(ctx)
+
+
+def test_mxfp4_decode_batch16_groups(ft):
+    """16 tokens per step, top-6: groups of several routes share one pass over the weights."""
+    model = make_model(1, 32, 6, 1024, 256, dtype=1, seed=22)
+    ctx, _, worst = run_decode(ft, model, S=40, K_max=64, r=(1, 2), steps=4, T=16)
+    ft.ft_moe_destroy(ctx)
+
+
+def test_mxfp4_decode_v4_expert_shape(ft):
+    """d=4096, f=2048 (the V4-Flash-style expert), top-6 of 16 experts, 3 steps."""
+    model = make_model(1, 16, 6, 4096, 2048, dtype=1, seed=23)
+    ctx, _, worst = run_decode(ft, model, S=8, K_max=16, r=(1, 1), steps=3)
+    ft.ft_moe_destroy(ctx)
