@@ -38,6 +38,9 @@ if ROOT not in sys.path:
 import ftsynth  # noqa: E402
 
 METRIC = "MoE decode tok/s (A3B-style, batch 1, GPU side; CPU-routed experts arrive as a partial sum)"
+V4 = dict(L=43, E=256, k=6, d=4096, f=2048, dtype=1, S=2393, K_max=256, T=1, rho=0.9, r=(1, 1),
+          desc="V4-Flash-style decode: 43 layers, d=4096, E=256, top-6, f=2048, MXFP4 experts (147 GB pool), "
+               "S=2393 (32 GB budget), BP/BH=1, K_max=256, AR(1) rho=0.9")
 A3B = dict(L=48, E=128, k=8, d=2048, f=768, dtype=0, S=1536, K_max=128, T=1, rho=0.9, r=(1, 1),
            desc="A3B-style decode: 48 layers, d=2048, E=128, top-8, f=768, bf16, batch 1, "
                 "S=1536 (25% of 6144), BP/BH=1, K_max=128, AR(1) rho=0.9")
@@ -405,21 +408,25 @@ def oracle_decode_rate(w, pool, hid, lg, budget_s, min_tokens=1, max_tokens=None
     bx = ftsynth.expert_bytes(d, f, w["dtype"])
     n_tok = min(hid.shape[0], max_tokens or hid.shape[0])
     cache = oracle.Cache(L * E, w["S"])
-    done, t_spent = 0, 0.0
+    layer_steps, t_spent = 0, 0.0
     for s in range(n_tok):
-        t0 = time.time()
         for l in range(L):
+            t0 = time.time()
             ids, wt = oracle.route(lg[s, l], k)
             ref = cache.step(l, E, ids, w["r"][0], w["r"][1], w["K_max"])
             oracle.moe_forward(pool[l * E * bx:(l + 1) * E * bx], bx, w["dtype"], d, f, ids, wt, hid[s, l],
                                slot_ids=ref.slot_ids.reshape(T, k))
-        t_spent += time.time() - t0
-        done += 1
-        if done >= min_tokens and t_spent >= budget_s:
-            break
+            t_spent += time.time() - t0
+            layer_steps += 1
+            if layer_steps >= min_tokens * L and t_spent >= budget_s:
+                break
+        else:
+            continue
+        break
     # the expert evaluations of one layer run in parallel over its T*k routes
     threads = min(oracle.threads(), T * k)
-    return done * T / t_spent, done, t_spent, threads
+    tokens = layer_steps / L
+    return tokens * T / t_spent, tokens, t_spent, threads
 
 
 def run_reference(args, w):
@@ -428,7 +435,7 @@ def run_reference(args, w):
     hid, lg = decode_inputs(w, max(2, min(args.steps, 64)))
     rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, args.ref_budget_s, min_tokens=max(1, min(args.steps, 2)),
                                               max_tokens=max(1, args.steps))
-    sample = f"{n} decode tokens x {w['L']} layers from a cold cache ({t:.1f} s of oracle work)"
+    sample = f"{n:.2f} decode tokens x {w['L']} layers from a cold cache ({t:.1f} s of oracle work)"
     return {
         "impl": "reference", "metric": METRIC, "value": round(rate, 5), "unit": "tok/s", "n_gpus": 1, "steps": n,
         "warmup": 0, "ms_per_step": round(t / max(1, n) * 1e3, 2), "higher_is_better": True, "scaling": "weak",
@@ -445,9 +452,11 @@ def build_line(args, w, world, dec, link_gbs, pre, ctl, peaks):
     fill_gbs = dec["fill_bytes"] / (dec["fill_ms"] / 1e3) / 1e9 if dec["fill_ms"] else 0.0
     bx = ftsynth.expert_bytes(w["d"], w["f"], w["dtype"])
     line = {
-        "metric": METRIC, "value": round(dec["value"], 3), "unit": "tok/s", "n_gpus": world, "steps": dec["K"],
+        "metric": METRIC if w["dtype"] == 0 else METRIC.replace("A3B-style, batch 1", f"V4-Flash-style MXFP4, batch {w['T']}"),
+        "value": round(dec["value"], 3), "unit": "tok/s", "n_gpus": world, "steps": dec["K"],
         "warmup": dec["W"], "ms_per_step": round(dec["elapsed"] / dec["K"] * 1e3, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w["dtype"] == 0 else "e2m1*e8m0 x bf16 -> f16/f32",
+        "data": "synthetic",
         "config": {"workload": w["desc"], "graph": "one CUDA graph per token", "batch": dec["T"],
                    "l2": "inputs larger than L2: %.2f GB of expert weights per token" % (w["L"] * w["k"] * bx / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
@@ -514,13 +523,33 @@ def main():
     ap.add_argument("--prefill-tokens", type=int, default=8192)
     ap.add_argument("--prefill-layers", type=int, default=0)
     ap.add_argument("--control-steps", type=int, default=10000)
+    ap.add_argument("--prefill-only", action="store_true", help="profiling case: the prefill leg alone")
+    ap.add_argument("--workload", choices=("a3b", "v4"), default="a3b",
+                    help="a3b: bf16 A3B-style decode (default line); v4: MXFP4 V4-Flash-style decode")
+    ap.add_argument("--batch", type=int, default=0, help="decode tokens per step (default 1)")
     ap.add_argument("--layers", type=int, default=0, help="override L (small profiling cases, not a bench line)")
     ap.add_argument("--slots", type=int, default=0, help="override S (small profiling cases, not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
-    w = dict(A3B)
+    w = dict(A3B if args.workload == "a3b" else V4)
+    if args.batch:
+        w["T"] = args.batch
+        w["desc"] = w["desc"].replace("batch 1, ", "") + f", batch {args.batch}"
+    if args.workload == "v4":
+        # keep the per-layer shapes; drop layers only if the host cannot hold the pinned pool
+        avail = 0
+        with open("/proc/meminfo") as fh:
+            for line in fh:
+                if line.startswith("MemAvailable:"):
+                    avail = int(line.split()[1]) * 1024
+        per_layer = w["E"] * ftsynth.expert_bytes(w["d"], w["f"], 1)
+        fit = int(max(0, avail - (24 << 30)) // per_layer)
+        if fit < w["L"]:
+            w["L"] = max(1, fit)
+            w["desc"] += f" [host RAM holds {w['L']} of the 43 layers]"
+        args.no_prefill = args.no_control = True
     if args.layers or args.slots:
         w["L"], w["S"] = args.layers or w["L"], args.slots or w["S"]
         w["desc"] += f" [profiling case: L={w['L']}, S={w['S']}]"
@@ -545,12 +574,15 @@ def main():
     from expert_cache_host_gb300 import build as ftbuild
     ftbuild.build()
     torch.cuda.set_device(local)
-    # The pool is written into memory that is already pinned (cudaHostAlloc through
-    # torch): over NVLink-C2C it streams ~5-15% faster than malloc'd pages pinned
-    # after the write, and much faster on first touch than huge-page-advised pages.
-    pool_t = torch.empty(w["L"] * w["E"] * ftsynth.expert_bytes(w["d"], w["f"], w["dtype"]), dtype=torch.uint8,
-                         pin_memory=True)
-    pool = ftsynth.make_pool(0, w["L"], w["E"], w["d"], w["f"], w["dtype"], 0.02, out=pool_t.numpy())
+    if args.prefill_only:
+        # profiling case: the prefill leg alone on the first --prefill-layers layers (not a bench line)
+        w["L"] = args.prefill_layers or w["L"]
+        pool = ftsynth.make_pool(0, w["L"], w["E"], w["d"], w["f"], 0, 0.02)
+        print(json.dumps({"profiling_case": "prefill", **run_prefill_leg(args, w, pool)}), flush=True)
+        return
+    # The pool is written into pageable memory and pinned by ft_moe_init afterwards
+    # (pin after write, the fast-start order of the method).
+    pool = ftsynth.make_pool(0, w["L"], w["E"], w["d"], w["f"], w["dtype"], 0.02)
     hid, lg = decode_inputs(w, args.warmup + args.steps + min(args.steps, args.profile_steps)
                             + min(args.steps, args.e2e_steps))
     dec = run_decode_leg(args, w, world, local, pool, hid, lg)
@@ -560,10 +592,10 @@ def main():
         import expert_cache_host_gb300 as ft
         # the pool is registered (pinned, mapped) for the measurement below by a throwaway context
         cfg = ft.make_config(num_layers=w["L"], num_experts=w["E"], top_k=w["k"], hidden=w["d"], inter=w["f"],
-                             num_slots=1, k_max=1, t_max=1)
+                             dtype=w["dtype"], num_slots=1, k_max=1, t_max=1)
         ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
         try:
-            link = link_peak_gbs(pool, w["E"] * ftsynth.expert_bytes(w["d"], w["f"], 0))
+            link = link_peak_gbs(pool, w["E"] * ftsynth.expert_bytes(w["d"], w["f"], w["dtype"]))
         finally:
             ft.ft_moe_destroy(ctx)
         if not args.no_prefill and not args.layers:
@@ -574,9 +606,10 @@ def main():
     if rank == 0:
         line = build_line(args, w, world, dec, link, pre, ctl, peaks)
         if not args.no_cpu_baseline:
-            rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, args.cpu_budget_s)
+            rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, args.cpu_budget_s,
+                                                     min_tokens=1.0 if w["T"] == 1 else 1.0 / w["L"])
             line["cpu_baseline"] = {"value": round(rate, 5), "unit": "tok/s", "cores": threads, "kind": "oracle",
-                                    "sample": f"{n} decode tokens x {w['L']} layers from a cold cache, "
+                                    "sample": f"{n:.2f} decode tokens x {w['L']} layers from a cold cache, "
                                               f"{t:.1f} s of oracle work"}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -49,7 +49,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* accb = empty + NSTAGE;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
 
-  const int mt = blockIdx.x, nt = blockIdx.y;
+  // N tiles of one M tile are adjacent in launch order (the activation tile is
+  // re-read from L2, not DRAM), and the few M tiles of one expert follow each
+  // other (its weight tiles stay in L2 too).
+  const int nt = blockIdx.x, mt = blockIdx.y;
   if (mt >= *a.n_mtiles) return;
   const int e = a.tile_expert[mt], r0 = a.tile_row0[mt], r_end = a.seg_start[e + 1];
   const int n0 = nt * C::BN;
@@ -174,7 +177,7 @@ cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const Gem
     if (e != cudaSuccess) return e;
     configured = dev;
   }
-  dim3 grid(max_mtiles, N / C::BN);
+  dim3 grid(N / C::BN, max_mtiles);
   grouped_gemm_kernel<MODE><<<grid, kThreads, C::SMEM, st>>>(*map_a, *map_b, a);
   return cudaGetLastError();
 }
