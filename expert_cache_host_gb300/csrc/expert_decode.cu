@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   int s = 0;
   uint32_t ph = 0;
   auto release = [&]() {
+    proxy_fence_reads();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     if (++s == NS) {

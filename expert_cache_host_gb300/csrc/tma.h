@@ -33,6 +33,12 @@ __device__ __forceinline__ void mbar_init_fence() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// A ring stage read with ordinary shared-memory loads is refilled by TMA, which
+// writes through the async proxy: order this thread's reads before any later
+// async-proxy write of the stage (write-after-read across proxies).  Without
+// it a slow load can still be pending when the refill lands.
+__device__ __forceinline__ void proxy_fence_reads() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(smem_u32(bar)),
                "r"(bytes)
