@@ -48,7 +48,7 @@ L2_BYTES = 129 * 2 ** 20
 
 # DRAM bytes per launch from ncu captures (profiles/); None once the kernel changed.
 NCU_TRAFFIC = {
-    "decode_experts": 75_544_832 + 1_589_248,  # profiles/decode_experts_a3b.md, one A3B layer, 8 experts
+    "decode_experts": None,  # not re-captured since the kernel last changed
 }
 
 
@@ -482,7 +482,8 @@ def build_line(args, w, world, dec, link_gbs, pre, ctl, peaks):
         "clocks": dec["clocks"],
         "e2e": {"value": round(dec["e2e"], 3), "unit": "tok/s", "h2d_bytes_per_step": dec["h2d"],
                 "d2h_bytes_per_step": dec["d2h"]},
-        "gpu_launches": int(dec["K"] * w["L"] * 5),
+        # per layer: route, control, fill, resident experts, installed experts, merge
+        "gpu_launches": int(dec["K"] * w["L"] * 6),
     }
     if pre:
         line["prefill"] = {

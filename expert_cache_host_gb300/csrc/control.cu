@@ -37,6 +37,7 @@ struct Smem {
   int gstart[kMaxExperts];   // first group_routes index of the expert's group
   int cursor[kMaxExperts];   // scatter cursor per expert
   int miss_local[kMaxExperts];
+  int filled[kMaxExperts];   // 1 if the expert is installed by this step's fill
   int victims[kMaxKmax];
   int eqsel[kMaxKmax];
   unsigned long long cand[kMaxKmax];  // (last_use << 32 | slot) below the threshold
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
     sm.ecount[e] = 0;
     sm.emap[e] = -1;
     sm.cursor[e] = 0;
+    sm.filled[e] = 0;
   }
   for (int s = tid; s < S; s += NT) lu[s] = a.last_use[s];
   __syncthreads();
@@ -286,6 +288,7 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
     a.fetch[i] = u;
     a.victims[i] = s;
     sm.emap[le] = s;
+    sm.filled[le] = 1;
   }
   for (int i = q + tid; i < m; i += NT) a.cpu_list[i - q] = base_id + sm.miss_local[i];
   const int evictions = __syncthreads_count(my_evict);
@@ -304,6 +307,7 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   if (resident) {
     int gi = ex3 >> 16, off = ex3 & 0xFFFF;
     a.group_slot[gi] = sm.emap[e];
+    a.group_new[gi] = sm.filled[e];
     a.group_off[gi] = off;
     sm.gstart[e] = off;
   }

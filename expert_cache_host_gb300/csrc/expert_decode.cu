@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int c = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
   if (g >= a.counts[5]) return;
+  // select 1: only experts resident before the step; 2: only those it installed
+  if (a.select != 0 && (a.group_new[g] != 0) != (a.select == 2)) return;
   const int slot = a.group_slot[g];
   if ((unsigned)slot >= (unsigned)a.S) {
     if (tid == 0) atomicOr(a.status, FT_ST_BAD_SLOT);

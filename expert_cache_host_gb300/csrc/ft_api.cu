@@ -224,6 +224,7 @@ int enqueue_control(ft_ctx* c, int layer, const int32_t* ids, int T, cudaStream_
   a.cpu_list = lb.cpu_list;
   a.counts = lb.counts;
   a.group_slot = lb.group_slot;
+  a.group_new = lb.group_new;
   a.group_off = lb.group_off;
   a.group_routes = lb.group_routes;
   cudaEvent_t pb = c->prof.begin(st);
@@ -255,8 +256,10 @@ int enqueue_fill(ft_ctx* c, int layer, cudaStream_t st) {
   cudaEvent_t pb = nullptr;
   if (c->cfg.fill_mode == FT_FILL_KERNEL) {
     pb = c->prof.begin(c->xfer);
+    // one CTA per SM saturates the host link and leaves room on every SM for
+    // the resident experts that run meanwhile
     CU(launch_fill(c->pool_dev, c->arena, lb.counts, lb.fetch, lb.victims, c->Bx, c->S, c->E_tot, c->status,
-                   4 * c->sm_count, c->xfer));
+                   c->sm_count, c->xfer));
   } else {
     // Copy-engine fills need the fetch list on the host: this reads it back.
     CU(cudaMemcpyAsync(c->h_counts, lb.counts, sizeof(int32_t) * kCountsLen, cudaMemcpyDeviceToHost, c->xfer));
@@ -273,8 +276,7 @@ int enqueue_fill(ft_ctx* c, int layer, cudaStream_t st) {
     }
   }
   c->prof.end(c->xfer, FT_K_FILL, pb);
-  CU(cudaEventRecord(c->ev_join, c->xfer));
-  CU(cudaStreamWaitEvent(st, c->ev_join, 0));
+  CU(cudaEventRecord(c->ev_join, c->xfer));  // the caller's stream waits on it before the installed experts run
   return FT_OK;
 }
 
@@ -340,8 +342,9 @@ int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx
 
   // per-layer step buffers, one allocation
   const int E = cfg->num_experts, TK = cfg->t_max * cfg->top_k, K = cfg->k_max;
-  const size_t per_layer_words = (size_t)TK * 4 /*ids w slot_ids group_routes*/ + (size_t)E * 4 /*uniq hit cpu gslot*/ +
-                                 (E + 1) /*goff*/ + (size_t)K * 3 + kCountsLen;
+  const size_t per_layer_words = (size_t)TK * 4 /*ids w slot_ids group_routes*/ +
+                                 (size_t)E * 5 /*uniq hit cpu gslot gnew*/ + (E + 1) /*goff*/ + (size_t)K * 3 +
+                                 kCountsLen;
   const size_t per_layer = (per_layer_words * 4 + 255) / 256 * 256;
   if (cudaMalloc(&c->layer_mem, per_layer * cfg->num_layers) != cudaSuccess) {
     cudaGetLastError();
@@ -359,6 +362,7 @@ int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx
     lb.hit_list = p; p += E;
     lb.cpu_list = p; p += E;
     lb.group_slot = p; p += E;
+    lb.group_new = p; p += E;
     lb.group_off = p; p += E + 1;
     lb.fetch = p; p += K;
     lb.victims = p; p += K;
@@ -455,6 +459,8 @@ int ft_moe_forward(ft_ctx* c, int layer, int mode, const float* logits, const ui
   if (mode != FT_DECODE_CACHED) return fail(FT_E_ARG, "unknown mode %d", mode);
   LayerBufs& lb = c->layers[layer];
   if (lb.last_T != T) return fail(FT_E_STATE, "decode forward of layer %d with T=%d needs a cache step with the same T", layer, T);
+  // The fill runs on the transfer stream; experts already resident run
+  // meanwhile on the caller's stream, those the step installs after the fill.
   if ((rc = enqueue_fill(c, layer, st))) return rc;
   DecodeArgs a{};
   a.arena = c->arena;
@@ -469,18 +475,24 @@ int ft_moe_forward(ft_ctx* c, int layer, int mode, const float* logits, const ui
   a.group_slot = lb.group_slot;
   a.group_off = lb.group_off;
   a.group_routes = lb.group_routes;
+  a.group_new = lb.group_new;
   a.hidden = hidden;
   a.ypart = c->ypart;
   a.status = c->status;
   a.tmap_wd = &c->tmap_wd;
   a.tmap_gu = &c->tmap_gu;
-  cudaEvent_t pb = c->prof.begin(st);
-  cudaError_t e = c->cfg.dtype == FT_DTYPE_BF16 ? launch_decode_experts(a, st) : launch_decode_experts_mxfp4(a, T, st);
-  if (e == cudaErrorNotSupported) return fail(FT_E_UNSUPPORTED, "decode experts for this dtype are not built");
-  if (e == cudaErrorInvalidValue)
-    return fail(FT_E_UNSUPPORTED, "decode experts need d <= 8192 (bf16) or d a multiple of 512 (MXFP4)");
-  CU(e);
-  c->prof.end(st, FT_K_EXPERTS, pb);
+  cudaEvent_t pb = nullptr;
+  for (int sel = 1; sel <= 2; ++sel) {
+    if (sel == 2) CU(cudaStreamWaitEvent(st, c->ev_join, 0));
+    a.select = sel;
+    pb = c->prof.begin(st);
+    cudaError_t e = c->cfg.dtype == FT_DTYPE_BF16 ? launch_decode_experts(a, st) : launch_decode_experts_mxfp4(a, T, st);
+    if (e == cudaErrorNotSupported) return fail(FT_E_UNSUPPORTED, "decode experts for this dtype are not built");
+    if (e == cudaErrorInvalidValue)
+      return fail(FT_E_UNSUPPORTED, "decode experts need d <= 8192 (bf16) or d a multiple of 512 (MXFP4)");
+    CU(e);
+    c->prof.end(st, FT_K_EXPERTS, pb);
+  }
   pb = c->prof.begin(st);
   CU(launch_merge(c->ypart, c->n_chunks, lb.slot_ids, lb.w, partial, out, T, c->cfg.top_k, c->cfg.hidden, st));
   c->prof.end(st, FT_K_MERGE, pb);

@@ -40,6 +40,7 @@ struct LayerBufs {
   int32_t* cpu_list;
   int32_t* counts;
   int32_t* group_slot;
+  int32_t* group_new;  // 1 if the group's expert is installed by this step's fill
   int32_t* group_off;
   int32_t* group_routes;
   int last_T;  // T of the last step (host-side record, -1 = none)
@@ -64,6 +65,7 @@ struct ControlArgs {
   int32_t* cpu_list;
   int32_t* counts;
   int32_t* group_slot;
+  int32_t* group_new;
   int32_t* group_off;
   int32_t* group_routes;
 };
@@ -95,6 +97,11 @@ struct DecodeArgs {
   uint32_t* status;
   const CUtensorMap_st* tmap_wd;  // 3-D map (f, d, slot) over the arena's down projections
   const CUtensorMap_st* tmap_gu;  // 4-D map (d, f, {gate, up}, slot) over the arena's gate/up projections
+  // Group selection, so that experts resident before the step can run while
+  // the step's fill is still in flight: 0 = every group; 1 = groups with
+  // group_new[g] == 0; 2 = groups with group_new[g] != 0.
+  const int32_t* group_new;
+  int select;
 };
 cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st);
 // MXFP4 experts; ypart is [T*k][f/kDecodeChunkFp4][d]; tokens = T of the step.

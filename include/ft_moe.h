@@ -151,8 +151,9 @@ int ft_cache_control(ft_ctx* ctx, int layer, const int32_t* ids_dev, int T, ft_s
 /* Expert FFNs of one layer.
  *  mode FT_DECODE_CACHED: uses the last ft_cache_step of `layer` (same T);
  *    fills the q fetched experts into their slots on the context's transfer
- *    stream, joined back into `stream`, then runs the routed SwiGLU experts
- *    of every route with a slot and merges:
+ *    stream; meanwhile runs on `stream` the routed SwiGLU experts that were
+ *    resident before the step, then (after joining the fill into `stream`)
+ *    the experts the step installed, and merges:
  *      out[t] = partial[t] + sum_j w[t,j] * y_{ids[t,j]}(hidden[t])   (slot >= 0)
  *    logits_dev is ignored.
  *  mode FT_PREFILL_LAYER: routes logits_dev itself (no cache access; the

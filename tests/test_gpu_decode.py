@@ -248,3 +248,20 @@ def test_mxfp4_decode_v4_expert_shape(ft):
     model = make_model(1, 16, 6, 4096, 2048, dtype=1, seed=23)
     ctx, _, worst = run_decode(ft, model, S=8, K_max=16, r=(1, 1), steps=3)
     ft.ft_moe_destroy(ctx)
+
+
+# ------------------------------------------------------------------ mixed hit / fill steps
+
+def test_mixed_steps_a3b_expert_shape(ft):
+    """A3B expert shape over steps that both hit and fill: the resident experts
+    stream from HBM through the TMA ring while the fill kernel shares their SMs
+    (a ring stage must not be refilled before its ordinary loads are done)."""
+    model = make_model(2, 128, 8, 2048, 768, seed=32)
+    ctx, cache, _ = run_decode(ft, model, S=20, K_max=128, r=(1, 1), steps=6)
+    so, eo, lu, now = ft.ft_get_table(ctx, 256, 20)
+    bx = model.bx
+    for s in range(20):
+        if eo[s] >= 0:
+            got = dev_view(ft.ft_slot_ptr(ctx, s), (bx,), "|u1").cpu().numpy()
+            assert np.array_equal(got, model.pool[int(eo[s]) * bx:(int(eo[s]) + 1) * bx]), f"slot {s}"
+    ft.ft_moe_destroy(ctx)
