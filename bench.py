@@ -447,6 +447,19 @@ def run_reference(args, w):
 
 # ----------------------------------------------------------------------------- main
 
+def make_host_pool(args, w):
+    """The expert pool, written in the canonical layout.  "pinned": into
+    ft_host_alloc memory (mapped in the GPU page tables before the write);
+    "registered": into pageable memory that ft_moe_init pins after the write.
+    Returns (HostPool or None, uint8 array, seconds to allocate and write)."""
+    import expert_cache_host_gb300 as ft
+    t0 = time.time()
+    n = w["L"] * w["E"] * ftsynth.expert_bytes(w["d"], w["f"], w["dtype"])
+    hp = ft.HostPool(n) if args.pool == "pinned" else None
+    pool = ftsynth.make_pool(0, w["L"], w["E"], w["d"], w["f"], w["dtype"], 0.02, out=hp.array if hp else None)
+    return hp, pool, time.time() - t0
+
+
 def build_line(args, w, world, dec, link_gbs, pre, ctl, peaks):
     ex_gbs = dec["ex_bytes"] / (dec["ex_ms"] / 1e3) / 1e9 if dec["ex_ms"] else 0.0
     fill_gbs = dec["fill_bytes"] / (dec["fill_ms"] / 1e3) / 1e9 if dec["fill_ms"] else 0.0
@@ -530,6 +543,9 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="decode tokens per step (default 1)")
     ap.add_argument("--layers", type=int, default=0, help="override L (small profiling cases, not a bench line)")
     ap.add_argument("--slots", type=int, default=0, help="override S (small profiling cases, not a bench line)")
+    ap.add_argument("--pool", choices=("pinned", "registered"), default="pinned",
+                    help="pinned: pool written into ft_host_alloc memory; registered: pageable pool pinned by "
+                         "ft_moe_init after the write")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -578,12 +594,14 @@ def main():
     if args.prefill_only:
         # profiling case: the prefill leg alone on the first --prefill-layers layers (not a bench line)
         w["L"] = args.prefill_layers or w["L"]
-        pool = ftsynth.make_pool(0, w["L"], w["E"], w["d"], w["f"], 0, 0.02)
+        w["dtype"] = 0
+        hp, pool, _ = make_host_pool(args, w)
         print(json.dumps({"profiling_case": "prefill", **run_prefill_leg(args, w, pool)}), flush=True)
+        if hp:
+            del pool
+            hp.free()
         return
-    # The pool is written into pageable memory and pinned by ft_moe_init afterwards
-    # (pin after write, the fast-start order of the method).
-    pool = ftsynth.make_pool(0, w["L"], w["E"], w["d"], w["f"], w["dtype"], 0.02)
+    hp, pool, t_pool = make_host_pool(args, w)
     hid, lg = decode_inputs(w, args.warmup + args.steps + min(args.steps, args.profile_steps)
                             + min(args.steps, args.e2e_steps))
     dec = run_decode_leg(args, w, world, local, pool, hid, lg)
@@ -612,7 +630,11 @@ def main():
             line["cpu_baseline"] = {"value": round(rate, 5), "unit": "tok/s", "cores": threads, "kind": "oracle",
                                     "sample": f"{n:.2f} decode tokens x {w['L']} layers from a cold cache, "
                                               f"{t:.1f} s of oracle work"}
+        line["config"]["pool"] = (f"{args.pool}: {pool.nbytes / 1e9:.2f} GB, allocated and written in {t_pool:.1f} s")
         print(json.dumps(line), flush=True)
+    if hp:
+        del pool
+        hp.free()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -28,7 +28,8 @@ COUNTS = ("n", "hits", "m", "q", "cpu", "n_groups", "now")
 EXPORTS = (
     "ft_moe_init", "ft_moe_destroy", "ft_cache_step", "ft_cache_control", "ft_moe_forward", "ft_cache_rebuild",
     "ft_get_status", "ft_get_counters", "ft_get_table", "ft_slot_ptr", "ft_get_epoch", "ft_num_slots", "ft_route",
-    "ft_profile_enable", "ft_profile_read", "ft_decode_experts_noalloc", "ft_last_error",
+    "ft_profile_enable", "ft_profile_read", "ft_decode_experts_noalloc", "ft_host_alloc", "ft_host_free",
+    "ft_last_error",
 )
 FT_K_ROUTE, FT_K_CONTROL, FT_K_FILL, FT_K_EXPERTS, FT_K_MERGE, FT_K_UPLOAD, FT_K_PREFILL, FT_K_GEMM = range(8)
 FT_K_COUNT = 8
@@ -88,6 +89,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "ft_profile_enable": ([vp, i32], i32),
             "ft_profile_read": ([vp, vp, vp, i32], i32),
             "ft_decode_experts_noalloc": ([vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp], i32),
+            "ft_host_alloc": ([sz, ctypes.POINTER(vp)], i32),
+            "ft_host_free": ([vp], i32),
             "ft_last_error": ([], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -213,6 +216,25 @@ def ft_decode_experts_noalloc(arena_ptr: int, num_slots: int, hidden: int, inter
     _chk(load().ft_decode_experts_noalloc(v(arena_ptr), num_slots, hidden, inter, top_k, T, v(slot_ids_ptr),
                                           v(weights_ptr), v(hidden_ptr), v(partial_ptr or None), v(out_ptr),
                                           v(status_ptr or None), v(stream)))
+
+
+class HostPool:
+    """Pinned, device-mapped host memory from ft_host_alloc, viewed as a uint8
+    numpy array (``.array``).  Free it (``.free()``) only after every context
+    using it has been destroyed; the array must not be used afterwards."""
+
+    def __init__(self, nbytes: int):
+        import numpy as np
+        p = ctypes.c_void_p()
+        _chk(load().ft_host_alloc(nbytes, ctypes.byref(p)))
+        self.ptr, self.nbytes = p.value, nbytes
+        self.array = np.ctypeslib.as_array((ctypes.c_uint8 * nbytes).from_address(self.ptr))
+
+    def free(self) -> None:
+        if self.ptr:
+            self.array = None
+            _chk(load().ft_host_free(ctypes.c_void_p(self.ptr)))
+            self.ptr = 0
 
 
 def ft_last_error() -> str:

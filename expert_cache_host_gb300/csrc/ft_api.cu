@@ -414,6 +414,24 @@ int ft_moe_destroy(ft_ctx* c) {
   return FT_OK;
 }
 
+int ft_host_alloc(size_t bytes, void** out) {
+  if (!out || bytes == 0) return fail(FT_E_ARG, "ft_host_alloc needs bytes > 0 and an output pointer");
+  *out = nullptr;
+  cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *out = nullptr;
+    return fail(FT_E_PIN, "cudaHostAlloc of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
+  }
+  return FT_OK;
+}
+
+int ft_host_free(void* p) {
+  if (!p) return FT_OK;
+  CU(cudaFreeHost(p));
+  return FT_OK;
+}
+
 int ft_cache_step(ft_ctx* c, int layer, const float* logits, int T, ft_step_out* out, void* stream) {
   int rc = check_layer(c, layer);
   if (rc) return rc;

@@ -135,6 +135,21 @@ int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx
  * the context's streams.  NULL is accepted. */
 int ft_moe_destroy(ft_ctx* ctx);
 
+/* Pinned, device-mapped host memory for a pool (cudaHostAlloc, mapped and
+ * portable), for callers that write the pool into memory that is already
+ * pinned instead of pinning it after the write.  The pages are mapped in the
+ * GPU's own page tables when the call returns, so the host link streams them
+ * at full rate from the first read; registered pageable memory can read
+ * slowly the first time each page is touched.  The cost moves to start-up:
+ * the whole range is faulted in here.  *out receives the host address (the
+ * device view is the one ft_moe_init takes by itself).  The caller owns the
+ * memory and frees it with ft_host_free after destroying every context that
+ * uses it.  Errors: FT_E_ARG (bytes == 0 or out == NULL), FT_E_PIN. */
+int ft_host_alloc(size_t bytes, void** out);
+
+/* Free memory from ft_host_alloc.  NULL is accepted.  Errors: FT_E_CUDA. */
+int ft_host_free(void* p);
+
 /* Routing + cache control for one decode step of `layer`: logits_dev is
  * [T, E] float32 row-major, 1 <= T <= t_max.  Enqueues the routing kernel and
  * the control kernel on `stream`; no host synchronisation, so the call can be

@@ -59,3 +59,11 @@ def test_route_shape_rejected_on_host(lib):
     with pytest.raises(ft.FtError) as ei:
         ft.ft_route(8, 4, 2000, 2, 8, 8)
     assert ei.value.code == ft.FT_E_ARG
+
+
+def test_host_alloc_arguments_checked_on_host(lib):
+    import ctypes
+    p = ctypes.c_void_p()
+    assert lib.ft_host_alloc(0, ctypes.byref(p)) == ft.FT_E_ARG
+    assert lib.ft_host_alloc(4096, None) == ft.FT_E_ARG
+    assert lib.ft_host_free(None) == ft.FT_OK
