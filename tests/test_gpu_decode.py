@@ -265,3 +265,21 @@ def test_mixed_steps_a3b_expert_shape(ft):
             got = dev_view(ft.ft_slot_ptr(ctx, s), (bx,), "|u1").cpu().numpy()
             assert np.array_equal(got, model.pool[int(eo[s]) * bx:(int(eo[s]) + 1) * bx]), f"slot {s}"
     ft.ft_moe_destroy(ctx)
+
+
+# ------------------------------------------------------------------ pool in memory pinned before the write
+
+def test_decode_from_host_alloc_pool(ft):
+    """A pool written into ft_host_alloc memory is used as is (no registration)
+    and gives the same answers; the memory outlives the context."""
+    from harness import Model
+    L, E, k, d, f = 2, 16, 2, 256, 128
+    hp = ft.HostPool(L * E * ftsynth.expert_bytes(d, f, 0))
+    try:
+        pool = ftsynth.make_pool(41, L, E, d, f, 0, out=hp.array)
+        model = Model(L, E, k, d, f, 0, pool, ftsynth.router_weights(41, L, E, d, 0.02), 41)
+        ctx, _, _ = run_decode(ft, model, S=6, K_max=16, r=(1, 1), steps=6)
+        ft.ft_moe_destroy(ctx)
+        assert np.array_equal(hp.array[:64], ftsynth.make_pool(41, L, E, d, f, 0)[:64])  # still mapped and intact
+    finally:
+        hp.free()  # nothing above holds the context any more
