@@ -490,7 +490,7 @@ def build_line(args, w, world, dec, link_gbs, pre, ctl, peaks):
                              "share": dec["shares"].get("experts")},
         "components": {
             "kernel_share": dec["shares"], "kernel_ms_per_token": dec["ms_per_token"],
-            "control_us_per_layer_step": round(dec["control_us"], 3), "route_us_per_layer_step": round(dec["route_us"], 3),
+            "route_control_us_per_layer_step": round(dec["control_us"], 3),
             "hit_rate": round(dec["hits"] / max(1.0, dec["hits"] + dec["misses"]), 4),
             "fills_per_token": round(dec["fills"] / dec["K"], 3), "cpu_routes_per_token": round(dec["cpu"] / dec["K"], 3),
             "eager_ms_per_token_profiled": round(dec["eager_ms"], 4) if dec["eager_ms"] else None,
@@ -499,8 +499,8 @@ def build_line(args, w, world, dec, link_gbs, pre, ctl, peaks):
         "clocks": dec["clocks"],
         "e2e": {"value": round(dec["e2e"], 3), "unit": "tok/s", "h2d_bytes_per_step": dec["h2d"],
                 "d2h_bytes_per_step": dec["d2h"]},
-        # per layer: route, control, fill, resident experts, installed experts, merge
-        "gpu_launches": int(dec["K"] * w["L"] * 6),
+        # per layer: route + control (one kernel), fill, resident experts, installed experts, merge
+        "gpu_launches": int(dec["K"] * w["L"] * 5),
     }
     if pre:
         line["prefill"] = {

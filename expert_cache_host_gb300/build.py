@@ -43,7 +43,8 @@ def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    deps = _sources() + glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(ROOT, "include", "ft_moe.h"), __file__]
+    deps = (_sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) +
+            [os.path.join(ROOT, "include", "ft_moe.h"), __file__])
     return any(os.path.getmtime(p) > t for p in deps)
 
 

@@ -24,6 +24,7 @@
 //  6. rewrite route ids to slot ids (-1 = CPU);
 //  7. group the routes by resident expert for the expert kernel (dispatch).
 #include "ft_internal.h"
+#include "route_warp.cuh"
 
 namespace ft {
 namespace {
@@ -74,6 +75,9 @@ __device__ __forceinline__ int block_scan(int v, int* wsum, int* total) {
   return base + x - v;
 }
 
+// RP > 0: route the step's tokens first (one warp per token, RP logits per
+// lane); RP = 0: the routes are given.
+template <int RP>
 __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   extern __shared__ __align__(16) unsigned char dyn[];
   Smem& sm = *reinterpret_cast<Smem*>(dyn);
@@ -81,6 +85,13 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   const int tid = threadIdx.x;
   const int E = a.E, S = a.S;
   const int base_id = a.layer * E;
+
+  if constexpr (RP > 0) {
+    // 0. routing; the __syncthreads below makes the routes visible to the block
+    for (int t = tid >> 5; t < a.T; t += NW)
+      route_token<RP>(a.logits + (size_t)t * E, E, a.k, a.ids_out + (size_t)t * a.k, a.w_out + (size_t)t * a.k,
+                      a.status, nullptr);
+  }
 
   const unsigned now0 = *a.now;
   const bool wrap = now0 == 0xFFFFFFFFu;
@@ -344,19 +355,32 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
 
 size_t control_smem_bytes(int S) { return sizeof(Smem) + sizeof(unsigned) * (size_t)S; }
 
-cudaError_t launch_control(const ControlArgs& a, cudaStream_t st) {
-  size_t smem = control_smem_bytes(a.S);
+namespace {
+template <int RP>
+cudaError_t launch_rp(const ControlArgs& a, cudaStream_t st) {
+  const size_t smem = control_smem_bytes(a.S);
   static thread_local int configured_for = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_for != dev) {
-    cudaError_t e = cudaFuncSetAttribute(control_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(control_kernel<RP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)control_smem_bytes(kMaxSlots));
     if (e != cudaSuccess) return e;
     configured_for = dev;
   }
-  control_kernel<<<1, NT, smem, st>>>(a);
+  control_kernel<RP><<<1, NT, smem, st>>>(a);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_control(const ControlArgs& a, cudaStream_t st) {
+  if (!a.logits) return launch_rp<0>(a, st);
+  if (a.ids != a.ids_out || a.T * a.k != a.n_routes) return cudaErrorInvalidValue;
+  const int per = (a.E + 31) / 32;
+  if (per <= 1) return launch_rp<1>(a, st);
+  if (per <= 4) return launch_rp<4>(a, st);
+  if (per <= 8) return launch_rp<8>(a, st);
+  return launch_rp<kMaxExperts / 32>(a, st);
 }
 
 }  // namespace ft

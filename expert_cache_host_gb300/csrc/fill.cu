@@ -48,6 +48,18 @@ __global__ void __launch_bounds__(kFillThreads)
 cudaError_t launch_fill(const uint8_t* pool_dev, uint8_t* arena, const int32_t* counts, const int32_t* fetch,
                         const int32_t* victims, size_t Bx, int S, int E_tot, uint32_t* status, int grid,
                         cudaStream_t st) {
+  // The fill needs no shared memory, but the expert kernel that runs beside it
+  // needs ~100 KB per CTA: keep the SMs in the largest shared-memory split, or
+  // an SM running a fill CTA cannot take an expert CTA until it drains.
+  static thread_local int configured_for = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_for != dev) {
+    cudaError_t e = cudaFuncSetAttribute(fill_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    configured_for = dev;
+  }
   fill_kernel<<<grid, kFillThreads, 0, st>>>(reinterpret_cast<const int4*>(pool_dev), reinterpret_cast<int4*>(arena),
                                              counts, fetch, victims, Bx / 16, S, E_tot, status);
   return cudaGetLastError();

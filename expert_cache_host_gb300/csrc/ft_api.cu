@@ -198,10 +198,20 @@ int check_layer(ft_ctx* c, int layer) {
   return FT_OK;
 }
 
-int enqueue_control(ft_ctx* c, int layer, const int32_t* ids, int T, cudaStream_t st) {
+// logits == nullptr: control on the given routes; else route into the layer's
+// ids / weights first, in the same kernel.
+int enqueue_control(ft_ctx* c, int layer, const float* logits, const int32_t* ids, int T, cudaStream_t st) {
   LayerBufs& lb = c->layers[layer];
   ControlArgs a{};
   a.layer = layer;
+  if (logits) {
+    a.logits = logits;
+    a.T = T;
+    a.k = c->cfg.top_k;
+    a.ids_out = lb.ids;
+    a.w_out = lb.w;
+    ids = lb.ids;
+  }
   a.E = c->cfg.num_experts;
   a.n_routes = T * c->cfg.top_k;
   a.S = c->S;
@@ -438,11 +448,7 @@ int ft_cache_step(ft_ctx* c, int layer, const float* logits, int T, ft_step_out*
   if (T < 1 || T > c->cfg.t_max) return fail(FT_E_ARG, "T=%d outside [1, t_max=%d]", T, c->cfg.t_max);
   if (!logits) return fail(FT_E_ARG, "null logits");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  LayerBufs& lb = c->layers[layer];
-  cudaEvent_t pb = c->prof.begin(st);
-  CU(launch_route(logits, T, c->cfg.num_experts, c->cfg.top_k, lb.ids, lb.w, c->status, nullptr, st));
-  c->prof.end(st, FT_K_ROUTE, pb);
-  if ((rc = enqueue_control(c, layer, lb.ids, T, st))) return rc;
+  if ((rc = enqueue_control(c, layer, logits, nullptr, T, st))) return rc;
   fill_out(c, layer, out);
   return FT_OK;
 }
@@ -453,7 +459,7 @@ int ft_cache_control(ft_ctx* c, int layer, const int32_t* ids, int T, ft_step_ou
   if (T < 1 || T > c->cfg.t_max) return fail(FT_E_ARG, "T=%d outside [1, t_max=%d]", T, c->cfg.t_max);
   if (!ids) return fail(FT_E_ARG, "null ids");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if ((rc = enqueue_control(c, layer, ids, T, st))) return rc;
+  if ((rc = enqueue_control(c, layer, nullptr, ids, T, st))) return rc;
   fill_out(c, layer, out);
   if (out) out->ids = const_cast<int32_t*>(ids);  // the control kernel read the caller's routes in place
   return FT_OK;

@@ -49,6 +49,12 @@ struct LayerBufs {
 struct ControlArgs {
   int layer, E, n_routes, S, K_max;
   long long r_num, r_den;
+  // Fused routing: when logits ([T, E] fp32) is given, the kernel first routes
+  // the T tokens into ids_out / w_out ([T, k]) and then reads ids = ids_out.
+  const float* logits;
+  int T, k;
+  int32_t* ids_out;
+  float* w_out;
   const int32_t* ids;
   int32_t* slot_of;
   int32_t* expert_of;

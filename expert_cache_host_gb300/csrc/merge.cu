@@ -6,16 +6,17 @@
 // float32 buffer `partial` (NULL = 0), and the GPU side is the weighted sum of
 // the expert outputs of the routes that have a slot:
 //     out[t] = partial[t] + sum_j [slot_ids[t,j] >= 0] w[t,j] * sum_c ypart[t*k+j, c]
-// A block owns 32 float4 columns of one token; its 8 warps-rows split the k
-// routes, each summing the chunk partials of its routes, and the final sum
-// over routes runs in a fixed order, so the result is deterministic.
+// A block owns 8 float4 columns of one token; its 32 thread rows split the
+// k * n_chunks (route, chunk) partials of those columns (each row issues its
+// loads together, so the merge costs about one L2 round trip), and the rows
+// are then summed in a fixed order, so the result is deterministic.
 #include "ft_internal.h"
 
 namespace ft {
 namespace {
 
-constexpr int kCols = 32;  // float4 columns per block
-constexpr int kRows = 8;   // route lanes per block
+constexpr int kCols = 8;   // float4 columns per block
+constexpr int kRows = 32;  // (route, chunk) lanes per block
 
 __global__ void __launch_bounds__(kCols* kRows)
     merge_kernel(const float4* __restrict__ ypart, int n_chunks, const int32_t* __restrict__ slot_ids,
@@ -23,40 +24,41 @@ __global__ void __launch_bounds__(kCols* kRows)
                  int d4) {
   __shared__ float4 red[kRows][kCols];
   const int t = blockIdx.y;
-  const int col = threadIdx.x & (kCols - 1), jl = threadIdx.x / kCols;
+  const int col = threadIdx.x % kCols, row = threadIdx.x / kCols;
   const int i = blockIdx.x * kCols + col;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (i < d4) {
-    for (int j = jl; j < k; j += kRows) {
-      const int r = t * k + j;
-      if (slot_ids[r] < 0) continue;
-      const float wr = w[r];
-      const float4* y = ypart + (size_t)r * n_chunks * d4 + i;
-      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-      int c = 0;
-      for (; c + 4 <= n_chunks; c += 4) {
-        float4 v0 = y[(size_t)c * d4], v1 = y[(size_t)(c + 1) * d4], v2 = y[(size_t)(c + 2) * d4],
-               v3 = y[(size_t)(c + 3) * d4];
-        s.x += v0.x; s.y += v0.y; s.z += v0.z; s.w += v0.w;
-        s.x += v1.x; s.y += v1.y; s.z += v1.z; s.w += v1.w;
-        s.x += v2.x; s.y += v2.y; s.z += v2.z; s.w += v2.w;
-        s.x += v3.x; s.y += v3.y; s.z += v3.z; s.w += v3.w;
+    const int npairs = k * n_chunks;
+    for (int p0 = row; p0 < npairs; p0 += 4 * kRows) {
+      float4 v[4];
+      float wv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int p = p0 + u * kRows;
+        wv[u] = 0.f;
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p < npairs) {
+          const int j = p / n_chunks, c = p - j * n_chunks, r = t * k + j;
+          if (slot_ids[r] >= 0) {
+            wv[u] = w[r];
+            v[u] = ypart[((size_t)r * n_chunks + c) * d4 + i];
+          }
+        }
       }
-      for (; c < n_chunks; ++c) {
-        float4 v = y[(size_t)c * d4];
-        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc.x = fmaf(wv[u], v[u].x, acc.x);
+        acc.y = fmaf(wv[u], v[u].y, acc.y);
+        acc.z = fmaf(wv[u], v[u].z, acc.z);
+        acc.w = fmaf(wv[u], v[u].w, acc.w);
       }
-      acc.x = fmaf(wr, s.x, acc.x);
-      acc.y = fmaf(wr, s.y, acc.y);
-      acc.z = fmaf(wr, s.z, acc.z);
-      acc.w = fmaf(wr, s.w, acc.w);
     }
   }
-  red[jl][col] = acc;
+  red[row][col] = acc;
   __syncthreads();
-  if (jl == 0 && i < d4) {
+  if (row == 0 && i < d4) {
     float4 o = partial ? partial[(size_t)t * d4 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
+#pragma unroll 8
     for (int q = 0; q < kRows; ++q) {
       o.x += red[q][col].x;
       o.y += red[q][col].y;

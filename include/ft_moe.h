@@ -151,8 +151,9 @@ int ft_host_alloc(size_t bytes, void** out);
 int ft_host_free(void* p);
 
 /* Routing + cache control for one decode step of `layer`: logits_dev is
- * [T, E] float32 row-major, 1 <= T <= t_max.  Enqueues the routing kernel and
- * the control kernel on `stream`; no host synchronisation, so the call can be
+ * [T, E] float32 row-major, 1 <= T <= t_max.  Enqueues one kernel on `stream`
+ * that routes the T tokens and then runs the control step; no host
+ * synchronisation, so the call can be
  * captured in a CUDA graph (shapes are fixed by T).  The step clock advances
  * by one per call.  `out` (may be NULL) receives the context's buffers. */
 int ft_cache_step(ft_ctx* ctx, int layer, const float* logits_dev, int T, ft_step_out* out, void* stream);
@@ -220,7 +221,7 @@ int ft_route(const float* logits_dev, int T, int E, int k, int32_t* ids_dev, flo
              void* stream);
 
 /* Kernel classes of ft_profile_read. */
-#define FT_K_ROUTE 0   /* routing kernel */
+#define FT_K_ROUTE 0   /* routing kernel (ft_route, prefill); decode routing runs inside the control kernel */
 #define FT_K_CONTROL 1 /* cache-control kernel */
 #define FT_K_FILL 2    /* decode fill (kernel or copy-engine copies), transfer stream */
 #define FT_K_EXPERTS 3 /* decode expert kernel */
