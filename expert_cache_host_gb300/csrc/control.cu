@@ -29,8 +29,8 @@
 namespace ft {
 namespace {
 
-constexpr int NT = kControlThreads;
-constexpr int NW = NT / 32;
+constexpr int kMaxWarps = kControlThreads / 32;
+constexpr int kControlRoutesSmem = 1024;  // routes kept in shared memory by the fused routing
 
 struct Smem {
   int ecount[kMaxExperts];   // routes per local expert
@@ -43,13 +43,16 @@ struct Smem {
   int eqsel[kMaxKmax];
   unsigned long long cand[kMaxKmax];  // (last_use << 32 | slot) below the threshold
   unsigned hist[256];
-  int wsum[NW];
-  unsigned wmin[NW], wmax[NW];
+  int wsum[kMaxWarps];
+  unsigned wmin[kMaxWarps], wmax[kMaxWarps];
   int sc[16];  // scalars
+  int rids[kControlRoutesSmem];  // the step's routes when routed in this kernel
 };
 
 // Exclusive block scan (NT threads); total returned through *total.
+template <int NT>
 __device__ __forceinline__ int block_scan(int v, int* wsum, int* total) {
+  constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -77,8 +80,10 @@ __device__ __forceinline__ int block_scan(int v, int* wsum, int* total) {
 
 // RP > 0: route the step's tokens first (one warp per token, RP logits per
 // lane); RP = 0: the routes are given.
-template <int RP>
+// NT threads (a multiple of 32, >= E and >= 256).
+template <int RP, int NT>
 __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
+  constexpr int NW = NT / 32;
   extern __shared__ __align__(16) unsigned char dyn[];
   Smem& sm = *reinterpret_cast<Smem*>(dyn);
   unsigned* lu = reinterpret_cast<unsigned*>(dyn + sizeof(Smem));  // [S] last_use copy
@@ -86,11 +91,16 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   const int E = a.E, S = a.S;
   const int base_id = a.layer * E;
 
+  // this layer's residency of every expert, fetched while the routes are computed
+  const int slot_pre = tid < E ? a.slot_of[base_id + tid] : -1;
+  // routes: read from shared memory when this kernel routed them
+  const bool rids_smem = RP > 0 && a.n_routes <= kControlRoutesSmem;
+  const int32_t* rids = rids_smem ? sm.rids : a.ids;
   if constexpr (RP > 0) {
     // 0. routing; the __syncthreads below makes the routes visible to the block
     for (int t = tid >> 5; t < a.T; t += NW)
       route_token<RP>(a.logits + (size_t)t * E, E, a.k, a.ids_out + (size_t)t * a.k, a.w_out + (size_t)t * a.k,
-                      a.status, nullptr);
+                      a.status, nullptr, rids_smem ? sm.rids + (size_t)t * a.k : nullptr);
   }
 
   const unsigned now0 = *a.now;
@@ -109,7 +119,7 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   // 1. count routes
   bool bad = false;
   for (int r = tid; r < a.n_routes; r += NT) {
-    int e = a.ids[r];
+    int e = rids[r];
     if ((unsigned)e >= (unsigned)E)
       bad = true;
     else if (!wrap)
@@ -129,10 +139,10 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   const int e = tid;
   const bool present = e < E && sm.ecount[e] > 0;
   int slot = -1;
-  if (present) slot = a.slot_of[base_id + e];
+  if (present) slot = slot_pre;
   const bool hit = present && slot >= 0;
   int tot;
-  int ex = block_scan(present ? (hit ? 1 : 0x10000) : 0, sm.wsum, &tot);
+  int ex = block_scan<NT>(present ? (hit ? 1 : 0x10000) : 0, sm.wsum, &tot);
   const int hits = tot & 0xFFFF, m = tot >> 16, n = hits + m;
   const int hpos = ex & 0xFFFF, mpos = ex >> 16;
   if (present) a.uniq[hpos + mpos] = base_id + e;
@@ -164,7 +174,7 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
     }
   }
   int avail;
-  (void)block_scan(my_elig, sm.wsum, &avail);
+  (void)block_scan<NT>(my_elig, sm.wsum, &avail);
   long long qstar = (2LL * m * a.r_num + a.r_den) / (2LL * a.r_den);
   if (qstar > m) qstar = m;
   int q = (int)qstar;
@@ -258,7 +268,7 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
       my_eq += v == thr;
     }
     int tot2;
-    int ex2 = block_scan(my_lt | (my_eq << 16), sm.wsum, &tot2);
+    int ex2 = block_scan<NT>(my_lt | (my_eq << 16), sm.wsum, &tot2);
     int lt_pos = ex2 & 0xFFFF, eq_pos = ex2 >> 16;
     const int c_lt = tot2 & 0xFFFF;
     for (int s = s0; s < s1; ++s) {
@@ -306,14 +316,14 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
 
   // 6. rewrite
   for (int r = tid; r < a.n_routes; r += NT) {
-    int le = a.ids[r];
+    int le = rids[r];
     a.slot_ids[r] = ((unsigned)le < (unsigned)E) ? sm.emap[le] : -1;
   }
 
   // 7. groups of routes per resident expert, experts ascending
   const bool resident = present && sm.emap[e] >= 0;
   int tot3;
-  int ex3 = block_scan(resident ? (sm.ecount[e] | 0x10000) : 0, sm.wsum, &tot3);
+  int ex3 = block_scan<NT>(resident ? (sm.ecount[e] | 0x10000) : 0, sm.wsum, &tot3);
   const int n_groups = tot3 >> 16, n_grouped = tot3 & 0xFFFF;
   if (resident) {
     int gi = ex3 >> 16, off = ex3 & 0xFFFF;
@@ -325,7 +335,7 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   if (tid == 0) a.group_off[n_groups] = n_grouped;
   __syncthreads();
   for (int r = tid; r < a.n_routes; r += NT) {
-    int le = a.ids[r];
+    int le = rids[r];
     if ((unsigned)le < (unsigned)E && sm.emap[le] >= 0) {
       int pos = sm.gstart[le] + atomicAdd(&sm.cursor[le], 1);
       a.group_routes[pos] = r;
@@ -356,31 +366,33 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
 size_t control_smem_bytes(int S) { return sizeof(Smem) + sizeof(unsigned) * (size_t)S; }
 
 namespace {
-template <int RP>
+template <int RP, int NT>
 cudaError_t launch_rp(const ControlArgs& a, cudaStream_t st) {
   const size_t smem = control_smem_bytes(a.S);
   static thread_local int configured_for = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_for != dev) {
-    cudaError_t e = cudaFuncSetAttribute(control_kernel<RP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(control_kernel<RP, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)control_smem_bytes(kMaxSlots));
     if (e != cudaSuccess) return e;
     configured_for = dev;
   }
-  control_kernel<RP><<<1, NT, smem, st>>>(a);
+  control_kernel<RP, NT><<<1, NT, smem, st>>>(a);
   return cudaGetLastError();
 }
+
 }  // namespace
 
 cudaError_t launch_control(const ControlArgs& a, cudaStream_t st) {
-  if (!a.logits) return launch_rp<0>(a, st);
+  constexpr int NT = kControlThreads;
+  if (!a.logits) return launch_rp<0, NT>(a, st);
   if (a.ids != a.ids_out || a.T * a.k != a.n_routes) return cudaErrorInvalidValue;
   const int per = (a.E + 31) / 32;
-  if (per <= 1) return launch_rp<1>(a, st);
-  if (per <= 4) return launch_rp<4>(a, st);
-  if (per <= 8) return launch_rp<8>(a, st);
-  return launch_rp<kMaxExperts / 32>(a, st);
+  if (per <= 1) return launch_rp<1, NT>(a, st);
+  if (per <= 4) return launch_rp<4, NT>(a, st);
+  if (per <= 8) return launch_rp<8, NT>(a, st);
+  return launch_rp<kMaxExperts / 32, NT>(a, st);
 }
 
 }  // namespace ft

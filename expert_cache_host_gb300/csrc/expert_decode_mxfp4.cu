@@ -116,10 +116,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   int* rs = reinterpret_cast<int*>(dyn + Ly.rs);
 
   const int c = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
-  if (g >= a.counts[5]) return;
-  // select 1: only experts resident before the step; 2: only those it installed
-  if (a.select != 0 && (a.group_new[g] != 0) != (a.select == 2)) return;
+  // Fetch every per-group value at once (one memory round trip before the
+  // first TMA issue); the group arrays hold at least max_groups (+1) entries,
+  // so these loads are in bounds for every g of the grid.
+  const int n_groups = a.counts[5];
+  const int is_new = a.select != 0 ? a.group_new[g] : 0;
   const int slot = a.group_slot[g];
+  const int r0 = a.group_off[g], r1 = a.group_off[g + 1];
+  if (g >= n_groups) return;
+  // select 1: only experts resident before the step; 2: only those it installed
+  if (a.select != 0 && (is_new != 0) != (a.select == 2)) return;
   if ((unsigned)slot >= (unsigned)a.S) {
     if (tid == 0) atomicOr(a.status, FT_ST_BAD_SLOT);
     return;
@@ -128,7 +134,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   const unsigned char* ex = a.arena + (size_t)slot * a.Bx;
   const unsigned char* sc_gate = ex + 3 * (df / 2);                 // [f][d/32]
   const unsigned char* sc_down = sc_gate + 2 * (df / 32);           // [d][f/32]
-  const int r0 = a.group_off[g], r1 = a.group_off[g + 1];
   const int n_batches = (r1 - r0 + TB - 1) / TB;
   const int cb_n = d / 512;            // 256-byte column blocks per gate/up row
   const int P1 = 2 * cb_n;

@@ -22,12 +22,13 @@ __device__ __forceinline__ bool route_better(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
-// Route token row `row` (E logits); lanes j < k write ids[j], w[j]; if hist is
-// given, every chosen expert is counted in it.
+// Route token row `row` (E logits); lanes j < k write ids[j], w[j] (and
+// ids2[j] if given, e.g. a shared-memory copy); if hist is given, every chosen
+// expert is counted in it.
 template <int PER_LANE>
 __device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k, int32_t* __restrict__ ids,
                                             float* __restrict__ w, uint32_t* __restrict__ status,
-                                            int32_t* __restrict__ hist) {
+                                            int32_t* __restrict__ hist, int32_t* ids2 = nullptr) {
   const int lane = threadIdx.x & 31;
   float v[PER_LANE];
   bool nan_seen = false;
@@ -81,6 +82,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ row, int E
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lane < k) {
     ids[lane] = my_id;
+    if (ids2) ids2[lane] = my_id;
     w[lane] = ex / sum;
     if (hist) atomicAdd(&hist[my_id], 1);
   }

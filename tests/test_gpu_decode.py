@@ -153,6 +153,15 @@ def test_batch16_decode_groups(ft):
     ft.ft_moe_destroy(ctx)
 
 
+@pytest.mark.parametrize("d,f,T,k", [(512, 256, 1, 2), (1024, 128, 16, 4), (768, 128, 4, 2), (2048, 128, 16, 8)])
+def test_decode_shapes(ft, d, f, T, k):
+    """Hidden sizes of 2, 3, 4 and 8 column blocks, f of 4 to 8 chunks, and
+    T = 16, which puts several token batches through one CTA."""
+    model = make_model(2, 16, k, d, f, seed=7 + d)
+    ctx, _, _ = run_decode(ft, model, S=max(6, 2 * k), K_max=16, r=(1, 1), steps=5, T=T)
+    ft.ft_moe_destroy(ctx)
+
+
 def test_rebuild_mid_run(ft):
     """A rebuild at a safe point resets the cache cold at the new size; the
     results stay equal to a fresh oracle cache of that size."""
