@@ -4,17 +4,21 @@
 // The routes of a prefill chunk are sorted by expert (counting sort), so the
 // rows of each expert form one contiguous segment of the gathered activation
 // matrix; segments are cut into 128-row M tiles (the last one ragged), listed
-// on the device.  One CTA computes one (M tile, N tile):
+// on the device.  An output tile is one (M tile, N tile):
 //   mode 1 (gate/up): G = X W_gate^T and U = X W_up^T for the same 128 N
 //     columns into two tensor-memory accumulators, then H = silu(G) * U,
 //     rounded to bf16 (the operand of the next GEMM);
 //   mode 2 (down):    Y = H W_down^T, 256 N columns, fp32 out.
-// Warp roles: warp 0 lane 0 issues TMA loads into a 4-stage ring (A tile
-// 128 x 64 and the B tiles, 128-byte swizzled), warp 1 allocates tensor
-// memory and its lane 0 issues tcgen05.mma (M=128, K=16 steps), committing
-// each stage back to the producer and finally to the epilogue, warps 2-5 read
-// the accumulators with tcgen05.ld (one row per thread) and store the rows
-// that belong to the segment.  All waits are bounded (FT_ST_TIMEOUT).
+// Persistent: one CTA per SM walks the tiles (N tiles of an M tile adjacent,
+// so the activation tile is re-read from L2).  Warp roles: warp 0 lane 0
+// issues TMA loads into a 4-stage ring (A tile 128 x 64 and the B tiles,
+// 128-byte swizzled), running ahead across tile boundaries; warp 1 allocates
+// all 512 tensor-memory columns as two accumulator buffers and its lane 0
+// issues tcgen05.mma (M=128, K=16 steps), committing each stage back to the
+// producer and each finished tile to the epilogue; warps 2-5 drain a buffer
+// with tcgen05.ld (one row per thread), store the rows that belong to the
+// segment and hand the buffer back -- so the epilogue of one tile overlaps
+// the MMAs of the next.  All waits are bounded (FT_ST_TIMEOUT).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -24,7 +28,7 @@
 namespace ft {
 namespace {
 
-constexpr int BM = 128, BK = 64, NSTAGE = 4, kThreads = 192;
+constexpr int BM = 128, BK = 64, NSTAGE = 4, kThreads = 192, kEpiWarps = 4;
 
 template <int MODE>
 struct Cfg {
@@ -33,29 +37,25 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + NB * B_BYTES;
-  static constexpr uint32_t TMEM_COLS = 256;
+  static constexpr uint32_t ACC_COLS = 256;          // fp32 columns of one accumulator buffer
+  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // double buffer: all 512 columns
   static constexpr size_t SMEM = (size_t)NSTAGE * STAGE + 1024 /*align*/ + 256 /*barriers*/;
 };
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                        GemmArgs a) {
+                        GemmArgs a, int n_ntiles) {
   using C = Cfg<MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NSTAGE * C::STAGE);
   uint64_t* empty = full + NSTAGE;
-  uint64_t* accb = empty + NSTAGE;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  uint64_t* accf = empty + NSTAGE;  // [2] accumulator buffer holds a finished tile
+  uint64_t* acce = accf + 2;        // [2] accumulator buffer drained by the epilogue
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
 
-  // N tiles of one M tile are adjacent in launch order (the activation tile is
-  // re-read from L2, not DRAM), and the few M tiles of one expert follow each
-  // other (its weight tiles stay in L2 too).
-  const int nt = blockIdx.x, mt = blockIdx.y;
-  if (mt >= *a.n_mtiles) return;
-  const int e = a.tile_expert[mt], r0 = a.tile_row0[mt], r_end = a.seg_start[e + 1];
-  const int n0 = nt * C::BN;
+  const int n_tiles = *a.n_mtiles * n_ntiles;
   const int KB = a.K / BK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -64,7 +64,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accb, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], kEpiWarps);
+    }
     mbar_init_fence();
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -76,84 +79,108 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % NSTAGE;
-        if (kb >= NSTAGE && !mbar_wait(&empty[s], (uint32_t)(((kb / NSTAGE) - 1) & 1), late)) late = true;
-        uint8_t* sa = smem + s * C::STAGE;
-        uint8_t* sb = sa + C::A_BYTES;
-        mbar_expect_tx(&full[s], C::STAGE);
-        tensor_g2s_2d(sa, &map_a, kb * BK, r0, &full[s]);
-        if (MODE == 1) {
-          tensor_g2s_4d(sb, &map_b, kb * BK, n0, 0, e, &full[s]);
-          tensor_g2s_4d(sb + C::B_BYTES, &map_b, kb * BK, n0, 1, e, &full[s]);
-        } else {
-          tensor_g2s_3d(sb, &map_b, kb * BK, n0, e, &full[s]);
+      uint32_t it = 0;  // k blocks issued so far (ring position)
+      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const int mt = t / n_ntiles, n0 = (t - mt * n_ntiles) * C::BN;
+        const int e = a.tile_expert[mt], r0 = a.tile_row0[mt];
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % NSTAGE;
+          if (it >= NSTAGE && !mbar_wait(&empty[s], (uint32_t)(((it / NSTAGE) - 1) & 1), late)) late = true;
+          uint8_t* sa = smem + s * C::STAGE;
+          uint8_t* sb = sa + C::A_BYTES;
+          mbar_expect_tx(&full[s], C::STAGE);
+          tensor_g2s_2d(sa, &map_a, kb * BK, r0, &full[s]);
+          if (MODE == 1) {
+            tensor_g2s_4d(sb, &map_b, kb * BK, n0, 0, e, &full[s]);
+            tensor_g2s_4d(sb + C::B_BYTES, &map_b, kb * BK, n0, 1, e, &full[s]);
+          } else {
+            tensor_g2s_3d(sb, &map_b, kb * BK, n0, e, &full[s]);
+          }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(BM, C::BN);
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % NSTAGE;
-        if (!mbar_wait(&full[s], (uint32_t)((kb / NSTAGE) & 1), late)) late = true;
+      uint32_t it = 0;
+      int i = 0;  // tiles of this CTA so far
+      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
+        const int b = i & 1;
+        // the epilogue must have drained this buffer (tile i - 2)
+        if (i >= 2 && !mbar_wait(&acce[b], (uint32_t)(((i >> 1) - 1) & 1), late)) late = true;
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + s * C::STAGE), sb = sa + C::A_BYTES;
+        const uint32_t acc_tm = tmem + (uint32_t)b * C::ACC_COLS;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % NSTAGE;
+          if (!mbar_wait(&full[s], (uint32_t)((it / NSTAGE) & 1), late)) late = true;
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * C::STAGE), sb = sa + C::A_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = umma_desc_sw128(sa + kk * 32);
-          const uint32_t acc = (kb | kk) ? 1u : 0u;
-          umma_bf16(tmem, ad, umma_desc_sw128(sb + kk * 32), idesc, acc);
-          if (MODE == 1) umma_bf16(tmem + C::BN, ad, umma_desc_sw128(sb + C::B_BYTES + kk * 32), idesc, acc);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = umma_desc_sw128(sa + kk * 32);
+            const uint32_t acc = (kb | kk) ? 1u : 0u;
+            umma_bf16(acc_tm, ad, umma_desc_sw128(sb + kk * 32), idesc, acc);
+            if (MODE == 1) umma_bf16(acc_tm + C::BN, ad, umma_desc_sw128(sb + C::B_BYTES + kk * 32), idesc, acc);
+          }
+          umma_commit(&empty[s]);
         }
-        umma_commit(&empty[s]);
+        umma_commit(&accf[b]);
       }
-      umma_commit(accb);
     }
   } else {
     // epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 (one row each)
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const int grow = r0 + row;
-    const bool valid = grow < r_end;
-    if (!mbar_wait(accb, 0, late)) late = true;
-    tc_fence_after();
-    const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-    if (MODE == 1) {
-      __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)grow * a.out_ld + n0;
+    int i = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      const int mt = t / n_ntiles, n0 = (t - mt * n_ntiles) * C::BN;
+      const int e = a.tile_expert[mt], r0 = a.tile_row0[mt], r_end = a.seg_start[e + 1];
+      const int grow = r0 + row;
+      const bool valid = grow < r_end;
+      if (!mbar_wait(&accf[b], (uint32_t)((i >> 1) & 1), late)) late = true;
+      tc_fence_after();
+      const uint32_t lane_addr = tmem + (uint32_t)b * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
+      if (MODE == 1) {
+        __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)grow * a.out_ld + n0;
 #pragma unroll 1
-      for (int c0 = 0; c0 < C::BN; c0 += 32) {
-        float gv[32], uv[32];
-        tmem_ld32(lane_addr + c0, gv);
-        tmem_ld32(lane_addr + C::BN + c0, uv);
-        if (valid) {
-          uint4 packed[4];
-          uint32_t* pw = reinterpret_cast<uint32_t*>(packed);
+        for (int c0 = 0; c0 < C::BN; c0 += 32) {
+          float gv[32], uv[32];
+          tmem_ld32(lane_addr + c0, gv);
+          tmem_ld32(lane_addr + C::BN + c0, uv);
+          if (valid) {
+            uint4 packed[4];
+            uint32_t* pw = reinterpret_cast<uint32_t*>(packed);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float g0 = gv[2 * i], g1 = gv[2 * i + 1];
-            const float h0 = g0 / (1.f + expf(-g0)) * uv[2 * i];
-            const float h1 = g1 / (1.f + expf(-g1)) * uv[2 * i + 1];
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
-            pw[i] = *reinterpret_cast<uint32_t*>(&b2);
+            for (int j = 0; j < 16; ++j) {
+              const float g0 = gv[2 * j], g1 = gv[2 * j + 1];
+              const float h0 = g0 / (1.f + expf(-g0)) * uv[2 * j];
+              const float h1 = g1 / (1.f + expf(-g1)) * uv[2 * j + 1];
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
+              pw[j] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(H + c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = packed[j];
           }
-          uint4* dst = reinterpret_cast<uint4*>(H + c0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = packed[i];
         }
-      }
-    } else {
-      float* Y = reinterpret_cast<float*>(a.out) + (size_t)grow * a.out_ld + n0;
+      } else {
+        float* Y = reinterpret_cast<float*>(a.out) + (size_t)grow * a.out_ld + n0;
 #pragma unroll 1
-      for (int c0 = 0; c0 < C::BN; c0 += 32) {
-        float yv[32];
-        tmem_ld32(lane_addr + c0, yv);
-        if (valid) {
-          float4* dst = reinterpret_cast<float4*>(Y + c0);
+        for (int c0 = 0; c0 < C::BN; c0 += 32) {
+          float yv[32];
+          tmem_ld32(lane_addr + c0, yv);
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(Y + c0);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) dst[i] = make_float4(yv[4 * i], yv[4 * i + 1], yv[4 * i + 2], yv[4 * i + 3]);
+            for (int j = 0; j < 8; ++j) dst[j] = make_float4(yv[4 * j], yv[4 * j + 1], yv[4 * j + 2], yv[4 * j + 3]);
+          }
         }
       }
+      // this warp's reads of the buffer are done: hand it back to the MMA issuer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(&acce[b]);
     }
   }
   tc_fence_before();
@@ -177,8 +204,11 @@ cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const Gem
     if (e != cudaSuccess) return e;
     configured = dev;
   }
-  dim3 grid(N / C::BN, max_mtiles);
-  grouped_gemm_kernel<MODE><<<grid, kThreads, C::SMEM, st>>>(*map_a, *map_b, a);
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int n_ntiles = N / C::BN;
+  const int grid = max_mtiles * n_ntiles < sms ? max_mtiles * n_ntiles : sms;  // persistent: one CTA per SM
+  grouped_gemm_kernel<MODE><<<grid, kThreads, C::SMEM, st>>>(*map_a, *map_b, a, n_ntiles);
   return cudaGetLastError();
 }
 

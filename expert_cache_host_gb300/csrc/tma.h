@@ -39,6 +39,11 @@ __device__ __forceinline__ void mbar_init_fence() {
 // it a slow load can still be pending when the refill lands.
 __device__ __forceinline__ void proxy_fence_reads() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Plain arrival (count 1) on a barrier of this CTA.
+__device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(smem_u32(bar)),
                "r"(bytes)
