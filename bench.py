@@ -448,6 +448,45 @@ def run_reference(args, w):
     }
 
 
+# ----------------------------------------------------------------------------- sweeps (report mode)
+
+def run_sweep(args, w, world, local):
+    """One JSON line per point.  capacity: the decode step at S = 5, 10, 25 and
+    50 % of the pool's experts (the synthetic counterpart of the article's
+    miss rate versus cache capacity, Figure 4b); prompt: the prefill chunk at
+    4096, 8192 and 16384 tokens with and without the double buffer (Figure 4a)."""
+    hp, pool, _ = make_host_pool(args, w)
+    try:
+        if args.sweep == "capacity":
+            e_tot = w["L"] * w["E"]
+            hid, lg = decode_inputs(w, args.warmup + args.steps + min(args.steps, args.profile_steps)
+                                    + min(args.steps, args.e2e_steps))
+            for pct in (5, 10, 25, 50):
+                ws = dict(w, S=max(w["k"] * w["T"], e_tot * pct // 100))
+                dec = run_decode_leg(args, ws, world, local, pool, hid, lg)
+                routes = dec["hits"] + dec["misses"]
+                print(json.dumps({
+                    "sweep": "capacity", "workload": w["desc"].split(":")[0], "slots": ws["S"],
+                    "capacity_pct": pct, "tok_s": round(dec["value"], 3),
+                    "expert_miss_rate": round(dec["misses"] / max(1.0, routes), 4),
+                    "fills_per_token": round(dec["fills"] / dec["K"], 3),
+                    "timed_tokens": dec["K"], "warmup_tokens": dec["W"], "device_status": dec["status"]}), flush=True)
+        else:
+            w = dict(w, dtype=0)
+            for tokens in (4096, 8192, 16384):
+                args.prefill_tokens = tokens
+                pre = run_prefill_leg(args, w, pool)
+                print(json.dumps({
+                    "sweep": "prompt", "tokens": tokens, "chunk_s": round(pre["chunk_s"], 4),
+                    "chunk_s_single_buffer": round(pre["chunk_s_single_buffer"], 4),
+                    "tok_s": round(tokens / pre["chunk_s"], 1), "link_gbs": round(pre["link_gbs"], 1),
+                    "gemm_tflops": round(pre["gemm_tflops"], 1), "device_status": pre["status"]}), flush=True)
+    finally:
+        if hp:
+            del pool
+            hp.free()
+
+
 # ----------------------------------------------------------------------------- main
 
 def make_host_pool(args, w):
@@ -547,6 +586,10 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="decode tokens per step (default 1)")
     ap.add_argument("--layers", type=int, default=0, help="override L (small profiling cases, not a bench line)")
     ap.add_argument("--slots", type=int, default=0, help="override S (small profiling cases, not a bench line)")
+    ap.add_argument("--sweep", choices=("capacity", "prompt"), default=None,
+                    help="report mode (not the bench line): decode miss rate and tok/s over cache capacities of "
+                         "5/10/25/50%% of the pool, or prefill chunk time over prompt lengths 4k/8k/16k with and "
+                         "without the double buffer")
     ap.add_argument("--pool", choices=("pinned", "registered"), default="pinned",
                     help="pinned: pool written into ft_host_alloc memory; registered: pageable pool pinned by "
                          "ft_moe_init after the write")
@@ -604,6 +647,9 @@ def main():
         if hp:
             del pool
             hp.free()
+        return
+    if args.sweep:
+        run_sweep(args, w, world, local)
         return
     hp, pool, t_pool = make_host_pool(args, w)
     hid, lg = decode_inputs(w, args.warmup + args.steps + min(args.steps, args.profile_steps)
