@@ -28,7 +28,7 @@ COUNTS = ("n", "hits", "m", "q", "cpu", "n_groups", "now")
 EXPORTS = (
     "ft_moe_init", "ft_moe_destroy", "ft_cache_step", "ft_cache_control", "ft_moe_forward", "ft_cache_rebuild",
     "ft_get_status", "ft_get_counters", "ft_get_table", "ft_slot_ptr", "ft_get_epoch", "ft_num_slots", "ft_route",
-    "ft_profile_enable", "ft_profile_read", "ft_decode_experts_noalloc", "ft_host_alloc", "ft_host_free",
+    "ft_profile_enable", "ft_profile_read", "ft_decode_experts_noalloc", "ft_host_alloc", "ft_host_free", "ft_set_ratio",
     "ft_last_error",
 )
 FT_K_ROUTE, FT_K_CONTROL, FT_K_FILL, FT_K_EXPERTS, FT_K_MERGE, FT_K_UPLOAD, FT_K_PREFILL, FT_K_GEMM = range(8)
@@ -90,6 +90,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "ft_profile_read": ([vp, vp, vp, i32], i32),
             "ft_decode_experts_noalloc": ([vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp], i32),
             "ft_host_alloc": ([sz, ctypes.POINTER(vp)], i32),
+            "ft_set_ratio": ([vp, i32, i32, vp], i32),
             "ft_host_free": ([vp], i32),
             "ft_last_error": ([], ctypes.c_char_p),
         }
@@ -179,6 +180,10 @@ def ft_get_table(ctx: int, E_tot: int, S: int):
 
 def ft_slot_ptr(ctx: int, slot: int) -> int:
     return load().ft_slot_ptr(ctypes.c_void_p(ctx), slot) or 0
+
+
+def ft_set_ratio(ctx: int, r_num: int, r_den: int, stream: int = 0) -> None:
+    _chk(load().ft_set_ratio(ctypes.c_void_p(ctx), r_num, r_den, ctypes.c_void_p(stream)))
 
 
 def ft_get_epoch(ctx: int) -> int:

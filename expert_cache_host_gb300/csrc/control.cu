@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
 
   // this layer's residency of every expert, fetched while the routes are computed
   const int slot_pre = tid < E ? a.slot_of[base_id + tid] : -1;
+  const long long r_num = a.ratio[0], r_den = a.ratio[1];
   // routes: read from shared memory when this kernel routed them
   const bool rids_smem = RP > 0 && a.n_routes <= kControlRoutesSmem;
   const int32_t* rids = rids_smem ? sm.rids : a.ids;
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   }
   int avail;
   (void)block_scan<NT>(my_elig, sm.wsum, &avail);
-  long long qstar = (2LL * m * a.r_num + a.r_den) / (2LL * a.r_den);
+  long long qstar = (2LL * m * r_num + r_den) / (2LL * r_den);
   if (qstar > m) qstar = m;
   int q = (int)qstar;
   if (q > a.K_max) q = a.K_max;
@@ -382,7 +383,16 @@ cudaError_t launch_rp(const ControlArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+__global__ void set_ratio_kernel(long long* ratio, long long r_num, long long r_den) {
+  ratio[0] = r_num;
+  ratio[1] = r_den;
+}
 }  // namespace
+
+cudaError_t launch_set_ratio(long long* ratio, long long r_num, long long r_den, cudaStream_t st) {
+  set_ratio_kernel<<<1, 1, 0, st>>>(ratio, r_num, r_den);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_control(const ControlArgs& a, cudaStream_t st) {
   constexpr int NT = kControlThreads;

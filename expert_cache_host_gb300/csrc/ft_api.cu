@@ -68,6 +68,7 @@ struct ft_ctx {
   int32_t* expert_of = nullptr;
   uint32_t* last_use = nullptr;
   uint32_t* now = nullptr;
+  long long* ratio = nullptr;  // [2] r_num, r_den
   uint32_t* status = nullptr;
   unsigned long long* counters = nullptr;
 
@@ -178,6 +179,7 @@ void free_all(ft_ctx* c) {
   cudaFree(c->expert_of);
   cudaFree(c->last_use);
   cudaFree(c->now);
+  cudaFree(c->ratio);
   cudaFree(c->status);
   cudaFree(c->counters);
   cudaFree(c->layer_mem);
@@ -216,8 +218,7 @@ int enqueue_control(ft_ctx* c, int layer, const float* logits, const int32_t* id
   a.n_routes = T * c->cfg.top_k;
   a.S = c->S;
   a.K_max = c->cfg.k_max;
-  a.r_num = c->cfg.r_num;
-  a.r_den = c->cfg.r_den;
+  a.ratio = c->ratio;
   a.ids = ids;
   a.slot_of = c->slot_of;
   a.expert_of = c->expert_of;
@@ -344,9 +345,17 @@ int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx
 
   if (cudaMalloc(&c->slot_of, sizeof(int32_t) * c->E_tot) != cudaSuccess ||
       cudaMalloc(&c->now, sizeof(uint32_t)) != cudaSuccess || cudaMalloc(&c->status, sizeof(uint32_t)) != cudaSuccess ||
+      cudaMalloc(&c->ratio, 2 * sizeof(long long)) != cudaSuccess ||
       cudaMalloc(&c->counters, sizeof(unsigned long long) * kCountersPerLayer * cfg->num_layers) != cudaSuccess) {
     cudaGetLastError();
     return bail(fail(FT_E_NOMEM, "table allocation failed"));
+  }
+  {
+    const long long r[2] = {cfg->r_num, cfg->r_den};
+    if (cudaMemcpy(c->ratio, r, sizeof(r), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      return bail(fail(FT_E_CUDA, "ratio upload failed"));
+    }
   }
   if ((rc = alloc_arena(c, cfg->num_slots))) return bail(rc);
 
@@ -421,6 +430,13 @@ int ft_moe_destroy(ft_ctx* c) {
   cudaDeviceSynchronize();
   free_all(c);
   delete c;
+  return FT_OK;
+}
+
+int ft_set_ratio(ft_ctx* c, int32_t r_num, int32_t r_den, void* stream) {
+  if (!c) return fail(FT_E_ARG, "null context");
+  if (r_num < 0 || r_den < 1) return fail(FT_E_ARG, "r = r_num/r_den needs r_num >= 0, r_den >= 1");
+  CU(launch_set_ratio(c->ratio, r_num, r_den, static_cast<cudaStream_t>(stream)));
   return FT_OK;
 }
 

@@ -48,7 +48,7 @@ struct LayerBufs {
 
 struct ControlArgs {
   int layer, E, n_routes, S, K_max;
-  long long r_num, r_den;
+  const long long* ratio;  // device [2]: r_num, r_den of r = BP/BH (set at init or by ft_set_ratio)
   // Fused routing: when logits ([T, E] fp32) is given, the kernel first routes
   // the T tokens into ids_out / w_out ([T, k]) and then reads ids = ids_out.
   const float* logits;
@@ -114,6 +114,9 @@ cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_experts_mxfp4(const DecodeArgs& a, int tokens, cudaStream_t st);
 
 // out[t] = partial[t] + sum_j [slot_ids >= 0] w[t,j] * sum_c ypart[t*k+j][c]
+// ratio[0] = r_num, ratio[1] = r_den, stream-ordered (capturable).
+cudaError_t launch_set_ratio(long long* ratio, long long r_num, long long r_den, cudaStream_t st);
+
 cudaError_t launch_merge(const float* ypart, int n_chunks, const int32_t* slot_ids, const float* w,
                          const float* partial, float* out, int T, int k, int d, cudaStream_t st);
 

@@ -208,6 +208,18 @@ int ft_get_table(ft_ctx* ctx, int32_t* slot_of, int32_t* expert_of, uint32_t* la
 /* Device pointer of slot s's bytes in the arena (for tests), or NULL. */
 void* ft_slot_ptr(ft_ctx* ctx, int slot);
 
+/* Change r = BP/BH (FreeToken article, section "设计：三大机制" 1, Decode
+ * bullet: the fill-vs-CPU split of the misses follows the measured link and
+ * host bandwidths, which vary at run time) for the steps enqueued on `stream`
+ * after this call.  r lives in device memory and the control kernel reads it
+ * at every step, so CUDA graphs captured earlier pick up the new value
+ * without re-capture; the call itself enqueues one tiny kernel and can be
+ * captured too (the captured values are then fixed).  The caller measures
+ * the two bandwidths (its CPU expert executor's, and the fill rate reported
+ * by ft_profile_read or its own timing) and chooses r.
+ * Errors: FT_E_ARG (r_num < 0 or r_den < 1), FT_E_CUDA. */
+int ft_set_ratio(ft_ctx* ctx, int32_t r_num, int32_t r_den, void* stream);
+
 /* Cache epoch: starts at 0, +1 per ft_cache_rebuild. */
 int ft_get_epoch(ft_ctx* ctx);
 

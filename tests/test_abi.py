@@ -67,3 +67,7 @@ def test_host_alloc_arguments_checked_on_host(lib):
     assert lib.ft_host_alloc(0, ctypes.byref(p)) == ft.FT_E_ARG
     assert lib.ft_host_alloc(4096, None) == ft.FT_E_ARG
     assert lib.ft_host_free(None) == ft.FT_OK
+
+
+def test_set_ratio_arguments_checked_on_host(lib):
+    assert lib.ft_set_ratio(None, 1, 1, None) == ft.FT_E_ARG

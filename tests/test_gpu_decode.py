@@ -64,10 +64,11 @@ def test_route_nan_sets_status(ft):
 # ------------------------------------------------------------------ decode steps
 
 def run_decode(ft, model, S, K_max, r, steps, T=1, fill_mode=0, check_every=1, out_tokens=None, rho=0.9,
-               rebuild_at=None, graph=False):
+               rebuild_at=None, graph=False, r_at=None):
     """Decode `steps` steps over all layers through the library and the oracle
     side by side; compare control state every step and outputs every
-    `check_every` steps."""
+    `check_every` steps.  r_at: {step: (r_num, r_den)} changes r (ft_set_ratio)
+    before that step."""
     L, E, k, d, f = model.L, model.E, model.k, model.d, model.f
     cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, dtype=model.dtype, num_slots=S,
                          k_max=K_max, t_max=T, r_num=r[0], r_den=r[1], fill_mode=fill_mode)
@@ -84,6 +85,9 @@ def run_decode(ft, model, S, K_max, r, steps, T=1, fill_mode=0, check_every=1, o
         stream = torch.cuda.current_stream().cuda_stream
         worst = (0.0, 0.0)
         for s in range(steps):
+            if r_at and s in r_at:
+                r = r_at[s]
+                ft.ft_set_ratio(ctx, r[0], r[1], stream)
             if rebuild_at is not None and s == rebuild_at[0]:
                 ft.ft_cache_rebuild(ctx, rebuild_at[1])
                 cache = oracle.Cache(L * E, rebuild_at[1])
@@ -137,6 +141,16 @@ def test_tiny_decode_cpu_split(ft, r, K_max):
     ctx, cache, worst = run_decode(ft, model, S=6, K_max=K_max, r=r, steps=20)
     cnt = ft.ft_get_counters(ctx, 2)
     assert cnt[:, 3].sum() > 0  # some routes did go to the CPU
+    ft.ft_moe_destroy(ctx)
+
+
+def test_ratio_changes_at_run_time(ft):
+    """ft_set_ratio between steps: the fill/CPU split follows the new r from
+    the next step on (all-fill, half, none, 2x), against the oracle run with
+    the same r per step."""
+    model = make_model(2, 16, 2, 256, 128, seed=8)
+    ctx, _, _ = run_decode(ft, model, S=6, K_max=16, r=(1, 1), steps=10,
+                           r_at={2: (1, 2), 4: (0, 1), 6: (2, 1), 8: (3, 4)})
     ft.ft_moe_destroy(ctx)
 
 
@@ -292,3 +306,69 @@ def test_decode_from_host_alloc_pool(ft):
         assert np.array_equal(hp.array[:64], ftsynth.make_pool(41, L, E, d, f, 0)[:64])  # still mapped and intact
     finally:
         hp.free()  # nothing above holds the context any more
+
+
+# ------------------------------------------------------------------ CUDA graph replay
+
+def test_graph_replay_matches_oracle(ft):
+    """One decode step of every layer captured once as a CUDA graph and
+    replayed with new inputs: control state and outputs equal the oracle's at
+    every replay; an ft_set_ratio between replays is seen by the graph."""
+    L, E, k, d, f, T, S, K_max = 2, 16, 2, 256, 128, 1, 6, 16
+    model = make_model(L, E, k, d, f, seed=9)
+    steps, r = 8, (1, 1)
+    cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, num_slots=S, k_max=K_max, t_max=T,
+                         r_num=r[0], r_den=r[1])
+    ctx = ft.ft_moe_init(cfg, model.pool.ctypes.data, model.pool.nbytes)
+    try:
+        cache = oracle.Cache(L * E, S)
+        hid = np.stack([ftsynth.ar1_hidden(model.seed, l, 0, steps, d)[:, None, :] for l in range(L)], axis=1)
+        logits = np.stack([ftsynth.router_logits(hid[:, l], model.wr[l]) for l in range(L)], axis=1)
+        cur_hid = torch.empty((L, T, d), dtype=torch.int16, device="cuda")
+        cur_lg = torch.empty((L, T, E), dtype=torch.float32, device="cuda")
+        partial = torch.zeros((L, T, d), dtype=torch.float32, device="cuda")
+        out = torch.empty((L, T, d), dtype=torch.float32, device="cuda")
+        stream = torch.cuda.Stream()
+        res = [None] * L
+
+        def step(st):
+            for l in range(L):
+                res[l] = ft.ft_cache_step(ctx, l, cur_lg[l].data_ptr(), T, st)
+                ft.ft_moe_forward(ctx, l, ft.FT_DECODE_CACHED, 0, cur_hid[l].data_ptr(), T, partial[l].data_ptr(),
+                                  out[l].data_ptr(), st)
+
+        graph = None
+        with torch.cuda.stream(stream):
+            for s in range(steps):
+                if s == 5:
+                    r = (1, 2)
+                    ft.ft_set_ratio(ctx, r[0], r[1], stream.cuda_stream)
+                refs, fulls = [], []
+                for l in range(L):  # oracle first: its CPU part is an input of the step
+                    ids, w = oracle.route(logits[s, l], k)
+                    ref = cache.step(l, E, ids, r[0], r[1], K_max)
+                    full, _, cpu_part = oracle.moe_forward(model.layer_pool(l), model.bx, 0, d, f, ids, w, hid[s, l],
+                                                           slot_ids=ref.slot_ids.reshape(T, k))
+                    partial[l].copy_(torch.from_numpy(cpu_part.astype(np.float32)))
+                    refs.append((ids, ref))
+                    fulls.append(full)
+                cur_hid.copy_(torch.from_numpy(hid[s].view(np.int16)))
+                cur_lg.copy_(torch.from_numpy(logits[s]))
+                if s == 0:
+                    step(stream.cuda_stream)  # eager: kernel attributes are set outside the capture
+                else:
+                    if graph is None:
+                        graph = torch.cuda.CUDAGraph()
+                        with torch.cuda.graph(graph, stream=stream):
+                            step(torch.cuda.current_stream().cuda_stream)
+                    graph.replay()
+                stream.synchronize()
+                for l in range(L):
+                    g = step_to_host(res[l], T, k, E, K_max)
+                    assert np.array_equal(g["ids"], refs[l][0]), f"step {s} layer {l}"
+                    compare_step(g, refs[l][1], f"step {s} layer {l}")
+                    check_output(out[l].cpu().numpy().astype(np.float64), fulls[l], f"step {s} layer {l}")
+                compare_table(ft, ctx, cache, f"after step {s}")
+        assert ft.ft_get_status(ctx) == 0
+    finally:
+        ft.ft_moe_destroy(ctx)
