@@ -52,6 +52,15 @@ __device__ __forceinline__ void e2m1x8(unsigned w, unsigned& p0, unsigned& p1, u
 
 __device__ __forceinline__ __half2 h2(unsigned v) { return *reinterpret_cast<__half2*>(&v); }
 
+// Shared-memory position of activation word i (an f16 pair) of a token row:
+// the four 16-byte chunks of each 16-word piece are rotated by (piece / 2),
+// so the 16 pieces of a column block read chunk c from all 32 banks (two
+// wavefronts) instead of two bank groups.
+__device__ __forceinline__ int xs_swz(int i) {
+  const int piece = i >> 4, c = (i >> 2) & 3;
+  return (piece << 4) | (((c + (piece >> 1)) & 3) << 2) | (i & 3);
+}
+
 // Sum over one 32-element group: 16 code bytes (w) against 16 f16x2 activation
 // pairs (x[0..3] as four uint4), returned in fp32 (unscaled).
 __device__ __forceinline__ float group_dot(const uint4 w, const uint4* x) {
@@ -189,7 +198,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   const int lane = tid & 31;
-  const int rl = tid >> 3, cq = tid & 7;      // gate/up: row, 16-byte column within a 128-byte half block
+  // gate/up: thread = 16-byte column piece p of rows 2rp and 2rp + 1, so the
+  // piece's 32 activations are loaded once per tile for two rows
+  const int p = tid & 15, rp = tid >> 4;
   const int rowq = tid >> 1, q = tid & 1;     // down: row within a 256-row box, scale group of the chunk
   const int n_chunks = f / FC;
   bool late = false;
@@ -216,50 +227,60 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int i = tid; i < d / 2; i += kConsumers) {
         const unsigned v = src[i];
         const __half2 hv = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-        xs[(size_t)t * (d / 2) + i] = *reinterpret_cast<const unsigned*>(&hv);
+        xs[(size_t)t * (d / 2) + xs_swz(i)] = *reinterpret_cast<const unsigned*>(&hv);
       }
     }
     consumer_sync();
     if (b == 0 && !mbar_wait(scbar, 0, late)) late = true;
 
-    float acc[2][TB];
+    float acc[2][2][TB];  // [gate/up][row 2rp + i][token]
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
-      for (int t = 0; t < TB; ++t) acc[m][t] = 0.f;
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int t = 0; t < TB; ++t) acc[m][i][t] = 0.f;
 
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
 #pragma unroll 1
       for (int cb = 0; cb < cb_n; ++cb) {
         if (!mbar_wait(&full[s], ph, late)) late = true;
-        const unsigned char* buf = ring + s * kTile + rl * 256 + cq * 16;
+        const unsigned char* buf = ring + s * kTile + (2 * rp) * 256 + p * 16;
         const uint4 w0 = *reinterpret_cast<const uint4*>(buf);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(buf + 128);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(buf + 256);
         release();
-        const int g0 = cb * 16 + cq;  // scale group of piece 0; piece 1 is g0 + 8
-        const float s0 = e8m0(sc[(m * FC + rl) * sc_row + g0]);
-        const float s1 = e8m0(sc[(m * FC + rl) * sc_row + g0 + 8]);
+        const int grp = cb * 16 + p;  // scale group (and global 16-word piece) of this thread
+        const float s0 = e8m0(sc[(m * FC + 2 * rp) * sc_row + grp]);
+        const float s1 = e8m0(sc[(m * FC + 2 * rp + 1) * sc_row + grp]);
 #pragma unroll
         for (int t = 0; t < TB; ++t) {
           if (t < nt) {
-            const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)t * (d / 2) + cb * 256 + cq * 16);
-            acc[m][t] = fmaf(group_dot(w0, xp), s0, acc[m][t]);
-            acc[m][t] = fmaf(group_dot(w1, xp + 32), s1, acc[m][t]);
+            const unsigned* xrow = xs + (size_t)t * (d / 2) + grp * 16;
+            uint4 xv[4];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+              xv[c4] = *reinterpret_cast<const uint4*>(xrow + (((c4 + (grp >> 1)) & 3) << 2));
+            acc[m][0][t] = fmaf(group_dot(w0, xv), s0, acc[m][0][t]);
+            acc[m][1][t] = fmaf(group_dot(w1, xv), s1, acc[m][1][t]);
           }
         }
       }
     }
+    // row sums: the 16 pieces of a row pair are 16 consecutive lanes
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
-      for (int t = 0; t < TB; ++t) {
-        float v = acc[m][t];
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        if (cq == 0 && t < nt) gu[(m * FC + rl) * TB + t] = v;
-      }
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+          float v = acc[m][i][t];
+          v += __shfl_xor_sync(0xffffffffu, v, 8);
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          if (p == 0 && t < nt) gu[(m * FC + 2 * rp + i) * TB + t] = v;
+        }
     consumer_sync();
     if (tid < (FC / 2) * TB) {
       const int pr = tid % (FC / 2), t = tid / (FC / 2);
