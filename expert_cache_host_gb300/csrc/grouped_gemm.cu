@@ -39,17 +39,25 @@ struct Cfg {
   static constexpr int STAGE = A_BYTES + NB * B_BYTES;
   static constexpr uint32_t ACC_COLS = 256;          // fp32 columns of one accumulator buffer
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // double buffer: all 512 columns
-  static constexpr size_t SMEM = (size_t)NSTAGE * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+  // epilogue staging (mode 2): per epilogue warp, two 32-row x 128-byte boxes (4 KB each)
+  static constexpr int OUT_COLS = MODE == 1 ? 64 : 32;  // output columns per 128-byte row piece (bf16 / fp32)
+  static constexpr int STG_BYTES = MODE == 2 ? kEpiWarps * 2 * 4096 : 0;
+  static constexpr size_t SMEM = (size_t)NSTAGE * STAGE + STG_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
+
+// Position of 16-byte chunk j of row r (0..31) inside a 32 x 128-byte staging
+// box in the 128-byte swizzle layout the store tensor map expects.
+__device__ __forceinline__ int stg_off(int r, int j) { return r * 128 + ((j ^ (r & 7)) << 4); }
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                        GemmArgs a, int n_ntiles) {
+                        const __grid_constant__ CUtensorMap map_out, GemmArgs a, int n_ntiles) {
   using C = Cfg<MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NSTAGE * C::STAGE);
+  uint8_t* stg = smem + NSTAGE * C::STAGE;  // epilogue staging (1024-byte aligned)
+  uint64_t* full = reinterpret_cast<uint64_t*>(stg + C::STG_BYTES);
   uint64_t* empty = full + NSTAGE;
   uint64_t* accf = empty + NSTAGE;  // [2] accumulator buffer holds a finished tile
   uint64_t* acce = accf + 2;        // [2] accumulator buffer drained by the epilogue
@@ -128,9 +136,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 (one row each)
+    // epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 (one row each).
+    // Mode 2: a warp whose 32 rows all belong to the segment stages them in
+    // shared memory (128-byte swizzle) and writes each 32-row x 128-byte box
+    // with one TMA store (32 scattered 16-byte row pieces per store
+    // instruction were bound by L2 write requests); otherwise valid rows are
+    // stored directly.
     const int q = warp & 3;
     const int row = q * 32 + lane;
+    uint8_t* my_stg = stg + q * 2 * 4096;
+    int nbuf = 0;  // staging buffer to fill next (0/1)
     int i = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
       const int b = i & 1;
@@ -138,43 +153,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = a.tile_expert[mt], r0 = a.tile_row0[mt], r_end = a.seg_start[e + 1];
       const int grow = r0 + row;
       const bool valid = grow < r_end;
+      // every row of this warp is valid (warp-uniform); the bf16 H rows of
+      // mode 1 are small and go out directly, the fp32 Y rows through TMA
+      const bool whole = MODE == 2 && r0 + q * 32 + 31 < r_end;
       if (!mbar_wait(&accf[b], (uint32_t)((i >> 1) & 1), late)) late = true;
       tc_fence_after();
       const uint32_t lane_addr = tmem + (uint32_t)b * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
-      if (MODE == 1) {
-        __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)grow * a.out_ld + n0;
 #pragma unroll 1
-        for (int c0 = 0; c0 < C::BN; c0 += 32) {
-          float gv[32], uv[32];
-          tmem_ld32(lane_addr + c0, gv);
-          tmem_ld32(lane_addr + C::BN + c0, uv);
-          if (valid) {
-            uint4 packed[4];
-            uint32_t* pw = reinterpret_cast<uint32_t*>(packed);
+      for (int c0 = 0; c0 < C::BN; c0 += C::OUT_COLS) {
+        uint4 packed[8];  // 128 bytes of this row's output columns c0 .. c0 + OUT_COLS
+        if (MODE == 1) {
+          uint32_t* pw = reinterpret_cast<uint32_t*>(packed);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float gv[32], uv[32];
+            tmem_ld32(lane_addr + c0 + 32 * half, gv);
+            tmem_ld32(lane_addr + C::BN + c0 + 32 * half, uv);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float g0 = gv[2 * j], g1 = gv[2 * j + 1];
               const float h0 = g0 / (1.f + expf(-g0)) * uv[2 * j];
               const float h1 = g1 / (1.f + expf(-g1)) * uv[2 * j + 1];
               __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
-              pw[j] = *reinterpret_cast<uint32_t*>(&b2);
+              pw[16 * half + j] = *reinterpret_cast<uint32_t*>(&b2);
             }
-            uint4* dst = reinterpret_cast<uint4*>(H + c0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = packed[j];
           }
-        }
-      } else {
-        float* Y = reinterpret_cast<float*>(a.out) + (size_t)grow * a.out_ld + n0;
-#pragma unroll 1
-        for (int c0 = 0; c0 < C::BN; c0 += 32) {
+        } else {
           float yv[32];
           tmem_ld32(lane_addr + c0, yv);
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(Y + c0);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) dst[j] = make_float4(yv[4 * j], yv[4 * j + 1], yv[4 * j + 2], yv[4 * j + 3]);
+          for (int j = 0; j < 8; ++j)
+            packed[j] = make_uint4(__float_as_uint(yv[4 * j]), __float_as_uint(yv[4 * j + 1]),
+                                   __float_as_uint(yv[4 * j + 2]), __float_as_uint(yv[4 * j + 3]));
+        }
+        if (whole) {
+          uint8_t* buf = my_stg + nbuf * 4096;
+          if (lane == 0) bulk_wait_read<1>();  // the store issued from this buffer two boxes ago has read it
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(buf + stg_off(lane, j)) = packed[j];
+          proxy_fence_writes();
+          __syncwarp();
+          if (lane == 0) {
+            tensor_s2g_2d(&map_out, n0 + c0, r0 + q * 32, buf);
+            bulk_commit();
           }
+          nbuf ^= 1;
+        } else if (valid) {
+          uint8_t* dst = reinterpret_cast<uint8_t*>(a.out) + ((size_t)grow * a.out_ld + n0 + c0) * (MODE == 1 ? 2 : 4);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) reinterpret_cast<uint4*>(dst)[j] = packed[j];
         }
       }
       // this warp's reads of the buffer are done: hand it back to the MMA issuer
@@ -182,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cta(&acce[b]);
     }
+    if (lane == 0) bulk_wait_all();  // every store of this warp has landed before the CTA exits
   }
   tc_fence_before();
   __syncthreads();
@@ -191,8 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int MODE>
-cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const GemmArgs& a, int max_mtiles, int N,
-                   cudaStream_t st) {
+cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const CUtensorMap* map_out, const GemmArgs& a,
+                   int max_mtiles, int N, cudaStream_t st) {
   using C = Cfg<MODE>;
   if (N % C::BN || a.K % BK) return cudaErrorInvalidValue;
   static thread_local int configured = -1;
@@ -208,20 +237,20 @@ cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const Gem
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int n_ntiles = N / C::BN;
   const int grid = max_mtiles * n_ntiles < sms ? max_mtiles * n_ntiles : sms;  // persistent: one CTA per SM
-  grouped_gemm_kernel<MODE><<<grid, kThreads, C::SMEM, st>>>(*map_a, *map_b, a, n_ntiles);
+  grouped_gemm_kernel<MODE><<<grid, kThreads, C::SMEM, st>>>(*map_a, *map_b, *map_out, a, n_ntiles);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_gateup(const CUtensorMap* map_x, const CUtensorMap* map_w1, const GemmArgs& a, int max_mtiles,
-                               int f, cudaStream_t st) {
-  return launch<1>(map_x, map_w1, a, max_mtiles, f, st);
+cudaError_t launch_gemm_gateup(const CUtensorMap* map_x, const CUtensorMap* map_w1, const CUtensorMap* map_h_out,
+                               const GemmArgs& a, int max_mtiles, int f, cudaStream_t st) {
+  return launch<1>(map_x, map_w1, map_h_out, a, max_mtiles, f, st);
 }
 
-cudaError_t launch_gemm_down(const CUtensorMap* map_h, const CUtensorMap* map_w2, const GemmArgs& a, int max_mtiles,
-                             int d, cudaStream_t st) {
-  return launch<2>(map_h, map_w2, a, max_mtiles, d, st);
+cudaError_t launch_gemm_down(const CUtensorMap* map_h, const CUtensorMap* map_w2, const CUtensorMap* map_y_out,
+                             const GemmArgs& a, int max_mtiles, int d, cudaStream_t st) {
+  return launch<2>(map_h, map_w2, map_y_out, a, max_mtiles, d, st);
 }
 
 }  // namespace ft

@@ -23,12 +23,14 @@ struct GemmArgs {
 // H[rows, f] = silu(X W_gate^T) * (X W_up^T) per expert segment.
 // map_x: 2-D (d, rows) bf16, box 64 x 128, 128-byte swizzle.
 // map_w1: 4-D (d, f, {gate, up}, expert) bf16, box 64 x 128 x 1 x 1, 128-byte swizzle.
-cudaError_t launch_gemm_gateup(const CUtensorMap* map_x, const CUtensorMap* map_w1, const GemmArgs& a, int max_mtiles,
-                               int f, cudaStream_t st);
+// map_h_out: 2-D (f, rows) bf16, box 64 x 32, 128-byte swizzle (epilogue stores).
+cudaError_t launch_gemm_gateup(const CUtensorMap* map_x, const CUtensorMap* map_w1, const CUtensorMap* map_h_out,
+                               const GemmArgs& a, int max_mtiles, int f, cudaStream_t st);
 
 // Y[rows, d] = H W_down^T per expert segment.
 // map_h: 2-D (f, rows) bf16, box 64 x 128; map_w2: 3-D (f, d, expert), box 64 x 256; both 128-byte swizzle.
-cudaError_t launch_gemm_down(const CUtensorMap* map_h, const CUtensorMap* map_w2, const GemmArgs& a, int max_mtiles,
-                             int d, cudaStream_t st);
+// map_y_out: 2-D (d, rows) fp32, box 32 x 32, 128-byte swizzle (epilogue stores).
+cudaError_t launch_gemm_down(const CUtensorMap* map_h, const CUtensorMap* map_w2, const CUtensorMap* map_y_out,
+                             const GemmArgs& a, int max_mtiles, int d, cudaStream_t st);
 
 }  // namespace ft

@@ -34,6 +34,7 @@ struct PrefillState {
   uint8_t* lbuf[2] = {nullptr, nullptr};
   int lbuf_layer[2] = {-1, -1};
   CUtensorMap map_w1[2], map_w2[2], map_x, map_h;
+  CUtensorMap map_h_out, map_y_out;  // epilogue store maps (32-row boxes)
   int rows_cap = 0, max_mtiles = 0;
   int32_t* ids = nullptr;
   float* w = nullptr;
@@ -262,6 +263,20 @@ PrefillState* prefill_create(const PrefillConfig& cfg, char* msg, size_t msg_len
     ok = encode_tensor_map(&p->map_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->hbuf, dims, strides, box, msg, msg_len,
                            true);
   }
+  if (ok) {
+    const uint64_t dims[2] = {(uint64_t)cfg.f, (uint64_t)p->rows_cap};
+    const uint64_t strides[1] = {(uint64_t)cfg.f * 2};
+    const uint32_t box[2] = {64, 32};
+    ok = encode_tensor_map(&p->map_h_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->hbuf, dims, strides, box, msg,
+                           msg_len, true);
+  }
+  if (ok) {
+    const uint64_t dims[2] = {(uint64_t)cfg.d, (uint64_t)p->rows_cap};
+    const uint64_t strides[1] = {(uint64_t)cfg.d * 4};
+    const uint32_t box[2] = {32, 32};
+    ok = encode_tensor_map(&p->map_y_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p->ybuf, dims, strides, box, msg,
+                           msg_len, true);
+  }
   if (!ok) {
     prefill_destroy(p);
     return nullptr;
@@ -305,13 +320,13 @@ int prefill_forward(PrefillState* p, int layer, const float* logits, const uint1
     ga.out = p->hbuf;
     ga.out_ld = c.f;
     ga.K = c.d;
-    e = launch_gemm_gateup(&p->map_x, &p->map_w1[b], ga, max_mt, c.f, st);
+    e = launch_gemm_gateup(&p->map_x, &p->map_w1[b], &p->map_h_out, ga, max_mt, c.f, st);
   }
   if (e == cudaSuccess) {
     ga.out = p->ybuf;
     ga.out_ld = c.d;
     ga.K = c.f;
-    e = launch_gemm_down(&p->map_h, &p->map_w2[b], ga, max_mt, c.d, st);
+    e = launch_gemm_down(&p->map_h, &p->map_w2[b], &p->map_y_out, ga, max_mt, c.d, st);
   }
   if (prof) prof->end(st, FT_K_GEMM, pb);
   pb = prof ? prof->begin(st) : nullptr;

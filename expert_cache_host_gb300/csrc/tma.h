@@ -39,6 +39,10 @@ __device__ __forceinline__ void mbar_init_fence() {
 // it a slow load can still be pending when the refill lands.
 __device__ __forceinline__ void proxy_fence_reads() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Ordinary shared-memory writes that a TMA store will read: make them visible
+// to the async proxy first (read-after-write across proxies).
+__device__ __forceinline__ void proxy_fence_writes() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Plain arrival (count 1) on a barrier of this CTA.
 __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(bar)) : "memory");
@@ -88,6 +92,22 @@ __device__ __forceinline__ void tensor_g2s_2d(void* dst, const CUtensorMap* map,
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+
+// 2-D tiled store of one box from shared memory at coordinates (x, y) (x and
+// y >= 0); bulk-group completion (commit, then wait before reusing the source).
+__device__ __forceinline__ void tensor_s2g_2d(const CUtensorMap* map, int x, int y, const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
+               "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most N committed bulk groups of this thread still read shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// wait until every committed bulk group of this thread has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // 3-D tiled tensor copy of one box at coordinates (x, y, z).
 __device__ __forceinline__ void tensor_g2s_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
