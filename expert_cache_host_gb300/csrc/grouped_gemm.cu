@@ -172,8 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float g0 = gv[2 * j], g1 = gv[2 * j + 1];
-              const float h0 = g0 / (1.f + expf(-g0)) * uv[2 * j];
-              const float h1 = g1 / (1.f + expf(-g1)) * uv[2 * j + 1];
+              // H is rounded to bf16 (8-bit mantissa) right after: the fast exp and
+              // divide (relative error ~1e-6) cannot change it beyond that rounding
+              const float h0 = __fdividef(g0, 1.f + __expf(-g0)) * uv[2 * j];
+              const float h1 = __fdividef(g1, 1.f + __expf(-g1)) * uv[2 * j + 1];
               __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
               pw[16 * half + j] = *reinterpret_cast<uint32_t*>(&b2);
             }
