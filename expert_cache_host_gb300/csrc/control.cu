@@ -31,6 +31,8 @@ namespace {
 
 constexpr int kMaxWarps = kControlThreads / 32;
 constexpr int kControlRoutesSmem = 1024;  // routes kept in shared memory by the fused routing
+constexpr int kRankRouteMax = kControlThreads / 2;  // T * E up to which routing ranks every (token, expert) pair
+constexpr int kSmallQ = 4;                // up to this many fills, victims by rounds of a block arg-min
 
 struct Smem {
   int ecount[kMaxExperts];   // routes per local expert
@@ -46,7 +48,10 @@ struct Smem {
   int wsum[kMaxWarps];
   unsigned wmin[kMaxWarps], wmax[kMaxWarps];
   int sc[16];  // scalars
-  int rids[kControlRoutesSmem];  // the step's routes when routed in this kernel
+  unsigned long long wkey[kMaxWarps];  // per-warp minimum keys (small-q victim rounds)
+  int rids[kControlRoutesSmem];        // the step's routes when routed in this kernel
+  float sel[kControlRoutesSmem];       // their logits, in rank order per token
+  float lg[kRankRouteMax];             // the step's logits (routing by rank, 2 T E <= threads)
 };
 
 // Exclusive block scan (NT threads); total returned through *total.
@@ -98,10 +103,65 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   const bool rids_smem = RP > 0 && a.n_routes <= kControlRoutesSmem;
   const int32_t* rids = rids_smem ? sm.rids : a.ids;
   if constexpr (RP > 0) {
-    // 0. routing; the __syncthreads below makes the routes visible to the block
-    for (int t = tid >> 5; t < a.T; t += NW)
-      route_token<RP>(a.logits + (size_t)t * E, E, a.k, a.ids_out + (size_t)t * a.k, a.w_out + (size_t)t * a.k,
-                      a.status, nullptr, rids_smem ? sm.rids + (size_t)t * a.k : nullptr);
+    const int TE = a.T * E, k = a.k;
+    if (rids_smem && 2 * TE <= NT) {
+      // 0. routing by rank (few tokens: at least two threads per (token, expert)
+      //    pair): expert e of token t is chosen at position
+      //    rank(e) = #{e' : l[e'] > l[e], or l[e'] == l[e] and e' < e} if that is < k
+      //    (the same order as k rounds of arg-max: larger logit first, ties to
+      //    the lower index); P threads share the count of one (t, e) pair.  More
+      //    tokens take the warp-per-token path below, which runs them in parallel.
+      bool nan_seen = false;
+      for (int i = tid; i < TE; i += NT) {
+        float x = a.logits[i];
+        if (isnan(x)) {
+          nan_seen = true;
+          x = -INFINITY;
+        }
+        sm.lg[i] = x;
+      }
+      if (__syncthreads_or(nan_seen) && tid == 0) atomicOr(a.status, FT_ST_NAN);
+      int P = NT / TE;
+      P = P >= 8 ? 8 : P >= 4 ? 4 : P >= 2 ? 2 : 1;
+      const int part = tid % P;
+      for (int pair = tid / P; pair < ((TE + NT / P - 1) / (NT / P)) * (NT / P); pair += NT / P) {
+        const bool live = pair < TE;
+        const int t = live ? pair / E : 0, e = live ? pair - t * E : 0;
+        const float v = live ? sm.lg[pair] : 0.f;
+        const float* row = sm.lg + t * E;
+        int cnt = 0;
+        if (live)
+          for (int j = part; j < E; j += P) {
+            const float u = row[j];
+            cnt += (u > v) || (u == v && j < e);
+          }
+        for (int o = P >> 1; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        if (live && part == 0 && cnt < k) {
+          sm.rids[t * k + cnt] = e;
+          sm.sel[t * k + cnt] = v;
+        }
+      }
+      __syncthreads();
+      // weights: softmax over the chosen logits (exp(l_j - l_top) / sum), a warp per token
+      const int lane = tid & 31;
+      for (int t = tid >> 5; t < a.T; t += NW) {
+        const float my_val = lane < k ? sm.sel[t * k + lane] : 0.f;
+        const float top = __shfl_sync(0xffffffffu, my_val, 0);
+        const float ex = lane < k ? expf(my_val - top) : 0.f;
+        float sum = ex;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane < k) {
+          a.ids_out[(size_t)t * k + lane] = sm.rids[t * k + lane];
+          a.w_out[(size_t)t * k + lane] = ex / sum;
+        }
+      }
+    } else {
+      // 0. routing, a warp per token; the __syncthreads below makes the routes visible
+      for (int t = tid >> 5; t < a.T; t += NW)
+        route_token<RP>(a.logits + (size_t)t * E, E, k, a.ids_out + (size_t)t * k, a.w_out + (size_t)t * k, a.status,
+                        nullptr, rids_smem ? sm.rids + (size_t)t * k : nullptr);
+    }
   }
 
   const unsigned now0 = *a.now;
@@ -183,7 +243,40 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   if (q > avail) q = avail;
 
   // 4. victims: the q smallest (last_use, slot) among eligible slots
-  if (q > 0) {
+  if (q > 0 && q <= kSmallQ) {
+    // few fills: q rounds of a block-wide arg-min over the keys; a chosen slot
+    // leaves the eligible set by taking the value `now` in the local copy
+    const int lane = tid & 31, wid = tid >> 5;
+    for (int i = 0; i < q; ++i) {
+      unsigned long long best = ~0ull;
+      for (int s = s0; s < s1; ++s) {
+        const unsigned v = lu[s];
+        const unsigned long long key = ((unsigned long long)v << 32) | (unsigned)s;
+        if (v < now && key < best) best = key;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other < best ? other : best;
+      }
+      if (lane == 0) sm.wkey[wid] = best;
+      __syncthreads();
+      if (wid == 0) {
+        unsigned long long b = lane < NW ? sm.wkey[lane] : ~0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const unsigned long long other = __shfl_xor_sync(0xffffffffu, b, o);
+          b = other < b ? other : b;
+        }
+        if (lane == 0) {
+          const int vs = (int)(b & 0xFFFFFFFFu);
+          sm.victims[i] = vs;
+          lu[vs] = now;
+        }
+      }
+      __syncthreads();
+    }
+  } else if (q > 0) {
     const int lane = tid & 31, wid = tid >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
