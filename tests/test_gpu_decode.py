@@ -61,6 +61,32 @@ def test_route_nan_sets_status(ft):
     assert int(st.item()) & ft.FT_ST_NAN
 
 
+@pytest.mark.parametrize("T,E,k", [(1, 16, 2), (4, 64, 4), (16, 128, 8), (2, 1000, 32)])
+def test_cache_step_routes_and_nan(ft, T, E, k):
+    """Routing inside the control kernel (by rank for few tokens, a warp per
+    token otherwise): ids bit-exact and weights equal to the oracle's on random
+    logits with ties; a NaN logit sets FT_ST_NAN."""
+    cfg = ft.make_config(num_layers=1, num_experts=E, top_k=k, hidden=256, inter=128, num_slots=4, k_max=4, t_max=T)
+    pool = np.zeros(E * ftsynth.expert_bytes(256, 128, 0), dtype=np.uint8)
+    ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
+    try:
+        rng = np.random.default_rng(E + T)
+        lg = rng.integers(-8, 8, size=(T, E)).astype(np.float32) * 0.25  # many ties
+        res = ft.ft_cache_step(ctx, 0, torch.from_numpy(lg).cuda().data_ptr(), T)
+        torch.cuda.synchronize()
+        ref_ids, ref_w = oracle.route(lg, k)
+        g = step_to_host(res, T, k, E, 4)
+        assert np.array_equal(g["ids"], ref_ids)
+        np.testing.assert_allclose(g["w"], ref_w, rtol=2e-6, atol=1e-7)
+        assert ft.ft_get_status(ctx, clear=True) == 0
+        lg[T - 1, E // 2] = np.nan
+        ft.ft_cache_step(ctx, 0, torch.from_numpy(lg).cuda().data_ptr(), T)
+        torch.cuda.synchronize()
+        assert ft.ft_get_status(ctx) & ft.FT_ST_NAN
+    finally:
+        ft.ft_moe_destroy(ctx)
+
+
 # ------------------------------------------------------------------ decode steps
 
 def run_decode(ft, model, S, K_max, r, steps, T=1, fill_mode=0, check_every=1, out_tokens=None, rho=0.9,
