@@ -55,7 +55,7 @@ def _l():
             i32, i64, u64, vp, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_double
             lib.or_route.argtypes = [vp, i32, i32, i32, vp, vp]
             lib.or_cache_step.argtypes = [i32, i32, i32, vp, i64, i64, i32, vp, i32, vp, vp, i32, vp,
-                                          vp, vp, vp, vp, vp, vp, vp, vp, vp]
+                                          vp, vp, vp, vp, vp, vp, vp, vp, vp, i32]
             lib.or_e2m1_value.argtypes = [i32]
             lib.or_e2m1_value.restype = dbl
             lib.or_e8m0_value.argtypes = [i32]
@@ -136,7 +136,10 @@ class Cache:
         self.last_use = np.zeros(self.S, dtype=np.uint32)
         self.now = np.zeros(1, dtype=np.uint32)
 
-    def step(self, layer: int, E: int, ids: np.ndarray, r_num: int, r_den: int, K_max: int) -> StepResult:
+    def step(self, layer: int, E: int, ids: np.ndarray, r_num: int, r_den: int, K_max: int,
+             fill_order: int = 0) -> StepResult:
+        """One control step; fill_order 0 fills the first q misses in ascending
+        id, 1 the q misses with the most routes in the step (ties: lower id)."""
         ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
         nr = ids.size
         cap = max(1, nr)
@@ -151,7 +154,8 @@ class Cache:
         sid = np.empty(cap, dtype=np.int32)
         rc = _l().or_cache_step(layer, E, nr, _p(ids), r_num, r_den, K_max, _p(self.slot_of), self.E_tot,
                                 _p(self.expert_of), _p(self.last_use), self.S, _p(self.now), _p(uniq),
-                                _p(counts), _p(hit), _p(miss), _p(fetch), _p(vict), _p(evic), _p(cpu), _p(sid))
+                                _p(counts), _p(hit), _p(miss), _p(fetch), _p(vict), _p(evic), _p(cpu), _p(sid),
+                                fill_order)
         _check(rc, "or_cache_step")
         n, h, m, q, c = (int(x) for x in counts)
         return StepResult(uniq[:n].copy(), counts, hit[:h].copy(), miss[:m].copy(), fetch[:q].copy(),

@@ -152,9 +152,9 @@ int or_cache_step(int layer, int E, int n_routes, const int32_t* ids, int64_t r_
                   int K_max, int32_t* slot_of, int E_tot, int32_t* expert_of, uint32_t* last_use, int S,
                   uint32_t* now, int32_t* uniq, int32_t* counts, int32_t* hit_list, int32_t* miss_list,
                   int32_t* fetch, int32_t* victims, int32_t* evicted, int32_t* cpu_list,
-                  int32_t* slot_ids) {
+                  int32_t* slot_ids, int fill_order) {
   if (E < 1 || layer < 0 || (int64_t)(layer + 1) * E > E_tot || n_routes < 0 || S < 1 || K_max < 0 ||
-      r_num < 0 || r_den < 1)
+      r_num < 0 || r_den < 1 || fill_order < 0 || fill_order > 1)
     return OR_EARG;
   for (int r = 0; r < n_routes; ++r)
     if (ids[r] < 0 || ids[r] >= E) return OR_ERANGE;
@@ -194,8 +194,32 @@ int or_cache_step(int layer, int E, int n_routes, const int32_t* ids, int64_t r_
   int64_t q = qstar;
   if (q > K_max) q = K_max;
   if (q > avail) q = avail;
-  for (int i = 0; i < q; ++i) fetch[i] = miss_list[i];
-  for (int i = (int)q; i < m; ++i) cpu_list[i - (int)q] = miss_list[i];
+  if (fill_order == 0 || q == m) {
+    /* the first q misses in ascending id */
+    for (int i = 0; i < q; ++i) fetch[i] = miss_list[i];
+    for (int i = (int)q; i < m; ++i) cpu_list[i - (int)q] = miss_list[i];
+  } else {
+    /* most-routed first: the q misses chosen by most routes in this step,
+       ties to the lower id; both lists stay in ascending id */
+    int* nroutes = (int*)calloc((size_t)(m > 0 ? m : 1), sizeof(int));
+    char* chosen = (char*)calloc((size_t)(m > 0 ? m : 1), 1);
+    for (int i = 0; i < m; ++i)
+      for (int r = 0; r < n_routes; ++r)
+        if (layer * E + ids[r] == miss_list[i]) ++nroutes[i];
+    for (int c = 0; c < q; ++c) {
+      int best = -1;
+      for (int i = 0; i < m; ++i)
+        if (!chosen[i] && (best < 0 || nroutes[i] > nroutes[best])) best = i; /* strict: lower id wins ties */
+      chosen[best] = 1;
+    }
+    int nf = 0, nc = 0;
+    for (int i = 0; i < m; ++i) {
+      if (chosen[i]) fetch[nf++] = miss_list[i];
+      else cpu_list[nc++] = miss_list[i];
+    }
+    free(nroutes);
+    free(chosen);
+  }
 
   /* 5. victims */
   if (q > 0) {

@@ -122,7 +122,7 @@ class RecencyListCache:
         self.resident = {}  # expert -> slot
         self.holder = [None] * S
 
-    def step(self, layer, E, ids, r, K_max):
+    def step(self, layer, E, ids, r, K_max, fill_order=0):
         uniq = sorted({layer * E + int(e) for e in ids})
         hits = [u for u in uniq if u in self.resident]
         misses = [u for u in uniq if u not in self.resident]
@@ -131,7 +131,12 @@ class RecencyListCache:
         qstar = min(m, math.floor(m * r + Fraction(1, 2)))
         untouched = [s for s in self.order if s not in touched]
         q = min(qstar, K_max, len(untouched))
-        fetch, cpu = misses[:q], misses[q:]
+        if fill_order == 0:
+            fetch, cpu = misses[:q], misses[q:]
+        else:  # the misses with the most routes in the step first, ties to the lower id
+            routes = [layer * E + int(e) for e in ids]
+            ranked = sorted(misses, key=lambda u: (-routes.count(u), u))
+            fetch, cpu = sorted(ranked[:q]), sorted(ranked[q:])
         victims = untouched[:q]
         evicted = []
         for s, u in zip(victims, fetch):
@@ -394,3 +399,33 @@ def test_expert_linear_in_down_and_up():
         blk[:] = ftsynth.f32_to_bf16(ftsynth.bf16_to_f32(blk) * 2)
         y2 = oracle.expert_ffn(w.view(np.uint8), 0, d, f, x)
         np.testing.assert_allclose(y2, 2 * y, rtol=1e-13, atol=1e-16)
+
+
+# ------------------------------------------------------------------ fill order: most-routed first
+
+def test_fill_order_most_routed_hand_example():
+    """8 experts, 4 empty slots, r = 1/2, three tokens routing [0,5], [5,7], [5,3]:
+    all four experts miss, q* = floor(4/2 + 1/2) = 2.  Expert 5 has three routes
+    and the others one each, so most-routed-first fills {5, 0} (the tie among
+    0, 3, 7 goes to the lowest id) where ascending-id order fills {0, 3}."""
+    ids = np.array([0, 5, 5, 7, 5, 3], dtype=np.int32)
+    res = oracle.Cache(8, 4).step(0, 8, ids, 1, 2, 16, fill_order=1)
+    assert res.counts.tolist() == [4, 0, 4, 2, 2]
+    assert res.fetch.tolist() == [0, 5] and res.cpu_list.tolist() == [3, 7]
+    assert res.victims.tolist() == [0, 1]
+    assert res.slot_ids.tolist() == [0, 1, 1, -1, 1, -1]
+    base = oracle.Cache(8, 4).step(0, 8, ids, 1, 2, 16, fill_order=0)
+    assert base.fetch.tolist() == [0, 3] and base.cpu_list.tolist() == [5, 7]
+
+
+@pytest.mark.parametrize("E,S,k,T,r,K_max", [(6, 3, 2, 3, (1, 2), 4), (8, 4, 2, 4, (1, 3), 2), (5, 2, 1, 4, (2, 3), 8)])
+def test_fill_order_random_replay(E, S, k, T, r, K_max):
+    """Multi-token steps (routes repeat, so route counts differ) against the
+    recency-list model with the same fill order, 400 random steps each."""
+    rng = np.random.default_rng(E * 100 + S * 10 + T)
+    c, mdl = oracle.Cache(2 * E, S), RecencyListCache(2 * E, S)
+    for step in range(400):
+        layer = int(rng.integers(0, 2))
+        ids = np.concatenate([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+        res = c.step(layer, E, ids, r[0], r[1], K_max, fill_order=1)
+        _compare(res, mdl.step(layer, E, ids.tolist(), Fraction(*r), K_max, fill_order=1))
