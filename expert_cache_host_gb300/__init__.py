@@ -22,6 +22,7 @@ FT_ST_ROUTE_RANGE, FT_ST_NAN, FT_ST_CLOCK_WRAP, FT_ST_BAD_SLOT = 1, 2, 4, 8
 FT_DTYPE_BF16, FT_DTYPE_MXFP4 = 0, 1
 FT_DECODE_CACHED, FT_PREFILL_LAYER = 0, 1
 FT_FILL_KERNEL, FT_FILL_COPY_ENGINE = 0, 1
+FT_FILL_ORDER_ID, FT_FILL_ORDER_MOST_ROUTED = 0, 1
 COUNTS = ("n", "hits", "m", "q", "cpu", "n_groups", "now")
 
 # Every symbol include/ft_moe.h declares.
@@ -48,7 +49,8 @@ class ft_config(ctypes.Structure):
         ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("dtype", ctypes.c_int32),
         ("num_slots", ctypes.c_int32), ("k_max", ctypes.c_int32), ("t_max", ctypes.c_int32),
         ("r_num", ctypes.c_int32), ("r_den", ctypes.c_int32), ("prefill_buffers", ctypes.c_int32),
-        ("prefill_t_max", ctypes.c_int32), ("fill_mode", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4),
+        ("prefill_t_max", ctypes.c_int32), ("fill_mode", ctypes.c_int32), ("fill_order", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
     ]
 
 
@@ -111,7 +113,8 @@ def _chk(rc: int) -> int:
 def make_config(**kw) -> ft_config:
     c = ft_config()
     defaults = dict(num_layers=1, num_experts=16, top_k=2, hidden=256, inter=128, dtype=FT_DTYPE_BF16, num_slots=8,
-                    k_max=16, t_max=1, r_num=1, r_den=1, prefill_buffers=0, prefill_t_max=0, fill_mode=FT_FILL_KERNEL)
+                    k_max=16, t_max=1, r_num=1, r_den=1, prefill_buffers=0, prefill_t_max=0, fill_mode=FT_FILL_KERNEL,
+                    fill_order=FT_FILL_ORDER_ID)
     defaults.update(kw)
     for k, v in defaults.items():
         setattr(c, k, int(v))

@@ -242,6 +242,26 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   if (q > a.K_max) q = a.K_max;
   if (q > avail) q = avail;
 
+  // 3b. most-routed first: when only q < m misses are filled, reorder the miss
+  //     list so the q with the most routes in the step (ties: lower id) come
+  //     first, each part still in ascending id; steps 5+ take the first q.
+  if (a.fill_order == FT_FILL_ORDER_MOST_ROUTED && q > 0 && q < m) {
+    const bool is_miss = present && !hit;
+    int rank = 0;
+    if (is_miss) {
+      const int c = sm.ecount[e];
+      for (int i = 0; i < m; ++i) {
+        const int e2 = sm.miss_local[i], c2 = sm.ecount[e2];
+        rank += (c2 > c) || (c2 == c && e2 < e);
+      }
+    }
+    const bool chosen = is_miss && rank < q;
+    int n_chosen;
+    const int cpos = block_scan<NT>(chosen ? 1 : 0, sm.wsum, &n_chosen);  // every rank is read before this returns
+    if (is_miss) sm.miss_local[chosen ? cpos : q + (mpos - cpos)] = e;
+    __syncthreads();
+  }
+
   // 4. victims: the q smallest (last_use, slot) among eligible slots
   if (q > 0 && q <= kSmallQ) {
     // few fills: q rounds of a block-wide arg-min over the keys; a chosen slot

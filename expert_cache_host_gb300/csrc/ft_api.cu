@@ -106,7 +106,8 @@ int check_config(const ft_config& c) {
   if (c.prefill_buffers > 0 && (c.prefill_t_max < 1 || c.prefill_t_max > 65536))
     return fail(FT_E_ARG, "prefill_t_max must be in [1, 65536] when prefill_buffers > 0");
   if (c.fill_mode != FT_FILL_KERNEL && c.fill_mode != FT_FILL_COPY_ENGINE) return fail(FT_E_ARG, "bad fill_mode");
-  for (int i = 0; i < 4; ++i)
+  if (c.fill_order != FT_FILL_ORDER_ID && c.fill_order != FT_FILL_ORDER_MOST_ROUTED) return fail(FT_E_ARG, "bad fill_order");
+  for (int i = 0; i < 3; ++i)
     if (c.reserved[i]) return fail(FT_E_ARG, "reserved fields must be zero");
   if ((long long)c.num_layers * c.num_experts > 0x7fffffffLL) return fail(FT_E_ARG, "too many experts");
   return FT_OK;
@@ -219,6 +220,7 @@ int enqueue_control(ft_ctx* c, int layer, const float* logits, const int32_t* id
   a.S = c->S;
   a.K_max = c->cfg.k_max;
   a.ratio = c->ratio;
+  a.fill_order = c->cfg.fill_order;
   a.ids = ids;
   a.slot_of = c->slot_of;
   a.expert_of = c->expert_of;

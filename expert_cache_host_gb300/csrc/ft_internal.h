@@ -48,6 +48,7 @@ struct LayerBufs {
 
 struct ControlArgs {
   int layer, E, n_routes, S, K_max;
+  int fill_order;  // FT_FILL_ORDER_*
   const long long* ratio;  // device [2]: r_num, r_den of r = BP/BH (set at init or by ft_set_ratio)
   // Fused routing: when logits ([T, E] fp32) is given, the kernel first routes
   // the T tokens into ids_out / w_out ([T, k]) and then reads ids = ids_out.

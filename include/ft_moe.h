@@ -81,6 +81,15 @@ extern "C" {
 #define FT_DECODE_CACHED 0 /* experts from the shared cache, after ft_cache_step */
 #define FT_PREFILL_LAYER 1 /* experts from the full-layer buffers */
 
+/* When only q < m misses can be filled (q* < m, K_max or free slots), which
+ * ones: the first q in ascending expert id (the plain reading of the article,
+ * section "设计：三大机制" 1, Decode bullet), or the q with the most routes in
+ * the step, ties to the lower id (a variant: the experts that serve the most
+ * routes run on the GPU).  Either way the fetch and CPU lists are in ascending
+ * id and fetch i goes to victim i. */
+#define FT_FILL_ORDER_ID 0
+#define FT_FILL_ORDER_MOST_ROUTED 1
+
 #define FT_FILL_KERNEL 0      /* SM copy from the mapped pool; graph capturable */
 #define FT_FILL_COPY_ENGINE 1 /* cudaMemcpyAsync per expert; reads the fetch list back (host sync) */
 
@@ -98,7 +107,8 @@ typedef struct ft_config {
   int32_t prefill_buffers; /* 0: no prefill; 1: one layer buffer (no overlap); 2: double buffer */
   int32_t prefill_t_max; /* tokens per prefill chunk (0 if no prefill) */
   int32_t fill_mode;     /* FT_FILL_KERNEL or FT_FILL_COPY_ENGINE */
-  int32_t reserved[4];   /* must be zero */
+  int32_t fill_order;    /* FT_FILL_ORDER_ID or FT_FILL_ORDER_MOST_ROUTED: which q of the m misses are filled */
+  int32_t reserved[3];   /* must be zero */
 } ft_config;
 
 /* Per-layer results of ft_cache_step / ft_cache_control.  All pointers are

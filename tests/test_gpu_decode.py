@@ -90,14 +90,14 @@ def test_cache_step_routes_and_nan(ft, T, E, k):
 # ------------------------------------------------------------------ decode steps
 
 def run_decode(ft, model, S, K_max, r, steps, T=1, fill_mode=0, check_every=1, out_tokens=None, rho=0.9,
-               rebuild_at=None, graph=False, r_at=None):
+               rebuild_at=None, graph=False, r_at=None, fill_order=0):
     """Decode `steps` steps over all layers through the library and the oracle
     side by side; compare control state every step and outputs every
     `check_every` steps.  r_at: {step: (r_num, r_den)} changes r (ft_set_ratio)
     before that step."""
     L, E, k, d, f = model.L, model.E, model.k, model.d, model.f
     cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, dtype=model.dtype, num_slots=S,
-                         k_max=K_max, t_max=T, r_num=r[0], r_den=r[1], fill_mode=fill_mode)
+                         k_max=K_max, t_max=T, r_num=r[0], r_den=r[1], fill_mode=fill_mode, fill_order=fill_order)
     ctx = ft.ft_moe_init(cfg, model.pool.ctypes.data, model.pool.nbytes)
     try:
         cache = oracle.Cache(L * E, S)
@@ -121,7 +121,7 @@ def run_decode(ft, model, S, K_max, r, steps, T=1, fill_mode=0, check_every=1, o
             for l in range(L):
                 res = ft.ft_cache_step(ctx, l, d_lg[s, l].data_ptr(), T, stream)
                 ref_ids, ref_w = oracle.route(logits[s, l], k)
-                ref = cache.step(l, E, ref_ids, r[0], r[1], K_max)
+                ref = cache.step(l, E, ref_ids, r[0], r[1], K_max, fill_order=fill_order)
                 torch.cuda.synchronize()
                 g = step_to_host(res, T, k, E, K_max)
                 where = f"step {s} layer {l}"
@@ -177,6 +177,16 @@ def test_ratio_changes_at_run_time(ft):
     model = make_model(2, 16, 2, 256, 128, seed=8)
     ctx, _, _ = run_decode(ft, model, S=6, K_max=16, r=(1, 1), steps=10,
                            r_at={2: (1, 2), 4: (0, 1), 6: (2, 1), 8: (3, 4)})
+    ft.ft_moe_destroy(ctx)
+
+
+@pytest.mark.parametrize("r,K_max", [((1, 2), 16), ((1, 1), 2), ((1, 3), 8)])
+def test_fill_order_most_routed(ft, r, K_max):
+    """FT_FILL_ORDER_MOST_ROUTED with several tokens per step (route counts
+    differ): control state bit-exact and outputs against the oracle run with
+    the same fill order, while q < m (r < 1, or K_max below the misses)."""
+    model = make_model(2, 16, 3, 256, 128, seed=12)
+    ctx, _, _ = run_decode(ft, model, S=8, K_max=K_max, r=r, steps=8, T=4, fill_order=ft.FT_FILL_ORDER_MOST_ROUTED)
     ft.ft_moe_destroy(ctx)
 
 
