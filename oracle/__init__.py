@@ -161,6 +161,24 @@ class Cache:
         return StepResult(uniq[:n].copy(), counts, hit[:h].copy(), miss[:m].copy(), fetch[:q].copy(),
                           vict[:q].copy(), evic[:q].copy(), cpu[:c].copy(), sid[:nr].copy())
 
+    def rebuild_retain(self, new_S: int) -> "Cache":
+        """A rebuild at new_S slots that keeps the most recently used residents
+        (the variant of the article's runtime cache rebuild, section
+        "弹性边缘资源管理": GPU memory changes only performance, so any subset
+        of the residents may stay).  Residents are taken in order of last use,
+        most recent first, ties to the lower slot; the i-th kept one moves to
+        slot i with its last use; the clock is unchanged."""
+        kept = sorted((s for s in range(self.S) if self.expert_of[s] >= 0),
+                      key=lambda s: (-int(self.last_use[s]), s))[:new_S]
+        n = Cache(self.E_tot, new_S)
+        n.now[:] = self.now
+        for i, s in enumerate(kept):
+            u = int(self.expert_of[s])
+            n.expert_of[i] = u
+            n.slot_of[u] = i
+            n.last_use[i] = self.last_use[s]
+        return n
+
 
 # ---------------------------------------------------------------- experts
 

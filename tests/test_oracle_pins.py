@@ -429,3 +429,47 @@ def test_fill_order_random_replay(E, S, k, T, r, K_max):
         ids = np.concatenate([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
         res = c.step(layer, E, ids, r[0], r[1], K_max, fill_order=1)
         _compare(res, mdl.step(layer, E, ids.tolist(), Fraction(*r), K_max, fill_order=1))
+
+
+# ------------------------------------------------------------------ MRU-retaining rebuild
+
+def test_rebuild_retain_hand_example():
+    """4 slots holding experts 10, 11, 12, 13 with last uses 5, 9, 9, 2 (slots
+    0..3); a rebuild to 2 slots keeps the two most recent: experts 11 and 12
+    (both used at 9; slot 1 before slot 2), in new slots 0 and 1."""
+    c = oracle.Cache(16, 4)
+    for s, (u, t) in enumerate([(10, 5), (11, 9), (12, 9), (13, 2)]):
+        c.expert_of[s], c.slot_of[u], c.last_use[s] = u, s, t
+    c.now[0] = 9
+    n = c.rebuild_retain(2)
+    assert n.expert_of.tolist() == [11, 12] and n.last_use.tolist() == [9, 9] and int(n.now[0]) == 9
+    assert n.slot_of[11] == 0 and n.slot_of[12] == 1 and n.slot_of[10] == -1 and n.slot_of[13] == -1
+
+
+@pytest.mark.parametrize("S,new_S", [(12, 20), (12, 12), (12, 5), (30, 1)])
+def test_rebuild_retain_properties(S, new_S):
+    """After random steps: the kept experts are a most-recent prefix of the
+    residents (none left out is more recent than one kept), the table stays
+    consistent, and -- when every resident fits -- the next step classifies
+    every route exactly as without the rebuild."""
+    rng = np.random.default_rng(S * 7 + new_S)
+    L, E, k = 3, 10, 3
+    c = oracle.Cache(L * E, S)
+    for _ in range(60):
+        layer = int(rng.integers(0, L))
+        c.step(layer, E, rng.choice(E, size=k, replace=False).astype(np.int32), 1, 1, 64)
+    n = c.rebuild_retain(new_S)
+    kept = {int(u) for u in n.expert_of if u >= 0}
+    res = {int(c.expert_of[s]): int(c.last_use[s]) for s in range(S) if c.expert_of[s] >= 0}
+    assert len(kept) == min(len(res), new_S) and kept <= set(res)
+    if kept:
+        assert min(res[u] for u in kept) >= max([res[u] for u in set(res) - kept], default=-1)
+    for i in range(new_S):
+        if n.expert_of[i] >= 0:
+            assert n.slot_of[n.expert_of[i]] == i and n.last_use[i] == res[int(n.expert_of[i])]
+    assert int(np.count_nonzero(n.slot_of >= 0)) == len(kept)
+    if new_S >= len(res):
+        layer = 1
+        ids = rng.choice(E, size=k, replace=False).astype(np.int32)
+        a, b = c.step(layer, E, ids, 1, 1, 64), n.step(layer, E, ids, 1, 1, 64)
+        assert a.hit_list.tolist() == b.hit_list.tolist() and a.miss_list.tolist() == b.miss_list.tolist()
