@@ -30,6 +30,7 @@ EXPORTS = (
     "ft_moe_init", "ft_moe_destroy", "ft_cache_step", "ft_cache_control", "ft_moe_forward", "ft_cache_rebuild",
     "ft_get_status", "ft_get_counters", "ft_get_table", "ft_slot_ptr", "ft_get_epoch", "ft_num_slots", "ft_route",
     "ft_profile_enable", "ft_profile_read", "ft_decode_experts_noalloc", "ft_host_alloc", "ft_host_free", "ft_set_ratio",
+    "ft_cache_rebuild_retain",
     "ft_last_error",
 )
 FT_K_ROUTE, FT_K_CONTROL, FT_K_FILL, FT_K_EXPERTS, FT_K_MERGE, FT_K_UPLOAD, FT_K_PREFILL, FT_K_GEMM = range(8)
@@ -93,6 +94,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "ft_decode_experts_noalloc": ([vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp], i32),
             "ft_host_alloc": ([sz, ctypes.POINTER(vp)], i32),
             "ft_set_ratio": ([vp, i32, i32, vp], i32),
+            "ft_cache_rebuild_retain": ([vp, i32], i32),
             "ft_host_free": ([vp], i32),
             "ft_last_error": ([], ctypes.c_char_p),
         }
@@ -154,6 +156,10 @@ def ft_moe_forward(ctx: int, layer: int, mode: int, logits_ptr: int, hidden_ptr:
 
 def ft_cache_rebuild(ctx: int, new_slots: int) -> None:
     _chk(load().ft_cache_rebuild(ctypes.c_void_p(ctx), new_slots))
+
+
+def ft_cache_rebuild_retain(ctx: int, new_slots: int) -> None:
+    _chk(load().ft_cache_rebuild_retain(ctypes.c_void_p(ctx), new_slots))
 
 
 def ft_get_status(ctx: int, clear: bool = False) -> int:

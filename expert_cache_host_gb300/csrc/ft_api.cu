@@ -2,6 +2,7 @@
 // order in which one MoE layer step's kernels are enqueued.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -439,6 +440,67 @@ int ft_set_ratio(ft_ctx* c, int32_t r_num, int32_t r_den, void* stream) {
   if (!c) return fail(FT_E_ARG, "null context");
   if (r_num < 0 || r_den < 1) return fail(FT_E_ARG, "r = r_num/r_den needs r_num >= 0, r_den >= 1");
   CU(launch_set_ratio(c->ratio, r_num, r_den, static_cast<cudaStream_t>(stream)));
+  return FT_OK;
+}
+
+int ft_cache_rebuild_retain(ft_ctx* c, int new_slots) {
+  if (!c) return fail(FT_E_ARG, "null context");
+  if (new_slots < 1 || new_slots > kMaxSlots) return fail(FT_E_ARG, "new_slots must be in [1, %d]", kMaxSlots);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(c->xfer, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return fail(FT_E_STATE, "rebuild during stream capture");
+  CU(cudaDeviceSynchronize());
+  const int S_old = c->S;
+  std::vector<int32_t> eo(S_old);
+  std::vector<uint32_t> lu(S_old);
+  CU(cudaMemcpy(eo.data(), c->expert_of, sizeof(int32_t) * S_old, cudaMemcpyDeviceToHost));
+  CU(cudaMemcpy(lu.data(), c->last_use, sizeof(uint32_t) * S_old, cudaMemcpyDeviceToHost));
+  // residents, most recent first (ties: lower slot); the first new_slots stay
+  std::vector<int> kept;
+  for (int s = 0; s < S_old; ++s)
+    if (eo[s] >= 0) kept.push_back(s);
+  std::stable_sort(kept.begin(), kept.end(), [&](int x, int y) { return lu[x] > lu[y]; });
+  if ((int)kept.size() > new_slots) kept.resize(new_slots);
+
+  // the new arena and tables next to the old ones (the old cache survives a failure)
+  uint8_t* old_arena = c->arena;
+  int32_t* old_eo = c->expert_of;
+  uint32_t* old_lu = c->last_use;
+  const CUtensorMap old_wd = c->tmap_wd, old_gu = c->tmap_gu;
+  c->arena = nullptr;
+  c->expert_of = nullptr;
+  c->last_use = nullptr;
+  int rc = alloc_arena(c, new_slots);
+  if (rc) {
+    cudaFree(c->arena);
+    cudaFree(c->expert_of);
+    cudaFree(c->last_use);
+    c->arena = old_arena;
+    c->expert_of = old_eo;
+    c->last_use = old_lu;
+    c->tmap_wd = old_wd;
+    c->tmap_gu = old_gu;
+    c->S = S_old;
+    return rc;
+  }
+  std::vector<int32_t> so_new(c->E_tot, -1), eo_new(new_slots, -1);
+  std::vector<uint32_t> lu_new(new_slots, 0);
+  for (size_t i = 0; i < kept.size(); ++i) {
+    const int s = kept[i], u = eo[s];
+    eo_new[i] = u;
+    so_new[u] = (int32_t)i;
+    lu_new[i] = lu[s];
+    CU(cudaMemcpyAsync(c->arena + i * c->Bx, old_arena + (size_t)s * c->Bx, c->Bx, cudaMemcpyDeviceToDevice, c->xfer));
+  }
+  CU(cudaMemcpy(c->slot_of, so_new.data(), sizeof(int32_t) * c->E_tot, cudaMemcpyHostToDevice));
+  CU(cudaMemcpy(c->expert_of, eo_new.data(), sizeof(int32_t) * new_slots, cudaMemcpyHostToDevice));
+  CU(cudaMemcpy(c->last_use, lu_new.data(), sizeof(uint32_t) * new_slots, cudaMemcpyHostToDevice));
+  CU(cudaStreamSynchronize(c->xfer));
+  cudaFree(old_arena);
+  cudaFree(old_eo);
+  cudaFree(old_lu);
+  for (auto& lb : c->layers) lb.last_T = -1;
+  ++c->epoch;
   return FT_OK;
 }
 

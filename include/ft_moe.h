@@ -218,6 +218,18 @@ int ft_get_table(ft_ctx* ctx, int32_t* slot_of, int32_t* expert_of, uint32_t* la
 /* Device pointer of slot s's bytes in the arena (for tests), or NULL. */
 void* ft_slot_ptr(ft_ctx* ctx, int slot);
 
+/* As ft_cache_rebuild, but the most recently used residents stay: residents
+ * ordered by last use (most recent first, ties to the lower slot) fill the new
+ * slots 0, 1, ... with their last use; the clock and counters are unchanged
+ * (FreeToken article, section "设计：三大机制" 3, runtime cache rebuild: GPU
+ * memory changes only performance, so which residents survive is a choice;
+ * this one keeps the recency the LRU would act on).  The old and the new
+ * arenas exist together during the call; if the new one does not fit,
+ * FT_E_NOMEM is returned and the cache is left as it was.  Epoch +1 on
+ * success; graphs captured before must be re-captured.  Synchronises.
+ * Errors: FT_E_ARG, FT_E_STATE (during a capture), FT_E_NOMEM, FT_E_CUDA. */
+int ft_cache_rebuild_retain(ft_ctx* ctx, int new_slots);
+
 /* Change r = BP/BH (FreeToken article, section "设计：三大机制" 1, Decode
  * bullet: the fill-vs-CPU split of the misses follows the measured link and
  * host bandwidths, which vary at run time) for the steps enqueued on `stream`

@@ -115,9 +115,14 @@ def run_decode(ft, model, S, K_max, r, steps, T=1, fill_mode=0, check_every=1, o
                 r = r_at[s]
                 ft.ft_set_ratio(ctx, r[0], r[1], stream)
             if rebuild_at is not None and s == rebuild_at[0]:
-                ft.ft_cache_rebuild(ctx, rebuild_at[1])
-                cache = oracle.Cache(L * E, rebuild_at[1])
+                if len(rebuild_at) > 2 and rebuild_at[2] == "retain":
+                    ft.ft_cache_rebuild_retain(ctx, rebuild_at[1])
+                    cache = cache.rebuild_retain(rebuild_at[1])
+                else:
+                    ft.ft_cache_rebuild(ctx, rebuild_at[1])
+                    cache = oracle.Cache(L * E, rebuild_at[1])
                 S = rebuild_at[1]
+                compare_table(ft, ctx, cache, f"after the rebuild at step {s}")
             for l in range(L):
                 res = ft.ft_cache_step(ctx, l, d_lg[s, l].data_ptr(), T, stream)
                 ref_ids, ref_w = oracle.route(logits[s, l], k)
@@ -218,6 +223,18 @@ def test_rebuild_mid_run(ft):
     model = make_model(2, 16, 2, 256, 128, seed=4)
     ctx, cache, _ = run_decode(ft, model, S=8, K_max=16, r=(1, 1), steps=10, rebuild_at=(5, 3))
     assert ft.ft_get_epoch(ctx) == 1 and ft.ft_num_slots(ctx) == 3
+    ft.ft_moe_destroy(ctx)
+
+
+@pytest.mark.parametrize("new_S", [3, 12, 20])
+def test_rebuild_retain_mid_run(ft, new_S):
+    """ft_cache_rebuild_retain: the most recently used residents stay (fewer,
+    equal or more slots); the table equals the oracle's retaining rebuild and
+    the steps after it (hits on the kept experts, whose bytes moved to new
+    slots) keep matching the oracle."""
+    model = make_model(2, 16, 2, 256, 128, seed=13)
+    ctx, cache, _ = run_decode(ft, model, S=8, K_max=16, r=(1, 1), steps=12, rebuild_at=(6, new_S, "retain"))
+    assert ft.ft_get_epoch(ctx) == 1 and ft.ft_num_slots(ctx) == new_S
     ft.ft_moe_destroy(ctx)
 
 
