@@ -24,6 +24,7 @@
 //  6. rewrite route ids to slot ids (-1 = CPU);
 //  7. group the routes by resident expert for the expert kernel (dispatch).
 #include "ft_internal.h"
+#include "tma.h"
 #include "route_warp.cuh"
 
 namespace ft {
@@ -96,9 +97,7 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   const int E = a.E, S = a.S;
   const int base_id = a.layer * E;
 
-  // this layer's residency of every expert, fetched while the routes are computed
-  const int slot_pre = tid < E ? a.slot_of[base_id + tid] : -1;
-  const long long r_num = a.ratio[0], r_den = a.ratio[1];
+
   // routes: read from shared memory when this kernel routed them
   const bool rids_smem = RP > 0 && a.n_routes <= kControlRoutesSmem;
   const int32_t* rids = rids_smem ? sm.rids : a.ids;
@@ -142,6 +141,9 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
         }
       }
       __syncthreads();
+      // the routes and weights go to the layer's step buffers, which the
+      // previous kernel may still read (a one-layer model's last merge)
+      pdl_wait();
       // weights: softmax over the chosen logits (exp(l_j - l_top) / sum), a warp per token
       const int lane = tid & 31;
       for (int t = tid >> 5; t < a.T; t += NW) {
@@ -157,13 +159,21 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
         }
       }
     } else {
-      // 0. routing, a warp per token; the __syncthreads below makes the routes visible
+      // 0. routing, a warp per token, straight into the step buffers (so after
+      // the previous kernel); the __syncthreads below makes the routes visible
+      pdl_wait();
       for (int t = tid >> 5; t < a.T; t += NW)
         route_token<RP>(a.logits + (size_t)t * E, E, k, a.ids_out + (size_t)t * k, a.w_out + (size_t)t * k, a.status,
                         nullptr, rids_smem ? sm.rids + (size_t)t * k : nullptr);
     }
   }
 
+  // The routing above reads only the logits, so it may run while the previous
+  // kernel (the last layer's merge) finishes; its results and the cache table
+  // are written only after that kernel has completed.
+  pdl_wait();
+  const int slot_pre = tid < E ? a.slot_of[base_id + tid] : -1;  // this layer's residency of every expert
+  const long long r_num = a.ratio[0], r_den = a.ratio[1];
   const unsigned now0 = *a.now;
   const bool wrap = now0 == 0xFFFFFFFFu;
   const unsigned now = now0 + 1u;
@@ -492,8 +502,10 @@ cudaError_t launch_rp(const ControlArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured_for = dev;
   }
-  control_kernel<RP, NT><<<1, NT, smem, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_config(cfg, attr, dim3(1), dim3(NT), smem, st);
+  return cudaLaunchKernelEx(&cfg, control_kernel<RP, NT>, a);
 }
 
 __global__ void set_ratio_kernel(long long* ratio, long long r_num, long long r_den) {

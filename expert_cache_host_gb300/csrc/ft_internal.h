@@ -115,6 +115,22 @@ cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_experts_mxfp4(const DecodeArgs& a, int tokens, cudaStream_t st);
 
 // out[t] = partial[t] + sum_j [slot_ids >= 0] w[t,j] * sum_c ypart[t*k+j][c]
+// Launch attributes for programmatic dependent launch: the kernel may start
+// while the previous kernel of the stream runs and calls pdl_wait() before it
+// touches anything that kernel (or an earlier one) writes or reads.
+inline void pdl_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st) {
+  cfg = cudaLaunchConfig_t{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+}
+
 // ratio[0] = r_num, ratio[1] = r_den, stream-ordered (capturable).
 cudaError_t launch_set_ratio(long long* ratio, long long r_num, long long r_den, cudaStream_t st);
 

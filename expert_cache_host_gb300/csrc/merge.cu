@@ -11,6 +11,7 @@
 // loads together, so the merge costs about one L2 round trip), and the rows
 // are then summed in a fixed order, so the result is deterministic.
 #include "ft_internal.h"
+#include "tma.h"
 
 namespace ft {
 namespace {
@@ -23,6 +24,10 @@ __global__ void __launch_bounds__(kCols* kRows)
                  const float* __restrict__ w, const float4* __restrict__ partial, float4* __restrict__ out, int k,
                  int d4) {
   __shared__ float4 red[kRows][kCols];
+  // the next kernel (the next layer's routing) may start now; this one waits
+  // for the experts' partial sums
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.y;
   const int col = threadIdx.x % kCols, row = threadIdx.x / kCols;
   const int i = blockIdx.x * kCols + col;
@@ -76,10 +81,11 @@ cudaError_t launch_merge(const float* ypart, int n_chunks, const int32_t* slot_i
   if (T <= 0) return cudaSuccess;
   const int d4 = d / 4;
   dim3 grid((d4 + kCols - 1) / kCols, T), block(kCols * kRows);
-  merge_kernel<<<grid, block, 0, st>>>(reinterpret_cast<const float4*>(ypart), n_chunks, slot_ids, w,
-                                       reinterpret_cast<const float4*>(partial), reinterpret_cast<float4*>(out), k,
-                                       d4);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_config(cfg, attr, grid, block, 0, st);
+  return cudaLaunchKernelEx(&cfg, merge_kernel, reinterpret_cast<const float4*>(ypart), n_chunks, slot_ids, w,
+                            reinterpret_cast<const float4*>(partial), reinterpret_cast<float4*>(out), k, d4);
 }
 
 }  // namespace ft

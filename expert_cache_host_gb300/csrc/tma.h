@@ -43,6 +43,14 @@ __device__ __forceinline__ void proxy_fence_reads() { asm volatile("fence.proxy.
 // to the async proxy first (read-after-write across proxies).
 __device__ __forceinline__ void proxy_fence_writes() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Programmatic dependent launch.  pdl_wait: block until the grid this one
+// depends on (the previous kernel in the stream, when launched with
+// programmatic stream serialization) has completed and its writes are
+// visible; a no-op otherwise.  pdl_trigger: let the dependent grid launch now
+// (it still waits with pdl_wait before using this grid's results).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Plain arrival (count 1) on a barrier of this CTA.
 __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(bar)) : "memory");
