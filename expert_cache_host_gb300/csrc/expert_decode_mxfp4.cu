@@ -2,14 +2,14 @@
 // consecutive elements of a row; OCP Microscaling v1.0), HBM-bound.
 //
 // Same work split and data movement as the bf16 decode kernel: one CTA per
-// (resident expert, chunk of FC = 64 rows of f), a producer warp streaming
-// 16 KB TMA tiles through a ring with full/empty mbarriers, 16 consumer warps.
-//  - gate/up codes: 64 rows x 256 bytes boxes of a 4-D map (d/2, f, {g,u}, slot);
-//    the chunk's gate/up scales (64 rows x d/32 bytes each) arrive once by
-//    two 1-D bulk copies;
-//  - down codes: 256 rows x 32 bytes boxes of a 3-D map (f/2, d, slot), two per
-//    stage; the two down scales of each row for this chunk are read directly
-//    (the 32 chunks of one expert share those sectors in L2).
+// (resident expert, chunk of FC = 32 rows of f), a producer warp streaming
+// 16 KB stages through a TMA ring with full/empty mbarriers, 16 consumer warps.
+//  - gate/up codes: 32 rows x 256 bytes boxes of a 4-D map (d/2, f, {g,u}, slot),
+//    two column blocks per stage; the chunk's gate/up scales (32 rows x d/32
+//    bytes each) arrive once by two 1-D bulk copies;
+//  - down codes: 256 rows x 16 bytes boxes of a 3-D map (f/2, d, slot), four per
+//    stage (1024 rows); each row's one down scale for this chunk is read
+//    directly, a stage ahead (the 64 chunks of an expert share those sectors).
 // Arithmetic: a 16-byte piece of a row is 32 elements = exactly one scale
 // group.  cvt.rn.f16x2.e2m1x2 turns each code byte into two exact f16 values;
 // the group's products with the f16 activations accumulate in two chains of
@@ -26,7 +26,7 @@
 namespace ft {
 namespace {
 
-constexpr int FC = kDecodeChunkFp4;        // 64 rows of f per CTA
+constexpr int FC = kDecodeChunkFp4;        // 32 rows of f per CTA
 constexpr int kConsumers = 512;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kTile = 16384;
@@ -100,8 +100,8 @@ __host__ __device__ inline Layout smem_layout(int d) {
   L.scbar = L.empty + 8 * NS;
   L.sc = (L.scbar + 8 + 127) / 128 * 128;                   // [2][FC][d/32] scale bytes
   L.xs = L.sc + (size_t)2 * FC * (d / 32);                  // [TB][d/2] f16x2 pairs
-  L.gu = L.xs + (size_t)TB * (d / 2) * 4;                   // [2][FC][TB] fp32 row sums
-  L.hs = L.gu + sizeof(float) * 2 * FC * TB;                // [TB][FC/2] f16x2
+  L.gu = L.xs + (size_t)TB * (d / 2) * 4;                   // [2 halves][2][FC][TB] fp32 row sums
+  L.hs = L.gu + sizeof(float) * 4 * FC * TB;                // [TB][FC/2] f16x2
   L.rs = L.hs + (size_t)TB * (FC / 2) * 4;                  // [TB]
   L.total = L.rs + sizeof(int) * TB;
   return L;
@@ -144,11 +144,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   const unsigned char* sc_gate = ex + 3 * (df / 2);                 // [f][d/32]
   const unsigned char* sc_down = sc_gate + 2 * (df / 32);           // [d][f/32]
   const int n_batches = (r1 - r0 + TB - 1) / TB;
-  const int cb_n = d / 512;            // 256-byte column blocks per gate/up row
-  const int P1 = 2 * cb_n;
-  const int NTL = P1 + d / 512;        // down stages: 512 rows (two 256-row boxes) each
+  const int cb_n = d / 512;              // 256-byte column blocks per gate/up row
+  const int gst = (cb_n + 1) / 2;        // gate (or up) stages: two column blocks each
+  const int nbox = d / 256;              // 256-row down boxes
+  const int dst = (nbox + 3) / 4;        // down stages: four boxes (1024 rows) each
+  const int NTL = 2 * gst + dst;         // stages per token batch
   const int total = n_batches * NTL;
-  const int sc_row = d / 32;           // scale bytes per gate/up row
+  const int sc_row = d / 32;             // scale bytes per gate/up row
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -171,15 +173,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       uint32_t ph = 0;
       for (int n = 0, i = 0; n < total; ++n) {
         if (n >= NS && !mbar_wait(&empty[s], ph ^ 1u, late)) late = true;
-        unsigned char* dst = ring + s * kTile;
-        mbar_expect_tx(&full[s], kTile);
-        if (i < P1) {
-          const int m = i < cb_n ? 0 : 1, cb = i - m * cb_n;
-          tensor_g2s_4d(dst, &tmap_gu, cb * 256, c * FC, m, slot, &full[s]);
+        unsigned char* dstp = ring + s * kTile;
+        if (i < 2 * gst) {
+          const int m = i < gst ? 0 : 1, cb0 = 2 * (i - m * gst), nb = min(2, cb_n - cb0);
+          mbar_expect_tx(&full[s], nb * (kTile / 2));
+          for (int b = 0; b < nb; ++b)
+            tensor_g2s_4d(dstp + b * (kTile / 2), &tmap_gu, (cb0 + b) * 256, c * FC, m, slot, &full[s]);
         } else {
-          const int j = i - P1;
-          tensor_g2s_3d(dst, &tmap_wd, c * (FC / 2), j * 512, slot, &full[s]);
-          tensor_g2s_3d(dst + kTile / 2, &tmap_wd, c * (FC / 2), j * 512 + 256, slot, &full[s]);
+          const int j = i - 2 * gst, box0 = 4 * j, nb = min(4, nbox - box0);
+          mbar_expect_tx(&full[s], nb * (kTile / 4));
+          for (int b = 0; b < nb; ++b)
+            tensor_g2s_3d(dstp + b * (kTile / 4), &tmap_wd, c * (FC / 2), (box0 + b) * 256, slot, &full[s]);
         }
         if (++i == NTL) i = 0;
         if (++s == NS) {
@@ -198,10 +202,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   const int lane = tid & 31;
-  // gate/up: thread = 16-byte column piece p of rows 2rp and 2rp + 1, so the
-  // piece's 32 activations are loaded once per tile for two rows
-  const int p = tid & 15, rp = tid >> 4;
-  const int rowq = tid >> 1, q = tid & 1;     // down: row within a 256-row box, scale group of the chunk
+  // gate/up: thread = 16-byte column piece p of rows 2rp and 2rp + 1 of the
+  // stage's column block hb, so a piece's 32 activations are loaded once per
+  // stage for two rows
+  const int p = tid & 15, rp = (tid >> 4) & 15, hb = tid >> 8;
   const int n_chunks = f / FC;
   bool late = false;
   int s = 0;
@@ -244,30 +248,37 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
 #pragma unroll 1
-      for (int cb = 0; cb < cb_n; ++cb) {
+      for (int k2 = 0; k2 < gst; ++k2) {
         if (!mbar_wait(&full[s], ph, late)) late = true;
-        const unsigned char* buf = ring + s * kTile + (2 * rp) * 256 + p * 16;
-        const uint4 w0 = *reinterpret_cast<const uint4*>(buf);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(buf + 256);
+        const int cb = 2 * k2 + hb;
+        uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+        if (cb < cb_n) {
+          const unsigned char* buf = ring + s * kTile + hb * (kTile / 2) + (2 * rp) * 256 + p * 16;
+          w0 = *reinterpret_cast<const uint4*>(buf);
+          w1 = *reinterpret_cast<const uint4*>(buf + 256);
+        }
         release();
-        const int grp = cb * 16 + p;  // scale group (and global 16-word piece) of this thread
-        const float s0 = e8m0(sc[(m * FC + 2 * rp) * sc_row + grp]);
-        const float s1 = e8m0(sc[(m * FC + 2 * rp + 1) * sc_row + grp]);
+        if (cb < cb_n) {
+          const int grp = cb * 16 + p;  // scale group (and global 16-word piece) of this thread
+          const float s0 = e8m0(sc[(m * FC + 2 * rp) * sc_row + grp]);
+          const float s1 = e8m0(sc[(m * FC + 2 * rp + 1) * sc_row + grp]);
 #pragma unroll
-        for (int t = 0; t < TB; ++t) {
-          if (t < nt) {
-            const unsigned* xrow = xs + (size_t)t * (d / 2) + grp * 16;
-            uint4 xv[4];
+          for (int t = 0; t < TB; ++t) {
+            if (t < nt) {
+              const unsigned* xrow = xs + (size_t)t * (d / 2) + grp * 16;
+              uint4 xv[4];
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-              xv[c4] = *reinterpret_cast<const uint4*>(xrow + (((c4 + (grp >> 1)) & 3) << 2));
-            acc[m][0][t] = fmaf(group_dot(w0, xv), s0, acc[m][0][t]);
-            acc[m][1][t] = fmaf(group_dot(w1, xv), s1, acc[m][1][t]);
+              for (int c4 = 0; c4 < 4; ++c4)
+                xv[c4] = *reinterpret_cast<const uint4*>(xrow + (((c4 + (grp >> 1)) & 3) << 2));
+              acc[m][0][t] = fmaf(group_dot(w0, xv), s0, acc[m][0][t]);
+              acc[m][1][t] = fmaf(group_dot(w1, xv), s1, acc[m][1][t]);
+            }
           }
         }
       }
     }
-    // row sums: the 16 pieces of a row pair are 16 consecutive lanes
+    // row sums: the 16 pieces of a row pair are 16 consecutive lanes; the two
+    // column-block halves are added in the SwiGLU step
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
@@ -279,49 +290,45 @@ __global__ void __launch_bounds__(kThreads, 2)
           v += __shfl_xor_sync(0xffffffffu, v, 4);
           v += __shfl_xor_sync(0xffffffffu, v, 2);
           v += __shfl_xor_sync(0xffffffffu, v, 1);
-          if (p == 0 && t < nt) gu[(m * FC + 2 * rp + i) * TB + t] = v;
+          if (p == 0 && t < nt) gu[((hb * 2 + m) * FC + 2 * rp + i) * TB + t] = v;
         }
     consumer_sync();
     if (tid < (FC / 2) * TB) {
       const int pr = tid % (FC / 2), t = tid / (FC / 2);
       if (t < nt) {
-        const float g0 = gu[(0 * FC + 2 * pr) * TB + t], u0 = gu[(1 * FC + 2 * pr) * TB + t];
-        const float g1 = gu[(0 * FC + 2 * pr + 1) * TB + t], u1 = gu[(1 * FC + 2 * pr + 1) * TB + t];
+        auto rsum = [&](int m, int row) { return gu[((0 * 2 + m) * FC + row) * TB + t] + gu[((1 * 2 + m) * FC + row) * TB + t]; };
+        const float g0 = rsum(0, 2 * pr), u0 = rsum(1, 2 * pr), g1 = rsum(0, 2 * pr + 1), u1 = rsum(1, 2 * pr + 1);
         const __half2 hv = __floats2half2_rn(g0 / (1.f + expf(-g0)) * u0, g1 / (1.f + expf(-g1)) * u1);
         hs[t * (FC / 2) + pr] = *reinterpret_cast<const unsigned*>(&hv);
       }
     }
     consumer_sync();
 
-    // the two down scales of a stage are fetched one stage ahead (L2 latency off the loop)
-    const unsigned char* scd = sc_down + (size_t)rowq * (f / 32) + c * 2 + q;
-    const size_t sc_step = (size_t)256 * (f / 32);  // 256 rows of scales
-    unsigned char e0n = __ldg(scd), e1n = __ldg(scd + sc_step);
+    // down: a stage holds rows 1024 j .. 1024 j + 1023 (16 bytes each, in order);
+    // thread = rows tid and tid + 512 of the stage, one scale group each
+    const size_t sc_step = (size_t)512 * (f / 32);  // 512 rows of scales
+    const unsigned char* scd = sc_down + (size_t)tid * (f / 32) + c;
+    unsigned char e0n = tid < d ? __ldg(scd) : 0, e1n = tid + 512 < d ? __ldg(scd + sc_step) : 0;
 #pragma unroll 1
-    for (int j = 0; j < d / 512; ++j) {
-      const int row0 = j * 512 + rowq, row1 = row0 + 256;
+    for (int j = 0; j < dst; ++j) {
+      const int row0 = j * 1024 + tid, row1 = row0 + 512;
       const float s0 = e8m0(e0n), s1 = e8m0(e1n);
-      if (j + 1 < d / 512) {
-        e0n = __ldg(scd + (size_t)(2 * j + 2) * sc_step);
-        e1n = __ldg(scd + (size_t)(2 * j + 3) * sc_step);
+      if (j + 1 < dst) {
+        e0n = row0 + 1024 < d ? __ldg(scd + (size_t)(2 * j + 2) * sc_step) : 0;
+        e1n = row1 + 1024 < d ? __ldg(scd + (size_t)(2 * j + 3) * sc_step) : 0;
       }
       if (!mbar_wait(&full[s], ph, late)) late = true;
       const unsigned char* buf = ring + s * kTile + tid * 16;
-      const uint4 w0 = *reinterpret_cast<const uint4*>(buf);
-      const uint4 w1 = *reinterpret_cast<const uint4*>(buf + kTile / 2);
+      const uint4 w0 = row0 < d ? *reinterpret_cast<const uint4*>(buf) : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 w1 = row1 < d ? *reinterpret_cast<const uint4*>(buf + kTile / 2) : make_uint4(0u, 0u, 0u, 0u);
       release();
 #pragma unroll
       for (int t = 0; t < TB; ++t) {
         if (t < nt) {
-          const uint4* hp = reinterpret_cast<const uint4*>(hs + t * (FC / 2) + q * 16);
-          float v0 = group_dot(w0, hp) * s0, v1 = group_dot(w1, hp) * s1;
-          v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
-          v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-          if (q == 0) {
-            float* yp = a.ypart + ((size_t)rs[t] * n_chunks + c) * d;
-            yp[row0] = v0;
-            yp[row1] = v1;
-          }
+          const uint4* hp = reinterpret_cast<const uint4*>(hs + t * (FC / 2));
+          float* yp = a.ypart + ((size_t)rs[t] * n_chunks + c) * d;
+          if (row0 < d) yp[row0] = group_dot(w0, hp) * s0;
+          if (row1 < d) yp[row1] = group_dot(w1, hp) * s1;
         }
       }
     }

@@ -25,7 +25,7 @@ constexpr int kControlThreads = 1024;
 // Rows of the intermediate dimension f handled by one decode work unit
 // (bf16 experts / MXFP4 experts).
 constexpr int kDecodeChunk = 32;
-constexpr int kDecodeChunkFp4 = 64;
+constexpr int kDecodeChunkFp4 = 32;
 
 // Per-layer fixed-shape step buffers (device).
 struct LayerBufs {
