@@ -21,6 +21,10 @@
 // The ring runs from the gate/up tiles straight into the down tiles.  Every
 // mbarrier wait is bounded; a wait that runs out records FT_ST_TIMEOUT and
 // the kernel carries on to a bounded drain, so it always terminates.
+// Except after the fill's event, the launch is a programmatic dependent one:
+// its CTAs may be placed while the control kernel still runs and wait for it
+// before their first load; with one token the hidden row is then fetched
+// beside the group values, and the route ids only after the gate/up pass.
 // The page's activation is not named; SwiGLU is the one of the served model
 // families (FreeToken article, section "核心亮点").
 #include <math.h>
@@ -37,6 +41,7 @@ constexpr int kThreads = kConsumers + 32;  // + 1 producer warp
 constexpr int kTokBatch = 4;               // tokens per pass over the weights
 constexpr int NS = 5;                      // ring stages
 constexpr int kTile = 16384;               // bytes per stage
+constexpr int kXPre = 2;                   // uint4 of a hidden row per consumer (d <= 8192)
 
 __device__ __forceinline__ float bf_lo(unsigned v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(unsigned v) { return __uint_as_float(v & 0xFFFF0000u); }
@@ -63,6 +68,16 @@ __device__ __forceinline__ float dot8h(const uint4 w, const float4 h0, const flo
   s = fmaf(bf_lo(w.w), h1.z, s);
   s = fmaf(bf_hi(w.w), h1.w, s);
   return s;
+}
+
+// 16-byte read-only load kept where it is written (not sunk past the branches
+// that follow), so that it overlaps the loads issued after it.
+__device__ __forceinline__ uint4 ld_nc_early(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
 }
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
@@ -103,6 +118,20 @@ __global__ void __launch_bounds__(kThreads, 2)
   int* rs = reinterpret_cast<int*>(dyn + Ly.rs);            // [kTokBatch]
 
   const int c = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
+  // Everything below reads what earlier kernels of the stream wrote.
+  pdl_wait();
+  // One token (decode): every route reads hidden row 0, so its copy can start
+  // now, beside the loads of the group values.
+  const bool one_tok = a.T == 1;
+  uint4 xpre[kXPre];
+  if (one_tok && tid < kConsumers) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.hidden);
+#pragma unroll
+    for (int j = 0; j < kXPre; ++j) {
+      const int i = tid + j * kConsumers;
+      if (i < d / 8) xpre[j] = ld_nc_early(src + i);
+    }
+  }
   // Fetch every per-group value at once (one memory round trip before the
   // first TMA issue); the group arrays hold at least max_groups (+1) entries,
   // so these loads are in bounds for every g of the grid.
@@ -188,13 +217,26 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int b = 0; b < n_batches; ++b) {
     const int tb = r0 + b * kTokBatch;
     const int nt = min(kTokBatch, r1 - tb);
+    // route ids of the batch: needed only for the partial-sum rows, so they
+    // reach shared memory after the gate/up pass
+    const int my_route = tid < nt ? a.group_routes[tb + tid] : 0;
     consumer_sync();  // previous batch done with xs / rs / hs
-    if (tid < nt) rs[tid] = a.group_routes[tb + tid];
-    for (int t = 0; t < nt; ++t) {
-      const int tok = a.group_routes[tb + t] / a.k;
-      const uint4* src = reinterpret_cast<const uint4*>(a.hidden + (size_t)tok * d);
-      uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)t * d);
-      for (int i = tid; i < d / 8; i += kConsumers) dst[i] = src[i];
+    if (one_tok) {
+      for (int t = 0; t < nt; ++t) {
+        uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)t * d);
+#pragma unroll
+        for (int j = 0; j < kXPre; ++j) {
+          const int i = tid + j * kConsumers;
+          if (i < d / 8) dst[i] = xpre[j];
+        }
+      }
+    } else {
+      for (int t = 0; t < nt; ++t) {
+        const int tok = a.group_routes[tb + t] / a.k;
+        const uint4* src = reinterpret_cast<const uint4*>(a.hidden + (size_t)tok * d);
+        uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)t * d);
+        for (int i = tid; i < d / 8; i += kConsumers) dst[i] = src[i];
+      }
     }
     consumer_sync();
 
@@ -237,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         v += __shfl_xor_sync(0xffffffffu, v, 1);
         if (cq == 0 && t < nt) gu[(m * FC + rl) * kTokBatch + t] = v;
       }
+    if (tid < nt) rs[tid] = my_route;
     consumer_sync();
     if (tid < FC * kTokBatch) {
       const int row = tid % FC, t = tid / FC;
@@ -296,8 +339,15 @@ cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st) {
     configured_dev = dev;
     configured_smem = smem;
   }
-  decode_bf16_kernel<<<grid, block, smem, st>>>(*a.tmap_gu, *a.tmap_wd, a);
-  return cudaGetLastError();
+  if (a.select == 2) {
+    // after a wait on another stream's event: no programmatic overlap
+    decode_bf16_kernel<<<grid, block, smem, st>>>(*a.tmap_gu, *a.tmap_wd, a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_config(cfg, attr, grid, block, smem, st);
+  return cudaLaunchKernelEx(&cfg, decode_bf16_kernel, *a.tmap_gu, *a.tmap_wd, a);
 }
 
 }  // namespace ft

@@ -80,7 +80,7 @@ extern "C" int ft_decode_experts_noalloc(const void* arena_dev, int num_slots, i
   if (!arena_dev || !slot_ids_dev || !weights_dev || !hidden_dev || !out_dev) return fail(FT_E_ARG, "null pointer");
   if (num_slots < 1 || T < 1 || top_k < 1 || top_k > kMaxTopK) return fail(FT_E_ARG, "bad slot count, T or top_k");
   if (hidden < 256 || hidden % 256 || hidden > 8192) return fail(FT_E_ARG, "hidden must be a multiple of 256, <= 8192");
-  if (inter < kDecodeChunk || inter % kDecodeChunk) return fail(FT_E_ARG, "inter must be a multiple of 32");
+  if (inter < kDecodeChunk || inter % kDecodeChunk) return record_error(FT_E_ARG, "inter must be a multiple of %d", kDecodeChunk);
   if (reinterpret_cast<uintptr_t>(arena_dev) % 16) return fail(FT_E_ARG, "the arena must be 16-byte aligned");
   const size_t need = noalloc_scratch_needed(T, top_k, hidden, inter);
   if (need > kStaticScratchBytes) {
@@ -145,6 +145,7 @@ extern "C" int ft_decode_experts_noalloc(const void* arena_dev, int num_slots, i
   a.k = top_k;
   a.dtype = FT_DTYPE_BF16;
   a.max_groups = R;
+  a.T = T;
   a.counts = counts;
   a.group_slot = group_slot;
   a.group_off = group_off;

@@ -575,6 +575,7 @@ int ft_moe_forward(ft_ctx* c, int layer, int mode, const float* logits, const ui
   a.k = c->cfg.top_k;
   a.dtype = c->cfg.dtype;
   a.max_groups = T * c->cfg.top_k < c->cfg.num_experts ? T * c->cfg.top_k : c->cfg.num_experts;
+  a.T = T;
   a.counts = lb.counts;
   a.group_slot = lb.group_slot;
   a.group_off = lb.group_off;

@@ -6,18 +6,21 @@
 // float32 buffer `partial` (NULL = 0), and the GPU side is the weighted sum of
 // the expert outputs of the routes that have a slot:
 //     out[t] = partial[t] + sum_j [slot_ids[t,j] >= 0] w[t,j] * sum_c ypart[t*k+j, c]
-// A block owns 8 float4 columns of one token; its 32 thread rows split the
-// k * n_chunks (route, chunk) partials of those columns (each row issues its
-// loads together, so the merge costs about one L2 round trip), and the rows
-// are then summed in a fixed order, so the result is deterministic.
+// A block owns 4 float4 columns of one token; its 64 thread rows split the
+// k * n_chunks (route, chunk) partials of those columns (each row issues up
+// to 8 loads together, so the merge costs about one L2 round trip), and the
+// rows are then summed in a fixed order (eight runs of eight rows, then the
+// eight run sums), so the result is deterministic.
 #include "ft_internal.h"
 #include "tma.h"
 
 namespace ft {
 namespace {
 
-constexpr int kCols = 8;   // float4 columns per block
-constexpr int kRows = 32;  // (route, chunk) lanes per block
+constexpr int kCols = 4;   // float4 columns per block
+constexpr int kRows = 64;  // (route, chunk) lanes per block
+constexpr int kUn = 8;     // loads in flight per lane
+constexpr int kRun = 8;    // rows per run of the final sum
 
 __global__ void __launch_bounds__(kCols* kRows)
     merge_kernel(const float4* __restrict__ ypart, int n_chunks, const int32_t* __restrict__ slot_ids,
@@ -34,24 +37,29 @@ __global__ void __launch_bounds__(kCols* kRows)
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (i < d4) {
     const int npairs = k * n_chunks;
-    for (int p0 = row; p0 < npairs; p0 += 4 * kRows) {
-      float4 v[4];
-      float wv[4];
+    for (int p0 = row; p0 < npairs; p0 += kUn * kRows) {
+      float4 v[kUn];
+      float wv[kUn];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kUn; ++u) {
         const int p = p0 + u * kRows;
         wv[u] = 0.f;
         v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (p < npairs) {
+          // the three loads are independent (ypart is allocated for every
+          // route); a route without a slot then contributes exactly nothing
           const int j = p / n_chunks, c = p - j * n_chunks, r = t * k + j;
-          if (slot_ids[r] >= 0) {
-            wv[u] = w[r];
-            v[u] = ypart[((size_t)r * n_chunks + c) * d4 + i];
+          const int sid = __ldg(slot_ids + r);
+          const float wr = __ldg(w + r);
+          const float4 y = ypart[((size_t)r * n_chunks + c) * d4 + i];
+          if (sid >= 0) {
+            wv[u] = wr;
+            v[u] = y;
           }
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kUn; ++u) {
         acc.x = fmaf(wv[u], v[u].x, acc.x);
         acc.y = fmaf(wv[u], v[u].y, acc.y);
         acc.z = fmaf(wv[u], v[u].z, acc.z);
@@ -61,14 +69,29 @@ __global__ void __launch_bounds__(kCols* kRows)
   }
   red[row][col] = acc;
   __syncthreads();
+  // each run of kRun rows into its first row, in row order
+  if (row < kRows / kRun) {
+    float4 s = red[row * kRun][col];
+#pragma unroll
+    for (int q = 1; q < kRun; ++q) {
+      const float4 x = red[row * kRun + q][col];
+      s.x += x.x;
+      s.y += x.y;
+      s.z += x.z;
+      s.w += x.w;
+    }
+    red[row * kRun][col] = s;
+  }
+  __syncthreads();
   if (row == 0 && i < d4) {
     float4 o = partial ? partial[(size_t)t * d4 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int q = 0; q < kRows; ++q) {
-      o.x += red[q][col].x;
-      o.y += red[q][col].y;
-      o.z += red[q][col].z;
-      o.w += red[q][col].w;
+#pragma unroll
+    for (int q = 0; q < kRows / kRun; ++q) {
+      const float4 x = red[q * kRun][col];
+      o.x += x.x;
+      o.y += x.y;
+      o.z += x.z;
+      o.w += x.w;
     }
     out[(size_t)t * d4 + i] = o;
   }
