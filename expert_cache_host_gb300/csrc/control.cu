@@ -93,9 +93,6 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
   extern __shared__ __align__(16) unsigned char dyn[];
   Smem& sm = *reinterpret_cast<Smem*>(dyn);
   unsigned* lu = reinterpret_cast<unsigned*>(dyn + sizeof(Smem));  // [S] last_use copy
-  // The expert kernel that follows may be placed on the SMs now; it waits for
-  // this grid to complete before it reads anything.
-  pdl_trigger();
   const int tid = threadIdx.x;
   const int E = a.E, S = a.S;
   const int base_id = a.layer * E;

@@ -21,10 +21,10 @@
 // The ring runs from the gate/up tiles straight into the down tiles.  Every
 // mbarrier wait is bounded; a wait that runs out records FT_ST_TIMEOUT and
 // the kernel carries on to a bounded drain, so it always terminates.
-// Except after the fill's event, the launch is a programmatic dependent one:
-// its CTAs may be placed while the control kernel still runs and wait for it
-// before their first load; with one token the hidden row is then fetched
-// beside the group values, and the route ids only after the gate/up pass.
+// The kernel waits for the previous kernel of the stream before its first load
+// (so it may be launched as a programmatic dependent where no other kernel
+// needs the SMs meanwhile); with one token the hidden row is fetched beside
+// the group values, and the route ids only after the gate/up pass.
 // The page's activation is not named; SwiGLU is the one of the served model
 // families (FreeToken article, section "核心亮点").
 #include <math.h>
@@ -214,6 +214,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   };
 
+  if (one_tok) {
+    // the one token's row in every batch row, for every batch (the first
+    // barrier of the batch loop publishes it)
+    for (int t = 0; t < kTokBatch; ++t) {
+      uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)t * d);
+#pragma unroll
+      for (int j = 0; j < kXPre; ++j) {
+        const int i = tid + j * kConsumers;
+        if (i < d / 8) dst[i] = xpre[j];
+      }
+    }
+  }
   for (int b = 0; b < n_batches; ++b) {
     const int tb = r0 + b * kTokBatch;
     const int nt = min(kTokBatch, r1 - tb);
@@ -221,16 +233,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // reach shared memory after the gate/up pass
     const int my_route = tid < nt ? a.group_routes[tb + tid] : 0;
     consumer_sync();  // previous batch done with xs / rs / hs
-    if (one_tok) {
-      for (int t = 0; t < nt; ++t) {
-        uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)t * d);
-#pragma unroll
-        for (int j = 0; j < kXPre; ++j) {
-          const int i = tid + j * kConsumers;
-          if (i < d / 8) dst[i] = xpre[j];
-        }
-      }
-    } else {
+    if (!one_tok) {
       for (int t = 0; t < nt; ++t) {
         const int tok = a.group_routes[tb + t] / a.k;
         const uint4* src = reinterpret_cast<const uint4*>(a.hidden + (size_t)tok * d);
@@ -339,8 +342,7 @@ cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st) {
     configured_dev = dev;
     configured_smem = smem;
   }
-  if (a.select == 2) {
-    // after a wait on another stream's event: no programmatic overlap
+  if (!a.pdl) {
     decode_bf16_kernel<<<grid, block, smem, st>>>(*a.tmap_gu, *a.tmap_wd, a);
     return cudaGetLastError();
   }

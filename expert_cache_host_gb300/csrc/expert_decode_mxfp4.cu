@@ -30,6 +30,7 @@ constexpr int FC = kDecodeChunkFp4;        // 32 rows of f per CTA
 constexpr int kConsumers = 512;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kTile = 16384;
+constexpr int kXPre = 4;  // uint4 of a hidden row per consumer (d <= 16384)
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(bar)) : "memory");
@@ -107,6 +108,22 @@ __host__ __device__ inline Layout smem_layout(int d) {
   return L;
 }
 
+// 16-byte read-only load kept where it is written (not sunk past the branches
+// that follow), so that it overlaps the loads issued after it.
+__device__ __forceinline__ uint4 ld_nc_early(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// bf16 pair -> f16 pair (the activations' f16 copy)
+__device__ __forceinline__ unsigned bf2_to_h2(unsigned v) {
+  const __half2 hv = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+  return *reinterpret_cast<const unsigned*>(&hv);
+}
+
 template <int TB, int NS>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tmap_gu, const __grid_constant__ CUtensorMap tmap_wd,
@@ -125,6 +142,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   int* rs = reinterpret_cast<int*>(dyn + Ly.rs);
 
   const int c = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
+  // Everything below reads what earlier kernels of the stream wrote.
+  pdl_wait();
+  // One token (TB == 1 is launched for one-token steps): every route reads
+  // hidden row 0, so its copy can start now, beside the group values.
+  uint4 xpre[kXPre];
+  if (TB == 1 && tid < kConsumers) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.hidden);
+#pragma unroll
+    for (int j = 0; j < kXPre; ++j) {
+      const int i = tid + j * kConsumers;
+      if (i < d / 8) xpre[j] = ld_nc_early(src + i);
+    }
+  }
   // Fetch every per-group value at once (one memory round trip before the
   // first TMA issue); the group arrays hold at least max_groups (+1) entries,
   // so these loads are in bounds for every g of the grid.
@@ -220,18 +250,32 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   };
 
+  if (TB == 1) {
+    // the one token's row, for every batch (the first barrier of the batch
+    // loop publishes it)
+#pragma unroll
+    for (int j = 0; j < kXPre; ++j) {
+      const int i = tid + j * kConsumers;
+      if (i < d / 8) {
+        xs[xs_swz(4 * i + 0)] = bf2_to_h2(xpre[j].x);
+        xs[xs_swz(4 * i + 1)] = bf2_to_h2(xpre[j].y);
+        xs[xs_swz(4 * i + 2)] = bf2_to_h2(xpre[j].z);
+        xs[xs_swz(4 * i + 3)] = bf2_to_h2(xpre[j].w);
+      }
+    }
+  }
   for (int b = 0; b < n_batches; ++b) {
     const int tb = r0 + b * TB;
     const int nt = min(TB, r1 - tb);
+    // route ids of the batch: needed only for the partial-sum rows, so they
+    // reach shared memory after the gate/up pass
+    const int my_route = tid < nt ? a.group_routes[tb + tid] : 0;
     consumer_sync();
-    if (tid < nt) rs[tid] = a.group_routes[tb + tid];
-    for (int t = 0; t < nt; ++t) {
-      const int tok = a.group_routes[tb + t] / a.k;
-      const unsigned* src = reinterpret_cast<const unsigned*>(a.hidden + (size_t)tok * d);  // bf16 pairs
-      for (int i = tid; i < d / 2; i += kConsumers) {
-        const unsigned v = src[i];
-        const __half2 hv = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-        xs[(size_t)t * (d / 2) + xs_swz(i)] = *reinterpret_cast<const unsigned*>(&hv);
+    if (TB != 1) {
+      for (int t = 0; t < nt; ++t) {
+        const int tok = a.group_routes[tb + t] / a.k;
+        const unsigned* src = reinterpret_cast<const unsigned*>(a.hidden + (size_t)tok * d);  // bf16 pairs
+        for (int i = tid; i < d / 2; i += kConsumers) xs[(size_t)t * (d / 2) + xs_swz(i)] = bf2_to_h2(src[i]);
       }
     }
     consumer_sync();
@@ -292,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           v += __shfl_xor_sync(0xffffffffu, v, 1);
           if (p == 0 && t < nt) gu[((hb * 2 + m) * FC + 2 * rp + i) * TB + t] = v;
         }
+    if (tid < nt) rs[tid] = my_route;
     consumer_sync();
     if (tid < (FC / 2) * TB) {
       const int pr = tid % (FC / 2), t = tid / (FC / 2);
@@ -350,9 +395,15 @@ cudaError_t launch(const DecodeArgs& a, cudaStream_t st) {
     configured_dev = dev;
     configured_smem = smem;
   }
-  dim3 grid(a.f / FC, a.max_groups);
-  decode_mxfp4_kernel<TB, NS><<<grid, kThreads, smem, st>>>(*a.tmap_gu, *a.tmap_wd, a);
-  return cudaGetLastError();
+  const dim3 grid(a.f / FC, a.max_groups), block(kThreads);
+  if (!a.pdl) {
+    decode_mxfp4_kernel<TB, NS><<<grid, block, smem, st>>>(*a.tmap_gu, *a.tmap_wd, a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_config(cfg, attr, grid, block, smem, st);
+  return cudaLaunchKernelEx(&cfg, decode_mxfp4_kernel<TB, NS>, *a.tmap_gu, *a.tmap_wd, a);
 }
 
 }  // namespace

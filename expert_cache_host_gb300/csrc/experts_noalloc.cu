@@ -146,6 +146,7 @@ extern "C" int ft_decode_experts_noalloc(const void* arena_dev, int num_slots, i
   a.dtype = FT_DTYPE_BF16;
   a.max_groups = R;
   a.T = T;
+  a.pdl = 1;  // no fill runs beside this launch
   a.counts = counts;
   a.group_slot = group_slot;
   a.group_off = group_off;

@@ -109,7 +109,8 @@ struct DecodeArgs {
   // group_new[g] == 0; 2 = groups with group_new[g] != 0.
   const int32_t* group_new;
   int select;
-  int T;  // tokens of the step
+  int T;    // tokens of the step
+  int pdl;  // launch as a programmatic dependent of the previous kernel
 };
 cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st);
 // MXFP4 experts; ypart is [T*k][f/kDecodeChunkFp4][d]; tokens = T of the step.
