@@ -48,10 +48,12 @@ L2_BYTES = 129 * 2 ** 20
 
 # DRAM bytes per launch from ncu captures (profiles/); None once the kernel changed.
 # dram__bytes_read + dram__bytes_write / algorithmic bytes of the decode expert
-# kernel over three A3B launches captured with ncu (--set full); the
+# kernels over the launches captured with ncu (--set full): three A3B bf16
+# launches (6 + 2 + 5 experts) and two V4 MXFP4 launches (4 + 2 experts); the
 # traffic reported per launch is this ratio times the launch's algorithmic bytes
 NCU_TRAFFIC_RATIO = {
-    "decode_experts": 123_127_296 / 122_683_392,
+    "decode_experts": 123_111_424 / 122_683_392,
+    "decode_experts_mxfp4": 80_432_896 / 80_216_064,
 }
 
 
@@ -522,7 +524,8 @@ def build_line(args, w, world, dec, link_gbs, pre, ctl, peaks):
                      "share": dec["shares"].get("fill")},
         "roofline_experts": {"bound": "hbm", "kernel": "decode experts", "achieved": round(ex_gbs, 1),
                              "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ex_gbs / peaks["hbm_gbs"], 4),
-                             "traffic": round(NCU_TRAFFIC_RATIO["decode_experts"] * dec["ex_bytes"] / max(1, dec["ex_n"])),
+                             "traffic": round(NCU_TRAFFIC_RATIO["decode_experts" if w["dtype"] == 0 else "decode_experts_mxfp4"]
+                                              * dec["ex_bytes"] / max(1, dec["ex_n"])),
                              "traffic_source": "ncu ratio x algorithmic bytes per launch", "peak_source": peaks["source"],
                              "bytes_per_launch": round(dec["ex_bytes"] / max(1, dec["ex_n"])),
                              "avg_launch_us": round(dec["ex_ms"] / max(1, dec["ex_n"]) * 1e3, 2),
