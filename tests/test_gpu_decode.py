@@ -247,11 +247,15 @@ def test_ragged_shapes_and_larger_model(ft):
 
 # ------------------------------------------------------------------ control alone
 
-@pytest.mark.parametrize("S,K_max,r,s_zipf", [(64, 64, (1, 1), 1.2), (40, 8, (1, 2), 0.6), (300, 512, (1, 1), 0.6),
-                                                (6144, 128, (1, 1), 1.2)])
-def test_control_zipf_stress_small(ft, S, K_max, r, s_zipf):
-    """The control kernel alone on Zipf route streams: 64 tokens x top-8 x E=128."""
-    L, E, k, T, steps = 4, 128, 8, 64, 25
+@pytest.mark.parametrize("S,K_max,r,s_zipf,T", [(64, 64, (1, 1), 1.2, 64), (40, 8, (1, 2), 0.6, 64),
+                                                  (300, 512, (1, 1), 0.6, 64), (6144, 128, (1, 1), 1.2, 64),
+                                                  (64, 64, (1, 1), 0.6, 16), (300, 128, (1, 1), 1.2, 16),
+                                                  (40, 8, (1, 1), 0.6, 1)])
+def test_control_zipf_stress_small(ft, S, K_max, r, s_zipf, T):
+    """The control kernel alone on Zipf route streams: T tokens x top-8 x E=128
+    (64 tokens take the full block, 16 and 1 the half block; both victim
+    searches, block arg-min rounds for q <= 4 and radix select above, run)."""
+    L, E, k, steps = 4, 128, 8, 25
     d, f = 256, 128  # the control path never reads expert bytes: smallest legal expert shape
     bx = ftsynth.expert_bytes(d, f, 0)
     pool = np.zeros(L * E * bx, dtype=np.uint8)
