@@ -188,6 +188,8 @@ def run_decode_leg(args, w, world, local, pool, hid, lg):
     ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
     t_init = time.time() - t0
     try:
+        if args.cpu_exec:
+            ft.ft_cpu_executor(ctx, args.cpu_exec)
         d_hid = torch.from_numpy(hid.view(np.int16)).cuda()
         d_lg = torch.from_numpy(lg).cuda()
         cur_hid = torch.empty((L, T, d), dtype=torch.int16, device="cuda")
@@ -504,12 +506,19 @@ def make_host_pool(args, w):
     return hp, pool, time.time() - t0
 
 
+def metric_name(args, w):
+    m = METRIC if w["dtype"] == 0 else METRIC.replace("A3B-style, batch 1", f"V4-Flash-style MXFP4, batch {w['T']}")
+    if args.cpu_exec:
+        m = m.replace("GPU side; CPU-routed experts arrive as a partial sum", "GPU + CPU expert executor")
+    return m
+
+
 def build_line(args, w, world, dec, link_gbs, pre, ctl, peaks):
     ex_gbs = dec["ex_bytes"] / (dec["ex_ms"] / 1e3) / 1e9 if dec["ex_ms"] else 0.0
     fill_gbs = dec["fill_bytes"] / (dec["fill_ms"] / 1e3) / 1e9 if dec["fill_ms"] else 0.0
     bx = ftsynth.expert_bytes(w["d"], w["f"], w["dtype"])
     line = {
-        "metric": METRIC if w["dtype"] == 0 else METRIC.replace("A3B-style, batch 1", f"V4-Flash-style MXFP4, batch {w['T']}"),
+        "metric": metric_name(args, w),
         "value": round(dec["value"], 3), "unit": "tok/s", "n_gpus": world, "steps": dec["K"],
         "warmup": dec["W"], "ms_per_step": round(dec["elapsed"] / dec["K"] * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w["dtype"] == 0 else "e2m1*e8m0 x bf16 -> f16/f32",
@@ -593,6 +602,10 @@ def main():
                     help="report mode (not the bench line): decode miss rate and tok/s over cache capacities of "
                          "5/10/25/50%% of the pool, or prefill chunk time over prompt lengths 4k/8k/16k with and "
                          "without the double buffer")
+    ap.add_argument("--ratio", default=None, help="r = BP/BH as NUM/DEN for the decode workload (default 1/1: every "
+                    "miss filled)")
+    ap.add_argument("--cpu-exec", type=int, default=0, help="variant: the context's CPU expert executor with this many "
+                    "host threads computes the misses that are not filled (not the bench line)")
     ap.add_argument("--pool", choices=("pinned", "registered"), default="pinned",
                     help="pinned: pool written into ft_host_alloc memory; registered: pageable pool pinned by "
                          "ft_moe_init after the write")
@@ -617,6 +630,12 @@ def main():
             w["L"] = max(1, fit)
             w["desc"] += f" [host RAM holds {w['L']} of the 43 layers]"
         args.no_prefill = args.no_control = True
+    if args.ratio:
+        num, den = (int(x) for x in args.ratio.split("/"))
+        w["r"] = (num, den)
+        w["desc"] = w["desc"].replace("BP/BH=1", f"BP/BH={num}/{den}")
+    if args.cpu_exec:
+        w["desc"] += f", CPU executor with {args.cpu_exec} host threads for the unfilled misses"
     if args.layers or args.slots:
         w["L"], w["S"] = args.layers or w["L"], args.slots or w["S"]
         w["desc"] += f" [profiling case: L={w['L']}, S={w['S']}]"

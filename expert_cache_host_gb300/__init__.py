@@ -30,12 +30,12 @@ EXPORTS = (
     "ft_moe_init", "ft_moe_destroy", "ft_cache_step", "ft_cache_control", "ft_moe_forward", "ft_cache_rebuild",
     "ft_get_status", "ft_get_counters", "ft_get_table", "ft_slot_ptr", "ft_get_epoch", "ft_num_slots", "ft_route",
     "ft_profile_enable", "ft_profile_read", "ft_decode_experts_noalloc", "ft_host_alloc", "ft_host_free", "ft_set_ratio",
-    "ft_cache_rebuild_retain",
+    "ft_cache_rebuild_retain", "ft_cpu_executor", "ft_cpu_experts",
     "ft_last_error",
 )
-FT_K_ROUTE, FT_K_CONTROL, FT_K_FILL, FT_K_EXPERTS, FT_K_MERGE, FT_K_UPLOAD, FT_K_PREFILL, FT_K_GEMM = range(8)
-FT_K_COUNT = 8
-KERNEL_CLASSES = ("route", "control", "fill", "experts", "merge", "upload", "prefill", "gemm")
+FT_K_ROUTE, FT_K_CONTROL, FT_K_FILL, FT_K_EXPERTS, FT_K_MERGE, FT_K_UPLOAD, FT_K_PREFILL, FT_K_GEMM, FT_K_CPU = range(9)
+FT_K_COUNT = 9
+KERNEL_CLASSES = ("route", "control", "fill", "experts", "merge", "upload", "prefill", "gemm", "cpu")
 
 
 class FtError(RuntimeError):
@@ -95,6 +95,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "ft_host_alloc": ([sz, ctypes.POINTER(vp)], i32),
             "ft_set_ratio": ([vp, i32, i32, vp], i32),
             "ft_cache_rebuild_retain": ([vp, i32], i32),
+            "ft_cpu_executor": ([vp, i32], i32),
+            "ft_cpu_experts": ([vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32], i32),
             "ft_host_free": ([vp], i32),
             "ft_last_error": ([], ctypes.c_char_p),
         }
@@ -193,6 +195,30 @@ def ft_slot_ptr(ctx: int, slot: int) -> int:
 
 def ft_set_ratio(ctx: int, r_num: int, r_den: int, stream: int = 0) -> None:
     _chk(load().ft_set_ratio(ctypes.c_void_p(ctx), r_num, r_den, ctypes.c_void_p(stream)))
+
+
+def ft_cpu_executor(ctx: int, threads: int) -> None:
+    """Enable (threads >= 1) or disable (0) the context's CPU expert executor."""
+    _chk(load().ft_cpu_executor(ctypes.c_void_p(ctx), threads))
+
+
+def ft_cpu_experts(pool, num_experts: int, top_k: int, hidden: int, inter: int, dtype: int, layer: int,
+                   ids, weights, slot_ids, hidden_rows, threads: int = 1):
+    """The executor's sum over the routes with slot id < 0, on host numpy
+    arrays: returns partial float32 [T, hidden]."""
+    import numpy as np
+    pool = np.ascontiguousarray(pool).view(np.uint8).reshape(-1)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    T = ids.shape[0]
+    w = np.ascontiguousarray(weights, dtype=np.float32).reshape(T, top_k)
+    sid = np.ascontiguousarray(slot_ids, dtype=np.int32).reshape(T, top_k)
+    hid = np.ascontiguousarray(hidden_rows).view(np.uint16).reshape(T, hidden)
+    out = np.empty((T, hidden), dtype=np.float32)
+    v = ctypes.c_void_p
+    _chk(load().ft_cpu_experts(v(pool.ctypes.data), num_experts, top_k, hidden, inter, dtype, layer, T,
+                               v(ids.ctypes.data), v(w.ctypes.data), v(sid.ctypes.data), v(hid.ctypes.data),
+                               v(out.ctypes.data), threads))
+    return out
 
 
 def ft_get_epoch(ctx: int) -> int:

@@ -87,6 +87,7 @@ struct ft_ctx {
   int32_t* h_victims = nullptr;
 
   PrefillState* prefill = nullptr;
+  CpuExec* cpu = nullptr;  // host expert executor, or none
   Profiler prof;
 };
 
@@ -189,6 +190,8 @@ void free_all(ft_ctx* c) {
   if (c->h_counts) cudaFreeHost(c->h_counts);
   if (c->h_fetch) cudaFreeHost(c->h_fetch);
   if (c->h_victims) cudaFreeHost(c->h_victims);
+  cpu_exec_destroy(c->cpu);
+  c->cpu = nullptr;
   if (c->ev_fork) cudaEventDestroy(c->ev_fork);
   if (c->ev_join) cudaEventDestroy(c->ev_join);
   if (c->xfer) cudaStreamDestroy(c->xfer);
@@ -223,6 +226,7 @@ int enqueue_control(ft_ctx* c, int layer, const float* logits, const int32_t* id
   a.ratio = c->ratio;
   a.fill_order = c->cfg.fill_order;
   a.ids = ids;
+  lb.ids_src = ids;
   a.slot_of = c->slot_of;
   a.expert_of = c->expert_of;
   a.last_use = c->last_use;
@@ -377,6 +381,7 @@ int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx
     int32_t* p = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(c->layer_mem) + per_layer * l);
     LayerBufs& lb = c->layers[l];
     lb.ids = p; p += TK;
+    lb.ids_src = lb.ids;
     lb.w = reinterpret_cast<float*>(p); p += TK;
     lb.slot_ids = p; p += TK;
     lb.group_routes = p; p += TK;
@@ -434,6 +439,21 @@ int ft_moe_destroy(ft_ctx* c) {
   free_all(c);
   delete c;
   return FT_OK;
+}
+
+int ft_cpu_executor(ft_ctx* c, int threads) {
+  if (!c) return fail(FT_E_ARG, "null context");
+  if (threads < 0 || threads > 1024) return fail(FT_E_ARG, "threads must be in [0, 1024]");
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(c->xfer, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return fail(FT_E_STATE, "the CPU executor cannot change during a stream capture");
+  CU(cudaDeviceSynchronize());
+  cpu_exec_destroy(c->cpu);
+  c->cpu = nullptr;
+  if (threads == 0) return FT_OK;
+  return cpu_exec_create(&c->cpu, threads, static_cast<const uint8_t*>(c->host_pool), c->cfg.num_layers,
+                         c->cfg.num_experts, c->cfg.top_k, c->cfg.hidden, c->cfg.inter, c->cfg.dtype, c->Bx,
+                         c->cfg.t_max);
 }
 
 int ft_set_ratio(ft_ctx* c, int32_t r_num, int32_t r_den, void* stream) {
@@ -563,8 +583,13 @@ int ft_moe_forward(ft_ctx* c, int layer, int mode, const float* logits, const ui
   if (mode != FT_DECODE_CACHED) return fail(FT_E_ARG, "unknown mode %d", mode);
   LayerBufs& lb = c->layers[layer];
   if (lb.last_T != T) return fail(FT_E_STATE, "decode forward of layer %d with T=%d needs a cache step with the same T", layer, T);
-  // The fill runs on the transfer stream; experts already resident run
-  // meanwhile on the caller's stream, those the step installs after the fill.
+  // The CPU routes (if the executor is on) run on its stream and the fill on
+  // the transfer stream; experts already resident run meanwhile on the
+  // caller's stream, those the step installs after the fill.
+  if (c->cpu) {
+    if (partial) return fail(FT_E_ARG, "partial_dev must be NULL while the CPU executor is enabled");
+    CU(cpu_exec_fork(c->cpu, layer, T, lb.slot_ids, lb.ids_src, lb.w, hidden, st, c->prof));
+  }
   if ((rc = enqueue_fill(c, layer, st))) return rc;
   DecodeArgs a{};
   a.arena = c->arena;
@@ -597,6 +622,10 @@ int ft_moe_forward(ft_ctx* c, int layer, int mode, const float* logits, const ui
       return fail(FT_E_UNSUPPORTED, "decode experts need d <= 8192 (bf16) or d a multiple of 512 (MXFP4)");
     CU(e);
     c->prof.end(st, FT_K_EXPERTS, pb);
+  }
+  if (c->cpu) {
+    CU(cpu_exec_join(c->cpu, st));
+    partial = cpu_exec_partial(c->cpu);
   }
   pb = c->prof.begin(st);
   CU(launch_merge(c->ypart, c->n_chunks, lb.slot_ids, lb.w, partial, out, T, c->cfg.top_k, c->cfg.hidden, st));

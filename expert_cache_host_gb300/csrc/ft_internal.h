@@ -43,6 +43,7 @@ struct LayerBufs {
   int32_t* group_new;  // 1 if the group's expert is installed by this step's fill
   int32_t* group_off;
   int32_t* group_routes;
+  const int32_t* ids_src;  // routes of the last step: ids, or the caller's array (ft_cache_control)
   int last_T;  // T of the last step (host-side record, -1 = none)
 };
 
@@ -191,5 +192,17 @@ struct Profiler {
     pool.clear();
   }
 };
+
+// CPU expert executor (cpu_experts.cu): the routes of a decode step that got
+// no slot run on the host from the pool; their partial sum reaches the device
+// in stream order (fork after the control kernel, join before the merge).
+struct CpuExec;
+int cpu_exec_create(CpuExec** out, int threads, const uint8_t* pool_host, int L, int E, int k, int d, int f,
+                    int dtype, size_t Bx, int t_max);
+void cpu_exec_destroy(CpuExec* ex);
+cudaError_t cpu_exec_fork(CpuExec* ex, int layer, int T, const int32_t* slot_ids, const int32_t* ids, const float* w,
+                          const uint16_t* hidden, cudaStream_t st, Profiler& prof);
+cudaError_t cpu_exec_join(CpuExec* ex, cudaStream_t st);
+const float* cpu_exec_partial(const CpuExec* ex);
 
 }  // namespace ft

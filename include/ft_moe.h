@@ -263,7 +263,8 @@ int ft_route(const float* logits_dev, int T, int E, int k, int32_t* ids_dev, flo
 #define FT_K_UPLOAD 5  /* prefill full-layer upload, transfer stream */
 #define FT_K_PREFILL 6 /* prefill routing, dispatch, gather and combine */
 #define FT_K_GEMM 7    /* prefill grouped GEMMs (gate/up + down) */
-#define FT_K_COUNT 8
+#define FT_K_CPU 8     /* CPU expert executor: route copies, host function, partial copy (its own stream) */
+#define FT_K_COUNT 9
 
 /* Per-kernel timing for measurement.  While on, every kernel or copy the
  * context enqueues outside a stream capture is bracketed by CUDA events
@@ -302,6 +303,39 @@ int ft_profile_read(ft_ctx* ctx, double* total_ms, uint64_t* launches, int reset
 int ft_decode_experts_noalloc(const void* arena_dev, int num_slots, int hidden, int inter, int top_k, int T,
                               const int32_t* slot_ids_dev, const float* weights_dev, const uint16_t* hidden_dev,
                               const float* partial_dev, float* out_dev, uint32_t* status_dev, void* stream);
+
+/* CPU expert executor: the host side of the decode split (FreeToken article,
+ * section "设计 1", Decode bullet: the m - q* misses that are not filled run
+ * on the CPU from the host pool, and their partial sum is merged exactly with
+ * the GPU's).  threads >= 1 enables it with that many host threads (the
+ * calling CUDA callback thread counts as one); threads == 0 disables it (the
+ * default).  While enabled, ft_moe_forward(FT_DECODE_CACHED) computes
+ *   partial[t] = sum over the routes of token t with slot id < 0 of
+ *                w[t,j] * SwiGLU expert ids[t,j] (host pool bytes) of hidden[t]
+ * in fp32 on the host and merges it in place of partial_dev, which must then
+ * be NULL (FT_E_ARG otherwise).  Stream order: after the step's control kernel
+ * the route ids, weights, slot ids and hidden rows are copied to pinned host
+ * memory, a host function (cudaLaunchHostFunc, capturable in a CUDA graph)
+ * computes the sum, and it is copied to a device buffer the merge reads; this
+ * runs on a stream of the context beside the fill and the GPU experts.  One
+ * set of staging buffers serves all layers, so the decode calls of a context
+ * go to one stream (as for the rest of the step).  For ft_cache_control steps
+ * the weights are those the caller wrote to out->weights.  Not during a
+ * stream capture; synchronises the device.  Errors: FT_E_ARG, FT_E_STATE,
+ * FT_E_NOMEM. */
+int ft_cpu_executor(ft_ctx* ctx, int threads);
+
+/* The executor's arithmetic on host arrays, without a context or a GPU:
+ * pool_host holds the experts in the canonical layout (expert (layer, e) at
+ * (layer*num_experts + e) * B_x); ids, weights, slot_ids are [T, top_k];
+ * hidden_rows [T, hidden] bf16; partial [T, hidden] float32 is written with
+ * the sum over the routes with slot_ids < 0 (ids outside [0, num_experts)
+ * are skipped).  hidden and inter: positive multiples of 32.  Runs on the
+ * calling thread plus threads - 1 helpers; returns when done.  The result does
+ * not depend on threads.  Errors: FT_E_ARG. */
+int ft_cpu_experts(const void* pool_host, int num_experts, int top_k, int hidden, int inter, int dtype, int layer,
+                   int T, const int32_t* ids, const float* weights, const int32_t* slot_ids,
+                   const uint16_t* hidden_rows, float* partial, int threads);
 
 /* Message of the calling thread's last error ("" if none). */
 const char* ft_last_error(void);

@@ -90,16 +90,20 @@ def test_cache_step_routes_and_nan(ft, T, E, k):
 # ------------------------------------------------------------------ decode steps
 
 def run_decode(ft, model, S, K_max, r, steps, T=1, fill_mode=0, check_every=1, out_tokens=None, rho=0.9,
-               rebuild_at=None, graph=False, r_at=None, fill_order=0):
+               rebuild_at=None, graph=False, r_at=None, fill_order=0, cpu_exec=0):
     """Decode `steps` steps over all layers through the library and the oracle
     side by side; compare control state every step and outputs every
     `check_every` steps.  r_at: {step: (r_num, r_den)} changes r (ft_set_ratio)
-    before that step."""
+    before that step.  cpu_exec > 0: the context's CPU expert executor (that
+    many threads) computes the CPU routes' partial sum; no partial is passed."""
     L, E, k, d, f = model.L, model.E, model.k, model.d, model.f
     cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, dtype=model.dtype, num_slots=S,
                          k_max=K_max, t_max=T, r_num=r[0], r_den=r[1], fill_mode=fill_mode, fill_order=fill_order)
     ctx = ft.ft_moe_init(cfg, model.pool.ctypes.data, model.pool.nbytes)
     try:
+        if cpu_exec:
+            ft.ft_cpu_executor(ctx, cpu_exec)
+            check_every = 1
         cache = oracle.Cache(L * E, S)
         hid = np.stack([np.stack([ftsynth.ar1_hidden(model.seed, l, b, steps, d, rho) for b in range(T)], axis=1)
                         for l in range(L)], axis=1)  # [steps, L, T, d]
@@ -141,8 +145,8 @@ def run_decode(ft, model, S, K_max, r, steps, T=1, fill_mode=0, check_every=1, o
                     partial.copy_(torch.from_numpy(cpu_part.astype(np.float32)))
                 else:
                     partial.zero_()
-                ft.ft_moe_forward(ctx, l, ft.FT_DECODE_CACHED, 0, d_hid[s, l].data_ptr(), T, partial.data_ptr(),
-                                  out.data_ptr(), stream)
+                ft.ft_moe_forward(ctx, l, ft.FT_DECODE_CACHED, 0, d_hid[s, l].data_ptr(), T,
+                                  0 if cpu_exec else partial.data_ptr(), out.data_ptr(), stream)
                 torch.cuda.synchronize()
                 if check:
                     y = out.cpu().numpy().astype(np.float64)
@@ -426,6 +430,126 @@ def test_graph_replay_matches_oracle(ft):
                     compare_step(g, refs[l][1], f"step {s} layer {l}")
                     check_output(out[l].cpu().numpy().astype(np.float64), fulls[l], f"step {s} layer {l}")
                 compare_table(ft, ctx, cache, f"after step {s}")
+        assert ft.ft_get_status(ctx) == 0
+    finally:
+        ft.ft_moe_destroy(ctx)
+
+
+# ------------------------------------------------------------------ CPU expert executor
+
+@pytest.mark.parametrize("dtype,d,f,r,K_max", [(0, 256, 128, (1, 2), 16), (0, 256, 128, (0, 1), 4),
+                                               (1, 512, 128, (1, 2), 16)])
+def test_cpu_executor_decode_split(ft, dtype, d, f, r, K_max):
+    """The misses left to the CPU run on the context's CPU expert executor
+    (host function in the stream order) instead of arriving as a partial sum:
+    outputs equal the oracle's full sum (GPU routes + CPU routes) every step,
+    control state bit-exact."""
+    model = make_model(2, 16, 2, d, f, dtype=dtype, seed=21)
+    ctx, _, worst = run_decode(ft, model, S=6, K_max=K_max, r=r, steps=12, cpu_exec=3)
+    try:
+        cnt = ft.ft_get_counters(ctx, 2)
+        assert cnt[:, 3].sum() > 0  # some routes did go to the CPU
+        prof = ft.ft_profile_read(ctx, reset=True)
+        assert set(prof) >= {"cpu"}
+    finally:
+        ft.ft_moe_destroy(ctx)
+
+
+def test_cpu_executor_batch_and_profile(ft):
+    """Four tokens per step (several CPU routes per token), the executor's
+    stream profiled under ft_profile_enable."""
+    model = make_model(2, 16, 3, 256, 128, seed=22)
+    ctx, _, _ = run_decode(ft, model, S=8, K_max=8, r=(1, 3), steps=6, T=4, cpu_exec=2)
+    try:
+        ft.ft_profile_enable(ctx, 1)
+        hid = torch.zeros((4, 256), dtype=torch.int16, device="cuda")
+        lg = torch.zeros((4, 16), dtype=torch.float32, device="cuda")
+        out = torch.empty((4, 256), dtype=torch.float32, device="cuda")
+        ft.ft_cache_step(ctx, 0, lg.data_ptr(), 4)
+        ft.ft_moe_forward(ctx, 0, ft.FT_DECODE_CACHED, 0, hid.data_ptr(), 4, 0, out.data_ptr(), 0)
+        prof = ft.ft_profile_read(ctx, reset=True)
+        assert prof["cpu"][1] == 1 and prof["cpu"][0] > 0
+        assert np.isfinite(out.cpu().numpy()).all()
+    finally:
+        ft.ft_moe_destroy(ctx)
+
+
+def test_cpu_executor_rejects_partial_and_disables(ft):
+    model = make_model(1, 16, 2, 256, 128, seed=23)
+    cfg = ft.make_config(num_layers=1, num_experts=16, top_k=2, hidden=256, inter=128, num_slots=4, k_max=4, t_max=1,
+                         r_num=1, r_den=2)
+    ctx = ft.ft_moe_init(cfg, model.pool.ctypes.data, model.pool.nbytes)
+    try:
+        ft.ft_cpu_executor(ctx, 2)
+        hid = torch.zeros((1, 256), dtype=torch.int16, device="cuda")
+        lg = torch.zeros((1, 16), dtype=torch.float32, device="cuda")
+        part = torch.zeros((1, 256), dtype=torch.float32, device="cuda")
+        out = torch.empty((1, 256), dtype=torch.float32, device="cuda")
+        ft.ft_cache_step(ctx, 0, lg.data_ptr(), 1)
+        with pytest.raises(ft.FtError) as ei:
+            ft.ft_moe_forward(ctx, 0, ft.FT_DECODE_CACHED, 0, hid.data_ptr(), 1, part.data_ptr(), out.data_ptr(), 0)
+        assert ei.value.code == ft.FT_E_ARG
+        ft.ft_cpu_executor(ctx, 0)  # off again: the caller's partial is accepted
+        ft.ft_moe_forward(ctx, 0, ft.FT_DECODE_CACHED, 0, hid.data_ptr(), 1, part.data_ptr(), out.data_ptr(), 0)
+        torch.cuda.synchronize()
+        with pytest.raises(ft.FtError):
+            ft.ft_cpu_executor(ctx, -1)
+    finally:
+        ft.ft_moe_destroy(ctx)
+
+
+def test_cpu_executor_graph_replay(ft):
+    """A token of every layer captured once as a CUDA graph with the executor
+    on (copies and the host function become graph nodes) and replayed with new
+    inputs: outputs equal the oracle's full sum at every replay."""
+    L, E, k, d, f, T, S, K_max = 2, 16, 2, 256, 128, 1, 5, 16
+    model = make_model(L, E, k, d, f, seed=24)
+    steps, r = 8, (1, 2)
+    cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, num_slots=S, k_max=K_max, t_max=T,
+                         r_num=r[0], r_den=r[1])
+    ctx = ft.ft_moe_init(cfg, model.pool.ctypes.data, model.pool.nbytes)
+    try:
+        ft.ft_cpu_executor(ctx, 2)
+        cache = oracle.Cache(L * E, S)
+        hid = np.stack([ftsynth.ar1_hidden(model.seed, l, 0, steps, d)[:, None, :] for l in range(L)], axis=1)
+        logits = np.stack([ftsynth.router_logits(hid[:, l], model.wr[l]) for l in range(L)], axis=1)
+        cur_hid = torch.empty((L, T, d), dtype=torch.int16, device="cuda")
+        cur_lg = torch.empty((L, T, E), dtype=torch.float32, device="cuda")
+        out = torch.empty((L, T, d), dtype=torch.float32, device="cuda")
+        stream = torch.cuda.Stream()
+        cpu_routes = 0
+
+        def step(st):
+            for l in range(L):
+                ft.ft_cache_step(ctx, l, cur_lg[l].data_ptr(), T, st)
+                ft.ft_moe_forward(ctx, l, ft.FT_DECODE_CACHED, 0, cur_hid[l].data_ptr(), T, 0, out[l].data_ptr(), st)
+
+        graph = None
+        with torch.cuda.stream(stream):
+            for s in range(steps):
+                fulls = []
+                for l in range(L):
+                    ids, w = oracle.route(logits[s, l], k)
+                    ref = cache.step(l, E, ids, r[0], r[1], K_max)
+                    cpu_routes += int((ref.slot_ids < 0).sum())
+                    full, _, _ = oracle.moe_forward(model.layer_pool(l), model.bx, 0, d, f, ids, w, hid[s, l],
+                                                    slot_ids=ref.slot_ids.reshape(T, k))
+                    fulls.append(full)
+                cur_hid.copy_(torch.from_numpy(hid[s].view(np.int16)))
+                cur_lg.copy_(torch.from_numpy(logits[s]))
+                if s == 0:
+                    step(stream.cuda_stream)
+                else:
+                    if graph is None:
+                        graph = torch.cuda.CUDAGraph()
+                        with torch.cuda.graph(graph, stream=stream):
+                            step(torch.cuda.current_stream().cuda_stream)
+                    graph.replay()
+                stream.synchronize()
+                for l in range(L):
+                    check_output(out[l].cpu().numpy().astype(np.float64), fulls[l], f"step {s} layer {l}")
+                compare_table(ft, ctx, cache, f"after step {s}")
+        assert cpu_routes > 0
         assert ft.ft_get_status(ctx) == 0
     finally:
         ft.ft_moe_destroy(ctx)
