@@ -14,14 +14,16 @@
 // threads, then the output rows; each output element sums its routes in route
 // order, so the result does not depend on how the rows were divided.
 //
-// In a context the executor runs inside the stream order: a copy of the step's
-// route arrays and hidden rows to pinned host memory, a host function
-// (capturable in a CUDA graph), and a copy of the partial sum back, on a stream
-// of its own that runs beside the fill and the GPU experts; the merge waits
-// for it.
+// In a context the executor runs inside the stream order: copies of the step's
+// route arrays and hidden rows to pinned host memory and a host function
+// (capturable in a CUDA graph) that writes the partial sum into mapped pinned
+// memory, on a stream of its own that runs beside the fill and the GPU experts;
+// the merge waits for it and reads the sum there.
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+#include <chrono>
 #include <condition_variable>
 #include <functional>
 #include <mutex>
@@ -79,7 +81,9 @@ inline float silu(float g) { return g / (1.f + expf(-g)); }
 // ------------------------------------------------------------ worker pool
 
 // A fixed set of threads that run one function over [0, n) in contiguous
-// ranges; the calling thread takes the first range.
+// ranges; the calling thread takes the first range.  Between tasks a worker
+// polls for the next one for a short while (decode layers follow each other
+// within a fraction of a millisecond) and then sleeps on a condition variable.
 class WorkerPool {
  public:
   explicit WorkerPool(int threads) : n_(threads < 1 ? 1 : threads) {
@@ -88,7 +92,7 @@ class WorkerPool {
   ~WorkerPool() {
     {
       std::lock_guard<std::mutex> l(mu_);
-      stop_ = true;
+      stop_.store(true);
     }
     cv_.notify_all();
     for (auto& t : th_) t.join();
@@ -107,51 +111,53 @@ class WorkerPool {
       fn(0, n);
       return;
     }
+    task_ = [&fn, &range, parts](int i) {
+      if (i >= parts) return;
+      int b, e;
+      range(i, &b, &e);
+      fn(b, e);
+    };
+    pending_.store(n_ - 1);
     {
-      std::lock_guard<std::mutex> l(mu_);
-      task_ = [&fn, &range, parts](int i) {
-        if (i >= parts) return;
-        int b, e;
-        range(i, &b, &e);
-        fn(b, e);
-      };
-      pending_ = n_ - 1;
-      ++gen_;
+      std::lock_guard<std::mutex> l(mu_);  // a worker about to sleep sees the new generation
+      gen_.fetch_add(1, std::memory_order_release);
     }
     cv_.notify_all();
     int b, e;
     range(0, &b, &e);
     fn(b, e);
-    std::unique_lock<std::mutex> l(mu_);
-    done_.wait(l, [this] { return pending_ == 0; });
+    while (pending_.load(std::memory_order_acquire) != 0) {
+    }
   }
 
  private:
   void loop(int i) {
     long long seen = 0;
     for (;;) {
-      std::function<void(int)> f;
-      {
-        std::unique_lock<std::mutex> l(mu_);
-        cv_.wait(l, [&] { return stop_ || gen_ != seen; });
-        if (stop_) return;
-        seen = gen_;
-        f = task_;
+      const auto t0 = std::chrono::steady_clock::now();
+      for (int spin = 0; gen_.load(std::memory_order_acquire) == seen && !stop_.load(); ++spin) {
+        if ((spin & 255) == 255 && std::chrono::steady_clock::now() - t0 > std::chrono::microseconds(kSpinUs)) {
+          std::unique_lock<std::mutex> l(mu_);
+          cv_.wait(l, [&] { return stop_.load() || gen_.load() != seen; });
+          break;
+        }
       }
-      f(i);
-      std::lock_guard<std::mutex> l(mu_);
-      if (--pending_ == 0) done_.notify_one();
+      if (stop_.load()) return;
+      seen = gen_.load(std::memory_order_acquire);
+      task_(i);
+      pending_.fetch_sub(1, std::memory_order_release);
     }
   }
 
+  static constexpr int kSpinUs = 300;
   int n_;
   std::vector<std::thread> th_;
   std::mutex mu_;
-  std::condition_variable cv_, done_;
+  std::condition_variable cv_;
   std::function<void(int)> task_;
-  long long gen_ = 0;
-  int pending_ = 0;
-  bool stop_ = false;
+  std::atomic<long long> gen_{0};
+  std::atomic<int> pending_{0};
+  std::atomic<bool> stop_{false};
 };
 
 }  // namespace
@@ -259,13 +265,16 @@ struct CpuExec {
   CpuScratch s;
   cudaStream_t st = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
-  // pinned staging of one step: routes, weights, slot ids, hidden rows, result
-  int32_t* h_slot = nullptr;
+  // pinned staging of one step: route ids | weights | slot ids (each t_max*k
+  // entries, the layout of a layer's step buffers, so one copy can bring all
+  // three), the hidden rows, and the result (mapped: the merge reads it there)
+  int32_t* h_routes = nullptr;
   int32_t* h_ids = nullptr;
   float* h_w = nullptr;
+  int32_t* h_slot = nullptr;
   uint16_t* h_hidden = nullptr;
   float* h_partial = nullptr;
-  float* d_partial = nullptr;  // device copy of the result, read by the merge
+  float* d_partial = nullptr;  // device view of h_partial
   std::vector<CpuJob> jobs;    // [L][t_max]: the host function's argument per (layer, T)
 };
 
@@ -282,12 +291,9 @@ void CUDART_CB cpu_job_fn(void* p) {
 void cpu_exec_destroy(CpuExec* ex) {
   if (!ex) return;
   if (ex->st) cudaStreamSynchronize(ex->st);
-  if (ex->h_slot) cudaFreeHost(ex->h_slot);
-  if (ex->h_ids) cudaFreeHost(ex->h_ids);
-  if (ex->h_w) cudaFreeHost(ex->h_w);
+  if (ex->h_routes) cudaFreeHost(ex->h_routes);
   if (ex->h_hidden) cudaFreeHost(ex->h_hidden);
   if (ex->h_partial) cudaFreeHost(ex->h_partial);
-  if (ex->d_partial) cudaFree(ex->d_partial);
   if (ex->ev_fork) cudaEventDestroy(ex->ev_fork);
   if (ex->ev_join) cudaEventDestroy(ex->ev_join);
   if (ex->st) cudaStreamDestroy(ex->st);
@@ -305,17 +311,19 @@ int cpu_exec_create(CpuExec** out, int threads, const uint8_t* pool_host, int L,
   bool ok = cudaStreamCreateWithFlags(&ex->st, cudaStreamNonBlocking) == cudaSuccess &&
             cudaEventCreateWithFlags(&ex->ev_fork, cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&ex->ev_join, cudaEventDisableTiming) == cudaSuccess &&
-            cudaHostAlloc(reinterpret_cast<void**>(&ex->h_slot), sizeof(int32_t) * R, 0) == cudaSuccess &&
-            cudaHostAlloc(reinterpret_cast<void**>(&ex->h_ids), sizeof(int32_t) * R, 0) == cudaSuccess &&
-            cudaHostAlloc(reinterpret_cast<void**>(&ex->h_w), sizeof(float) * R, 0) == cudaSuccess &&
+            cudaHostAlloc(reinterpret_cast<void**>(&ex->h_routes), sizeof(int32_t) * 3 * R, 0) == cudaSuccess &&
             cudaHostAlloc(reinterpret_cast<void**>(&ex->h_hidden), sizeof(uint16_t) * TD, 0) == cudaSuccess &&
-            cudaHostAlloc(reinterpret_cast<void**>(&ex->h_partial), sizeof(float) * TD, 0) == cudaSuccess &&
-            cudaMalloc(reinterpret_cast<void**>(&ex->d_partial), sizeof(float) * TD) == cudaSuccess;
+            cudaHostAlloc(reinterpret_cast<void**>(&ex->h_partial), sizeof(float) * TD, cudaHostAllocMapped) ==
+                cudaSuccess &&
+            cudaHostGetDevicePointer(reinterpret_cast<void**>(&ex->d_partial), ex->h_partial, 0) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     cpu_exec_destroy(ex);
     return record_error(FT_E_NOMEM, "CPU executor: stream, events or staging buffers could not be allocated");
   }
+  ex->h_ids = ex->h_routes;
+  ex->h_w = reinterpret_cast<float*>(ex->h_routes + R);
+  ex->h_slot = ex->h_routes + 2 * R;
   ex->jobs.resize((size_t)L * t_max);
   for (int l = 0; l < L; ++l)
     for (int t = 1; t <= t_max; ++t) ex->jobs[(size_t)l * t_max + (t - 1)] = CpuJob{ex, l, t};
@@ -325,20 +333,24 @@ int cpu_exec_create(CpuExec** out, int threads, const uint8_t* pool_host, int L,
 
 cudaError_t cpu_exec_fork(CpuExec* ex, int layer, int T, const int32_t* slot_ids, const int32_t* ids, const float* w,
                           const uint16_t* hidden, cudaStream_t st, Profiler& prof) {
-  const size_t R = (size_t)T * ex->m.k, TD = (size_t)T * ex->m.d;
+  const size_t R = (size_t)T * ex->m.k, TD = (size_t)T * ex->m.d, RC = (size_t)ex->t_max * ex->m.k;
   cudaError_t e;
   if ((e = cudaEventRecord(ex->ev_fork, st)) != cudaSuccess) return e;
   if ((e = cudaStreamWaitEvent(ex->st, ex->ev_fork, 0)) != cudaSuccess) return e;
   cudaEvent_t pb = prof.begin(ex->st);
-  if ((e = cudaMemcpyAsync(ex->h_slot, slot_ids, sizeof(int32_t) * R, cudaMemcpyDeviceToHost, ex->st)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(ex->h_ids, ids, sizeof(int32_t) * R, cudaMemcpyDeviceToHost, ex->st)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(ex->h_w, w, sizeof(float) * R, cudaMemcpyDeviceToHost, ex->st)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(ex->h_hidden, hidden, sizeof(uint16_t) * TD, cudaMemcpyDeviceToHost, ex->st)) != cudaSuccess)
+  const bool one_block = reinterpret_cast<const void*>(w) == ids + RC && slot_ids == ids + 2 * RC;
+  if (one_block) {
+    // ids | w | slot_ids adjacent on the device, as in the staging block
+    e = cudaMemcpyAsync(ex->h_routes, ids, sizeof(int32_t) * (2 * RC + R), cudaMemcpyDeviceToHost, ex->st);
+  } else if ((e = cudaMemcpyAsync(ex->h_ids, ids, sizeof(int32_t) * R, cudaMemcpyDeviceToHost, ex->st)) == cudaSuccess &&
+             (e = cudaMemcpyAsync(ex->h_w, w, sizeof(float) * R, cudaMemcpyDeviceToHost, ex->st)) == cudaSuccess) {
+    e = cudaMemcpyAsync(ex->h_slot, slot_ids, sizeof(int32_t) * R, cudaMemcpyDeviceToHost, ex->st);
+  }
+  if (e != cudaSuccess) return e;
+  if ((e = cudaMemcpyAsync(ex->h_hidden, hidden, sizeof(uint16_t) * TD, cudaMemcpyDeviceToHost, ex->st)) != cudaSuccess)
     return e;
+  // the result lands in mapped host memory, which the merge reads directly
   if ((e = cudaLaunchHostFunc(ex->st, cpu_job_fn, &ex->jobs[(size_t)layer * ex->t_max + (T - 1)])) != cudaSuccess)
-    return e;
-  if ((e = cudaMemcpyAsync(ex->d_partial, ex->h_partial, sizeof(float) * TD, cudaMemcpyHostToDevice, ex->st)) !=
-      cudaSuccess)
     return e;
   prof.end(ex->st, FT_K_CPU, pb);
   return cudaEventRecord(ex->ev_join, ex->st);

@@ -315,8 +315,8 @@ int ft_decode_experts_noalloc(const void* arena_dev, int num_slots, int hidden, 
  * in fp32 on the host and merges it in place of partial_dev, which must then
  * be NULL (FT_E_ARG otherwise).  Stream order: after the step's control kernel
  * the route ids, weights, slot ids and hidden rows are copied to pinned host
- * memory, a host function (cudaLaunchHostFunc, capturable in a CUDA graph)
- * computes the sum, and it is copied to a device buffer the merge reads; this
+ * memory and a host function (cudaLaunchHostFunc, capturable in a CUDA graph)
+ * computes the sum into mapped pinned memory, which the merge reads; this
  * runs on a stream of the context beside the fill and the GPU experts.  One
  * set of staging buffers serves all layers, so the decode calls of a context
  * go to one stream (as for the rest of the step).  For ft_cache_control steps
