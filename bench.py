@@ -171,6 +171,42 @@ def link_peak_gbs(pool, nbytes):
     return nbytes / best / 1e9
 
 
+def experts_alone(w, pool, hid, reps=40):
+    """The bf16 decode expert kernel with its merge, outside the step: the
+    first k experts of layer 0 resident in a scratch arena, one token, L2
+    flushed (256 MB written) before every call, CUDA events around the call
+    (route grouping + experts + merge of the allocation-free entry).  Returns
+    {experts: median seconds} for k and for 2 experts."""
+    import torch
+
+    import expert_cache_host_gb300 as ft
+    d, f, k = w["d"], w["f"], w["k"]
+    bx = ftsynth.expert_bytes(d, f, 0)
+    arena = torch.from_numpy(pool[:k * bx]).cuda()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    x = torch.from_numpy(hid[0, 0, :1].view(np.int16)).cuda()
+    out = torch.empty((1, d), dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream()
+    res = {}
+    for n in (k, 2):
+        sid = torch.arange(n, dtype=torch.int32, device="cuda")
+        wt = torch.full((n,), 1.0 / n, dtype=torch.float32, device="cuda")
+        ts = []
+        for r in range(reps + 3):
+            flush.add_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            ft.ft_decode_experts_noalloc(arena.data_ptr(), k, d, f, n, 1, sid.data_ptr(), wt.data_ptr(), x.data_ptr(),
+                                         0, out.data_ptr(), 0, st.cuda_stream)
+            e1.record(st)
+            e1.synchronize()
+            if r >= 3:
+                ts.append(e0.elapsed_time(e1) / 1e3)
+        res[n] = statistics.median(ts)
+    del arena, flush
+    return res
+
+
 # ----------------------------------------------------------------------------- decode (headline)
 
 def run_decode_leg(args, w, world, local, pool, hid, lg):
@@ -677,7 +713,7 @@ def main():
     hid, lg = decode_inputs(w, args.warmup + args.steps + min(args.steps, args.profile_steps)
                             + min(args.steps, args.e2e_steps))
     dec = run_decode_leg(args, w, world, local, pool, hid, lg)
-    pre = ctl = None
+    pre = ctl = alone = None
     link = 0.0
     if rank == 0:
         import expert_cache_host_gb300 as ft
@@ -689,6 +725,8 @@ def main():
             link = link_peak_gbs(pool, w["E"] * ftsynth.expert_bytes(w["d"], w["f"], w["dtype"]))
         finally:
             ft.ft_moe_destroy(ctx)
+        if w["dtype"] == 0:
+            alone = experts_alone(w, pool, hid)
         if not args.no_prefill and not args.layers:
             pre = run_prefill_leg(args, w, pool)
         if not args.no_control and not args.layers:
@@ -696,6 +734,15 @@ def main():
     peaks = measured_peaks()
     if rank == 0:
         line = build_line(args, w, world, dec, link, pre, ctl, peaks)
+        if alone:
+            bx = ftsynth.expert_bytes(w["d"], w["f"], 0)
+            t8 = alone[w["k"]]
+            line["roofline_experts_alone"] = {
+                "bound": "hbm", "kernel": f"decode experts + merge outside the step ({w['k']} resident experts, "
+                                          "batch 1, L2 flushed; allocation-free entry: route grouping, experts, merge)",
+                "achieved": round(w["k"] * bx / t8 / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(w["k"] * bx / t8 / 1e9 / peaks["hbm_gbs"], 4), "us": round(t8 * 1e6, 2),
+                "us_2_experts": round(alone[2] * 1e6, 2), "peak_source": peaks["source"]}
         if not args.no_cpu_baseline:
             rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, args.cpu_budget_s,
                                                      min_tokens=1.0 if w["T"] == 1 else 1.0 / w["L"])
