@@ -553,3 +553,43 @@ def test_cpu_executor_graph_replay(ft):
         assert ft.ft_get_status(ctx) == 0
     finally:
         ft.ft_moe_destroy(ctx)
+
+
+def test_cpu_executor_with_caller_routes(ft):
+    """ft_cache_control steps (routes from the caller, read in place; weights
+    written by the caller into out->weights) with the executor on: the route
+    arrays are not adjacent, so they reach the host by separate copies; the
+    outputs equal the oracle's full sum."""
+    L, E, k, d, f, T, S, K_max, steps, r = 2, 16, 2, 256, 128, 3, 6, 16, 8, (1, 2)
+    model = make_model(L, E, k, d, f, seed=25)
+    cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, num_slots=S, k_max=K_max, t_max=T,
+                         r_num=r[0], r_den=r[1])
+    ctx = ft.ft_moe_init(cfg, model.pool.ctypes.data, model.pool.nbytes)
+    try:
+        ft.ft_cpu_executor(ctx, 3)
+        cache = oracle.Cache(L * E, S)
+        hid = np.stack([np.stack([ftsynth.ar1_hidden(model.seed, l, b, steps, d) for b in range(T)], axis=1)
+                        for l in range(L)], axis=1)  # [steps, L, T, d]
+        logits = np.stack([ftsynth.router_logits(hid[:, l], model.wr[l]) for l in range(L)], axis=1)
+        d_hid = torch.from_numpy(hid.view(np.int16)).cuda()
+        ids_dev = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        out = torch.empty((T, d), dtype=torch.float32, device="cuda")
+        cpu_routes = 0
+        for s in range(steps):
+            for l in range(L):
+                ids, w = oracle.route(logits[s, l], k)
+                ids_dev.copy_(torch.from_numpy(ids))
+                res = ft.ft_cache_control(ctx, l, ids_dev.data_ptr(), T)
+                dev_view(res.weights, (T * k,), "<f4").copy_(torch.from_numpy(w.astype(np.float32).reshape(-1)))
+                ref = cache.step(l, E, ids, r[0], r[1], K_max)
+                cpu_routes += int((ref.slot_ids < 0).sum())
+                full, _, _ = oracle.moe_forward(model.layer_pool(l), model.bx, 0, d, f, ids,
+                                                w.astype(np.float32).astype(np.float64), hid[s, l],
+                                                slot_ids=ref.slot_ids.reshape(T, k))
+                ft.ft_moe_forward(ctx, l, ft.FT_DECODE_CACHED, 0, d_hid[s, l].data_ptr(), T, 0, out.data_ptr())
+                torch.cuda.synchronize()
+                check_output(out.cpu().numpy().astype(np.float64), full, f"step {s} layer {l}")
+        assert cpu_routes > 0
+        assert ft.ft_get_status(ctx) == 0
+    finally:
+        ft.ft_moe_destroy(ctx)
