@@ -543,7 +543,8 @@ def make_host_pool(args, w):
 
 
 def metric_name(args, w):
-    m = METRIC if w["dtype"] == 0 else METRIC.replace("A3B-style, batch 1", f"V4-Flash-style MXFP4, batch {w['T']}")
+    m = METRIC.replace("batch 1", f"batch {w['T']}") if w["dtype"] == 0 else \
+        METRIC.replace("A3B-style, batch 1", f"V4-Flash-style MXFP4, batch {w['T']}")
     if args.cpu_exec:
         m = m.replace("GPU side; CPU-routed experts arrive as a partial sum", "GPU + CPU expert executor")
     return m
