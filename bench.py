@@ -509,7 +509,7 @@ def run_sweep(args, w, world, local):
                     "sweep": "capacity", "workload": w["desc"].split(":")[0], "slots": ws["S"],
                     "capacity_pct": pct, "tok_s": round(dec["value"], 3),
                     "expert_miss_rate": round(dec["misses"] / max(1.0, routes), 4),
-                    "fills_per_token": round(dec["fills"] / dec["K"], 3),
+                    "fills_per_token": round(dec["fills"] / (dec["K"] * dec["T"]), 3),
                     "timed_tokens": dec["K"], "warmup_tokens": dec["W"], "device_status": dec["status"]}), flush=True)
         else:
             w = dict(w, dtype=0)
@@ -577,11 +577,14 @@ def build_line(args, w, world, dec, link_gbs, pre, ctl, peaks):
                              "avg_launch_us": round(dec["ex_ms"] / max(1, dec["ex_n"]) * 1e3, 2),
                              "share": dec["shares"].get("experts")},
         "components": {
-            "kernel_share": dec["shares"], "kernel_ms_per_token": dec["ms_per_token"],
+            "kernel_share": dec["shares"],
+            "kernel_ms_per_token": {n: round(v / dec["T"], 4) for n, v in dec["ms_per_token"].items()},
             "route_control_us_per_layer_step": round(dec["control_us"], 3),
             "hit_rate": round(dec["hits"] / max(1.0, dec["hits"] + dec["misses"]), 4),
-            "fills_per_token": round(dec["fills"] / dec["K"], 3), "cpu_routes_per_token": round(dec["cpu"] / dec["K"], 3),
-            "eager_ms_per_token_profiled": round(dec["eager_ms"], 4) if dec["eager_ms"] else None,
+            "fills_per_token": round(dec["fills"] / (dec["K"] * dec["T"]), 3),
+            "cpu_routes_per_token": round(dec["cpu"] / (dec["K"] * dec["T"]), 3),
+            "fills_per_step": round(dec["fills"] / dec["K"], 3), "tokens_per_step": dec["T"],
+            "eager_ms_per_token_profiled": round(dec["eager_ms"] / dec["T"], 4) if dec["eager_ms"] else None,
             "init_pin_s": round(dec["t_init"], 2), "device_status": dec["status"],
         },
         "clocks": dec["clocks"],
