@@ -22,6 +22,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <condition_variable>
@@ -206,25 +207,30 @@ void cpu_partial(const CpuModel& m, int layer, int T, const int32_t* ids, const 
   auto expert = [&](int e) { return m.pool + ((size_t)layer * m.E + e) * m.Bx; };
   const bool bf16 = m.dtype == FT_DTYPE_BF16;
 
-  // h[route][i] = silu(W_gate[i] . x) * (W_up[i] . x)
-  pool.parallel(nc * f, [&](int b, int end) {
-    for (int it = b; it < end; ++it) {
-      const int ri = it / f, i = it - ri * f;
-      const uint8_t* ex = expert(s.re[ri]);
-      const float* x = s.x.data() + (size_t)s.rt[ri] * d;
-      float g, u;
-      if (bf16) {
-        const uint16_t* wg = reinterpret_cast<const uint16_t*>(ex);
-        g = dot_bf16(wg + (size_t)i * d, x, d);
-        u = dot_bf16(wg + df + (size_t)i * d, x, d);
-      } else {
-        const uint8_t* sc = ex + 3 * df / 2;  // scales gate [f][d/32], then up
-        g = dot_mxfp4(ex + (size_t)i * (d / 2), sc + (size_t)i * (d / 32), x, d);
-        u = dot_mxfp4(ex + df / 2 + (size_t)i * (d / 2), sc + df / 32 + (size_t)i * (d / 32), x, d);
+  // h[route][i] = silu(W_gate[i] . x) * (W_up[i] . x), over blocks of routes
+  // small enough that the item count stays an int
+  const int rb = (int)std::max<long long>(1, (1LL << 30) / f);
+  for (int r0 = 0; r0 < nc; r0 += rb) {
+    const int nr = std::min(rb, nc - r0);
+    pool.parallel(nr * f, [&](int b, int end) {
+      for (int it = b; it < end; ++it) {
+        const int ri = r0 + it / f, i = it % f;
+        const uint8_t* ex = expert(s.re[ri]);
+        const float* x = s.x.data() + (size_t)s.rt[ri] * d;
+        float g, u;
+        if (bf16) {
+          const uint16_t* wg = reinterpret_cast<const uint16_t*>(ex);
+          g = dot_bf16(wg + (size_t)i * d, x, d);
+          u = dot_bf16(wg + df + (size_t)i * d, x, d);
+        } else {
+          const uint8_t* sc = ex + 3 * df / 2;  // scales gate [f][d/32], then up
+          g = dot_mxfp4(ex + (size_t)i * (d / 2), sc + (size_t)i * (d / 32), x, d);
+          u = dot_mxfp4(ex + df / 2 + (size_t)i * (d / 2), sc + df / 32 + (size_t)i * (d / 32), x, d);
+        }
+        s.h[(size_t)ri * f + i] = silu(g) * u;
       }
-      s.h[(size_t)ri * f + i] = silu(g) * u;
-    }
-  });
+    });
+  }
 
   // partial[t][row] = sum over the CPU routes of token t, in route order,
   // of w * (W_down[row] . h[route])
@@ -370,10 +376,10 @@ extern "C" int ft_cpu_experts(const void* pool_host, int num_experts, int top_k,
   using namespace ft;
   if (!pool_host || !ids || !weights || !slot_ids || !hidden_rows || !partial)
     return record_error(FT_E_ARG, "null pointer argument");
-  if (num_experts < 1 || top_k < 1 || top_k > num_experts || layer < 0 || T < 1)
-    return record_error(FT_E_ARG, "bad num_experts, top_k, layer or T");
-  if (hidden < 32 || hidden % 32 || inter < 32 || inter % 32)
-    return record_error(FT_E_ARG, "hidden and inter must be positive multiples of 32");
+  if (num_experts < 1 || top_k < 1 || top_k > num_experts || layer < 0 || T < 1 || (long long)T * top_k > (1 << 24))
+    return record_error(FT_E_ARG, "bad num_experts, top_k, layer or T (T * top_k <= 2^24)");
+  if (hidden < 32 || hidden % 32 || inter < 32 || inter % 32 || hidden > (1 << 20) || inter > (1 << 20))
+    return record_error(FT_E_ARG, "hidden and inter must be multiples of 32 in [32, 2^20]");
   if (dtype != FT_DTYPE_BF16 && dtype != FT_DTYPE_MXFP4) return record_error(FT_E_ARG, "dtype must be BF16 or MXFP4");
   if (threads < 1 || threads > 1024) return record_error(FT_E_ARG, "threads must be in [1, 1024]");
   const size_t df = (size_t)hidden * inter;
