@@ -124,3 +124,23 @@ def test_argument_errors(lib):
     with pytest.raises(ft.FtError) as ei:
         ft.ft_cpu_experts(pool, 1, 1, 256, 128, 0, 0, ids, w, ids, hid, threads=0)
     assert ei.value.code == ft.FT_E_ARG
+
+
+def test_mxfp4_nan_scale_propagates(lib):
+    """OCP MX v1.0: the e8m0 byte 255 is NaN; a route through a row group with
+    that scale yields NaN in the executor as in the oracle, and other tokens
+    stay finite."""
+    E, k, d, f, T = 4, 1, 256, 128, 2
+    bx = ftsynth.expert_bytes(d, f, 1)
+    pool = ftsynth.make_pool(3, 1, E, d, f, 1, 0.05, threads=2)
+    df = d * f
+    pool[2 * bx + 3 * df // 2] = 255  # expert 2: first gate scale byte (row 0, group 0)
+    ids = np.array([[2], [1]], np.int32)
+    w = np.ones((T, k), np.float32)
+    sid = np.full((T, k), -1, np.int32)
+    hid = ftsynth.normal_bf16(4, 6, 0, 0, T * d).reshape(T, d)
+    got = ft.ft_cpu_experts(pool, E, k, d, f, 1, 0, ids, w, sid, hid)
+    ref = _oracle_cpu(pool, 0, E, 1, d, f, ids, w, hid, sid)
+    assert np.isnan(got[0]).any() and np.isnan(ref[0]).any()
+    assert np.isfinite(got[1]).all()
+    assert oracle.max_rel_err(got[1:], ref[1:]) <= CPU_MAX_REL
