@@ -71,3 +71,10 @@ def test_host_alloc_arguments_checked_on_host(lib):
 
 def test_set_ratio_arguments_checked_on_host(lib):
     assert lib.ft_set_ratio(None, 1, 1, None) == ft.FT_E_ARG
+
+
+def test_cpu_executor_arguments_checked_on_host(lib):
+    assert lib.ft_cpu_executor(None, 4) == ft.FT_E_ARG
+    null = None
+    assert lib.ft_cpu_experts(null, 8, 2, 256, 128, 0, 0, 1, null, null, null, null, null, 1) == ft.FT_E_ARG
+    assert "null" in lib.ft_last_error().decode()
