@@ -335,6 +335,100 @@ def test_mxfp4_packing_and_layout():
     assert np.all(y0[1:] == 0) and np.all(y1[1:] == 0)
 
 
+def _mx_fixture_expert():
+    """The expert of tests/golden/mxfp4_scales.json packed in the canonical
+    MXFP4 layout (written here from the layout's definition, not by the oracle)."""
+    g = gold("mxfp4_scales.json")
+    d, f = g["d"], g["f"]
+    df = d * f
+    mats = ("gate", "up", "down")
+    codes = [np.zeros(df, dtype=np.uint8) for _ in mats]  # one code per element, row-major
+    for name, row, col, code, _ in g["codes"]["entries"]:
+        m = mats.index(name)
+        cols = f if name == "down" else d
+        codes[m][row * cols + col] = code
+    packed = [(c[0::2] | (c[1::2] << 4)).astype(np.uint8) for c in codes]  # element 2i in the low nibble
+    scales = []
+    for name in mats:
+        rows, cols = (d, f) if name == "down" else (f, d)
+        r, grp = np.meshgrid(np.arange(rows), np.arange(cols // 32), indexing="ij")
+        scales.append((g["scale_byte"]["offset"][name] + 2 * r + grp).astype(np.uint8).reshape(-1))
+    ex = np.concatenate(packed + scales)
+    assert ex.nbytes == ftsynth.expert_bytes(d, f, 1)
+    return g, ex
+
+
+def _mx_fixture_check(ffn):
+    """Max relative error of ffn(ex, x) over the fixture's cases (inf if a
+    zero element comes out nonzero)."""
+    g, ex = _mx_fixture_expert()
+    d, f = g["d"], g["f"]
+    sig = lambda z: 1.0 / (1.0 + math.exp(-z))
+    worst = 0.0
+    for c in g["cases"]:
+        x = np.zeros(d, dtype=np.float32)
+        x[c["x_ones"]] = 1.0
+        y = ffn(ex, d, f, _bf16(x))
+        want = np.zeros(d)
+        for idx, a, z in c["y"]:
+            want[idx] += a * sig(z)
+        nz = want != 0
+        if np.any(y[~nz] != 0):
+            return math.inf
+        worst = max(worst, float(np.max(np.abs(y[nz] - want[nz]) / np.abs(want[nz]))))
+    return worst
+
+
+def test_mxfp4_scale_addressing_golden():
+    """Several rows per matrix hold nonzero codes, in both 32-column groups of
+    a row, and every (row, group) has its own scale byte: the oracle must read
+    the scale of the element's own row and group, the nibble of its own
+    column, and W_down in [d, f] orientation."""
+    err = _mx_fixture_check(lambda ex, d, f, x: oracle.expert_ffn(ex, 1, d, f, x))
+    assert err < 1e-14, err
+
+
+# Slips an MXFP4 reader could plausibly make, each planted in a private copy of
+# the oracle's C source; the fixture above must reject every one of them.
+_MX_SLIPS = {
+    "scale from the column group alone": ("scales[idx / 32]", "scales[col / 32]"),
+    "scales stored column-major": ("scales[idx / 32]", "scales[(size_t)(col / 32) * cols + row]"),
+    "nibbles swapped": ("(idx & 1) ? (byte >> 4) : (byte & 15)", "(idx & 1) ? (byte & 15) : (byte >> 4)"),
+    "W_down read transposed": ("return mx_elem(codes, scales, cols, row, col);",
+                               "return which == 2 ? mx_elem(codes, scales, cols, col, row) "
+                               ": mx_elem(codes, scales, cols, row, col);"),
+    "gate and up swapped": ("const uint8_t* codes = ex + (size_t)which * (df / 2);",
+                            "const uint8_t* codes = ex + (size_t)(which == 2 ? 2 : 1 - which) * (df / 2);"),
+}
+
+
+@pytest.mark.parametrize("slip", sorted(_MX_SLIPS))
+def test_mxfp4_fixture_rejects_planted_slip(slip, tmp_path):
+    import ctypes
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "ftoracle.c")).read()
+    old, new = _MX_SLIPS[slip]
+    assert src.count(old) == 1, f"the oracle no longer contains {old!r}"
+    (tmp_path / "m.c").write_text(src.replace(old, new))
+    so = tmp_path / "m.so"
+    subprocess.run(["gcc", "-O1", "-fPIC", "-shared", "-o", str(so), str(tmp_path / "m.c"), "-lm"], check=True,
+                   capture_output=True)
+    lib = ctypes.CDLL(str(so))
+    lib.or_expert_ffn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                  ctypes.c_void_p]
+    lib.or_expert_ffn.restype = ctypes.c_int
+
+    def ffn(ex, d, f, x):
+        y = np.zeros(d)
+        assert lib.or_expert_ffn(ex.ctypes.data, 1, d, f, x.ctypes.data, y.ctypes.data) == 0
+        return y
+
+    assert _mx_fixture_check(ffn) > 1e-3, f"the fixture did not catch: {slip}"
+
+
 def _tiny_pool(E, d, f, dtype, seed=5):
     return ftsynth.make_pool(seed, 1, E, d, f, dtype, 0.05, threads=2)
 
