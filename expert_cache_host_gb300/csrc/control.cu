@@ -319,7 +319,8 @@ __global__ void __launch_bounds__(NT, 1) control_kernel(ControlArgs a) {
     }
     __syncthreads();
     if (wid == 0) {
-      unsigned mn = sm.wmin[lane], mx = sm.wmax[lane];
+      // a launch of NW < 32 warps writes only the first NW entries
+      unsigned mn = lane < NW ? sm.wmin[lane] : 0xFFFFFFFFu, mx = lane < NW ? sm.wmax[lane] : 0u;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));

@@ -1,10 +1,11 @@
 // CPU expert executor: the host side of the decode split.
 //
 // FreeToken article, section "设计 1" (bandwidth-adaptive execution), Decode
-// bullet: of the m experts a step misses, q* are filled into the GPU cache and
-// the other m - q* run on the CPU, straight from the host pool; the CPU's
-// partial sum and the GPU's are then merged exactly.  This file is that CPU
-// side: for the routes of a step that got no slot (slot id < 0) it computes
+// bullet.  Of a step's m missed experts the control kernel fills q into slots;
+// the routes of the remaining misses are computed here on the host cores from
+// the pool bytes, and the merge kernel adds the GPU's routes to this sum, so
+// the layer output is unchanged by the split.  For the routes of a step that
+// got no slot (slot id < 0) this file computes
 //     partial[t] = sum_j w[t,j] * SwiGLU expert ids[t,j] applied to hidden[t]
 // on the host cores, in fp32, reading the expert bytes from the pool in the
 // canonical layout (bf16, or MXFP4 codes with e8m0 scales).

@@ -33,16 +33,21 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // One group per route that has a slot: group g = the g-th such route.
+// merge_sid receives the slot ids the merge acts on: a route whose slot id is
+// outside [0, S) is reported and becomes -1 there, so it adds nothing (its
+// partial-sum rows are not written by this call and may hold an earlier
+// call's values).
 __global__ void route_groups_kernel(const int32_t* __restrict__ slot_ids, int n_routes, int S,
                                     int32_t* __restrict__ counts, int32_t* __restrict__ group_slot,
                                     int32_t* __restrict__ group_off, int32_t* __restrict__ group_routes,
-                                    uint32_t* __restrict__ status) {
+                                    int32_t* __restrict__ merge_sid, uint32_t* __restrict__ status) {
   __shared__ int n;
   if (threadIdx.x == 0) n = 0;
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int r = 0; r < n_routes; ++r) {
       const int s = slot_ids[r];
+      merge_sid[r] = s < S ? s : -1;
       if (s < 0) continue;
       if (s >= S) {
         atomicOr(status, FT_ST_BAD_SLOT);
@@ -63,7 +68,7 @@ __global__ void route_groups_kernel(const int32_t* __restrict__ slot_ids, int n_
 
 size_t noalloc_scratch_needed(int T, int k, int d, int f) {
   const size_t R = (size_t)T * k;
-  const size_t small = 256 + 4 * (3 * R + 1) + 4 /*status*/;
+  const size_t small = 256 + 4 * (4 * R + 1) + 4 /*status*/;
   const size_t small_pad = (small + 255) / 256 * 256;
   return small_pad + R * (size_t)(f / kDecodeChunk) * d * sizeof(float);
 }
@@ -110,8 +115,9 @@ extern "C" int ft_decode_experts_noalloc(const void* arena_dev, int num_slots, i
   int32_t* group_slot = counts + 64;
   int32_t* group_off = group_slot + R;
   int32_t* group_routes = group_off + R + 1;
-  uint32_t* status = status_dev ? status_dev : reinterpret_cast<uint32_t*>(group_routes + R);
-  size_t small = 256 + 4 * (3 * (size_t)R + 1) + 4;
+  int32_t* merge_sid = group_routes + R;
+  uint32_t* status = status_dev ? status_dev : reinterpret_cast<uint32_t*>(merge_sid + R);
+  size_t small = 256 + 4 * (4 * (size_t)R + 1) + 4;
   float* ypart = reinterpret_cast<float*>(p + (small + 255) / 256 * 256);
 
   const uint64_t d = hidden, f = inter;
@@ -134,7 +140,7 @@ extern "C" int ft_decode_experts_noalloc(const void* arena_dev, int num_slots, i
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   route_groups_kernel<<<1, 32, 0, st>>>(slot_ids_dev, R, num_slots, counts, group_slot, group_off, group_routes,
-                                        status);
+                                        merge_sid, status);
   if (cudaGetLastError() != cudaSuccess) return fail(FT_E_CUDA, "route group launch failed");
   DecodeArgs a{};
   a.arena = static_cast<const uint8_t*>(arena_dev);
@@ -158,7 +164,7 @@ extern "C" int ft_decode_experts_noalloc(const void* arena_dev, int num_slots, i
   a.tmap_gu = &tmap_gu;
   cudaError_t e = launch_decode_experts(a, st);
   if (e != cudaSuccess) return record_error(FT_E_CUDA, "expert launch failed: %s", cudaGetErrorString(e));
-  e = launch_merge(ypart, inter / kDecodeChunk, slot_ids_dev, weights_dev, partial_dev, out_dev, T, top_k, hidden, st);
+  e = launch_merge(ypart, inter / kDecodeChunk, merge_sid, weights_dev, partial_dev, out_dev, T, top_k, hidden, st);
   if (e != cudaSuccess) return record_error(FT_E_CUDA, "merge launch failed: %s", cudaGetErrorString(e));
   return FT_OK;
 }

@@ -482,7 +482,12 @@ int ft_cache_rebuild_retain(ft_ctx* c, int new_slots) {
   std::stable_sort(kept.begin(), kept.end(), [&](int x, int y) { return lu[x] > lu[y]; });
   if ((int)kept.size() > new_slots) kept.resize(new_slots);
 
-  // the new arena and tables next to the old ones (the old cache survives a failure)
+  // The new arena and tables are built next to the old ones; the context
+  // switches to them only once every copy has succeeded, so on any failure
+  // the old cache is left as it was.  slot_of is shared: its old contents are
+  // kept on the host to put back.
+  std::vector<int32_t> so_old(c->E_tot);
+  CU(cudaMemcpy(so_old.data(), c->slot_of, sizeof(int32_t) * c->E_tot, cudaMemcpyDeviceToHost));
   uint8_t* old_arena = c->arena;
   int32_t* old_eo = c->expert_of;
   uint32_t* old_lu = c->last_use;
@@ -490,8 +495,9 @@ int ft_cache_rebuild_retain(ft_ctx* c, int new_slots) {
   c->arena = nullptr;
   c->expert_of = nullptr;
   c->last_use = nullptr;
-  int rc = alloc_arena(c, new_slots);
-  if (rc) {
+  auto restore = [&](int code) {
+    cudaStreamSynchronize(c->xfer);
+    cudaGetLastError();
     cudaFree(c->arena);
     cudaFree(c->expert_of);
     cudaFree(c->last_use);
@@ -501,8 +507,16 @@ int ft_cache_rebuild_retain(ft_ctx* c, int new_slots) {
     c->tmap_wd = old_wd;
     c->tmap_gu = old_gu;
     c->S = S_old;
-    return rc;
-  }
+    cudaMemcpy(c->slot_of, so_old.data(), sizeof(int32_t) * c->E_tot, cudaMemcpyHostToDevice);
+    return code;
+  };
+  int rc = alloc_arena(c, new_slots);
+  if (rc) return restore(rc);
+#define CU_OR_RESTORE(call)                                                                               \
+  do {                                                                                                    \
+    cudaError_t e_ = (call);                                                                              \
+    if (e_ != cudaSuccess) return restore(fail(FT_E_CUDA, "%s: %s", #call, cudaGetErrorString(e_))); \
+  } while (0)
   std::vector<int32_t> so_new(c->E_tot, -1), eo_new(new_slots, -1);
   std::vector<uint32_t> lu_new(new_slots, 0);
   for (size_t i = 0; i < kept.size(); ++i) {
@@ -510,12 +524,14 @@ int ft_cache_rebuild_retain(ft_ctx* c, int new_slots) {
     eo_new[i] = u;
     so_new[u] = (int32_t)i;
     lu_new[i] = lu[s];
-    CU(cudaMemcpyAsync(c->arena + i * c->Bx, old_arena + (size_t)s * c->Bx, c->Bx, cudaMemcpyDeviceToDevice, c->xfer));
+    CU_OR_RESTORE(cudaMemcpyAsync(c->arena + i * c->Bx, old_arena + (size_t)s * c->Bx, c->Bx,
+                                  cudaMemcpyDeviceToDevice, c->xfer));
   }
-  CU(cudaMemcpy(c->slot_of, so_new.data(), sizeof(int32_t) * c->E_tot, cudaMemcpyHostToDevice));
-  CU(cudaMemcpy(c->expert_of, eo_new.data(), sizeof(int32_t) * new_slots, cudaMemcpyHostToDevice));
-  CU(cudaMemcpy(c->last_use, lu_new.data(), sizeof(uint32_t) * new_slots, cudaMemcpyHostToDevice));
-  CU(cudaStreamSynchronize(c->xfer));
+  CU_OR_RESTORE(cudaMemcpy(c->expert_of, eo_new.data(), sizeof(int32_t) * new_slots, cudaMemcpyHostToDevice));
+  CU_OR_RESTORE(cudaMemcpy(c->last_use, lu_new.data(), sizeof(uint32_t) * new_slots, cudaMemcpyHostToDevice));
+  CU_OR_RESTORE(cudaStreamSynchronize(c->xfer));
+  CU_OR_RESTORE(cudaMemcpy(c->slot_of, so_new.data(), sizeof(int32_t) * c->E_tot, cudaMemcpyHostToDevice));
+#undef CU_OR_RESTORE
   cudaFree(old_arena);
   cudaFree(old_eo);
   cudaFree(old_lu);

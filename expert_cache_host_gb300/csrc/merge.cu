@@ -1,10 +1,9 @@
-// Partial-sum merge.
+// Partial-sum merge (FreeToken article, section "设计 1", Decode bullet).
 //
-// FreeToken article, section "设计 1" Decode bullet: the CPU and the GPU each
-// compute a partial sum over their experts and the two are merged exactly,
-// with no algorithmic approximation.  Here the CPU-side sum arrives as a
-// float32 buffer `partial` (NULL = 0), and the GPU side is the weighted sum of
-// the expert outputs of the routes that have a slot:
+// Contract: the routes a decode step leaves to the host side contribute one
+// float32 buffer `partial` [T, d] (NULL means zero); this kernel adds the
+// weighted outputs of the routes that run on the GPU, so that the layer's
+// output is the same sum the unsplit MoE would give:
 //     out[t] = partial[t] + sum_j [slot_ids[t,j] >= 0] w[t,j] * sum_c ypart[t*k+j, c]
 // A block owns 4 float4 columns of one token; its 64 thread rows split the
 // k * n_chunks (route, chunk) partials of those columns (each row issues up

@@ -38,8 +38,9 @@
  *    Pointers returned in ft_step_out are owned by the context.
  *  - bf16 values are passed as their 16-bit patterns (uint16_t).
  *
- * Canonical host pool layout (the "final runtime layout" the page has the
- * loader write before pinning, section "设计 3" fast start):
+ * Canonical host pool layout (the layout the experts are served from, written
+ * once by the loader before the memory is pinned; section "设计 3", fast
+ * start):
  *  expert (l, e) starts at byte (l*E + e) * B_x;
  *  bf16   expert: [W_gate f x d | W_up f x d | W_down d x f], row-major,
  *         B_x = 6*d*f;
