@@ -65,7 +65,9 @@ def _l():
             lib.or_dense_moe.argtypes = [vp, u64, i32, i32, i32, i32, i32, vp, vp, vp]
             lib.or_threads.argtypes = []
             lib.or_threads.restype = i32
-            for fn in ("or_route", "or_cache_step", "or_expert_ffn", "or_moe_forward", "or_dense_moe"):
+            lib.or_adapt_ratio.argtypes = [i32, vp, vp, dbl, i32, i32, vp]
+            for fn in ("or_route", "or_cache_step", "or_expert_ffn", "or_moe_forward", "or_dense_moe",
+                       "or_adapt_ratio"):
                 getattr(lib, fn).restype = i32
             _lib = lib
     return _lib
@@ -252,3 +254,16 @@ def normwise_err(y: np.ndarray, ref: np.ndarray) -> float:
     ref = np.asarray(ref, dtype=np.float64)
     n = float(np.linalg.norm(ref))
     return float(np.linalg.norm(y - ref)) / n if n > 0 else float(np.linalg.norm(y - ref))
+
+
+# ------------------------------------------------------- run-time r = BP/BH
+
+def adapt_ratio_trace(bp, bh, alpha: float, r_den: int = 256, r_num_max: int = 256 * 64) -> np.ndarray:
+    """r_num after each measurement window of (BP, BH) samples (<= 0 = none);
+    -1 until both have a sample.  See or_adapt_ratio."""
+    bp = np.ascontiguousarray(bp, dtype=np.float64)
+    bh = np.ascontiguousarray(bh, dtype=np.float64)
+    assert bp.shape == bh.shape
+    out = np.empty(bp.size, dtype=np.int32)
+    _check(_l().or_adapt_ratio(bp.size, _p(bp), _p(bh), float(alpha), r_den, r_num_max, _p(out)), "or_adapt_ratio")
+    return out

@@ -396,3 +396,37 @@ int or_dense_moe(const uint8_t* layer_base, uint64_t expert_bytes, int dtype, in
   free(y);
   return OR_OK;
 }
+
+/* ------------------------------------------------- run-time r = BP/BH */
+
+/*
+ * [D1-Dec] splits the misses by q* ~ m*BP/BH with BP and BH the bandwidths
+ * measured while the system runs.  The page does not say how measurements
+ * become r; the reading taken: each measurement window gives at most one
+ * sample of each (a value <= 0 = no sample); an estimate starts at its first
+ * sample and then moves by est <- est + alpha*(sample - est); once both
+ * estimates exist r is BP/BH rounded half up onto the grid 1/r_den, at most
+ * r_num_max/r_den, and -1 marks "no r yet".  out[i] is r_num after window i.
+ */
+int or_adapt_ratio(int n, const double* bp, const double* bh, double alpha, int r_den, int r_num_max, int32_t* out) {
+  if (n < 0 || !(alpha > 0.0 && alpha <= 1.0) || r_den < 1 || r_num_max < 0) return OR_EARG;
+  double est_p = 0.0, est_h = 0.0;
+  int have_p = 0, have_h = 0;
+  int32_t r = -1;
+  for (int i = 0; i < n; ++i) {
+    if (bp[i] > 0.0) {
+      est_p = have_p ? alpha * bp[i] + (1.0 - alpha) * est_p : bp[i];
+      have_p = 1;
+    }
+    if (bh[i] > 0.0) {
+      est_h = have_h ? alpha * bh[i] + (1.0 - alpha) * est_h : bh[i];
+      have_h = 1;
+    }
+    if (have_p && have_h) {
+      double q = floor((double)r_den * est_p / est_h + 0.5);
+      r = q >= (double)r_num_max ? r_num_max : (int32_t)q;
+    }
+    out[i] = r;
+  }
+  return OR_OK;
+}
