@@ -7,10 +7,22 @@ N(0, 0.02) in a 57.98 GB pinned host pool, batch 1, AR(1) hidden states
 (rho = 0.9), a shared LRU cache of 1536 slots (25% of 48x128), BP/BH = 1,
 K_max = 128.  One step is one decode token through all 48 layers -- routing,
 cache control, fills from the host pool, expert FFNs and merge -- replayed as
-one CUDA graph per token.  The same run adds, as components, the 8192-token
-prefill chunk of the same model (full-layer double buffer on and off, grouped
-GEMM throughput with weights resident) and the cache-control stress workload
-(48 layers x 64 tokens x top-8, 6144 slots, Zipf routes).
+one CUDA graph per token.  `e2e` runs the same tokens from the same cache state
+on a twin context with the token's inputs copied in from pinned host memory and
+every layer's output copied back inside the timed region.
+
+The same run adds, as components, every other workload of the method:
+  - the whole 512-token decode sequence from a cold cache, and A3B decode at
+    BP/BH = 1/2 and 2;
+  - the 8192-token prefill chunk of the same model (full-layer double buffer
+    on and off, grouped GEMM throughput with weights resident);
+  - route + control alone, graph-timed, at batch 1 and 16;
+  - the cache-control stress workload (48 layers x 64 tokens x top-8, 6144
+    slots, Zipf routes, 10 000 steps);
+  - the tiny single-layer model (64-token prefill chunk, 32 decode steps);
+  - V4-Flash-style MXFP4 decode at batch 1 and 16 (147 GB pool, built after the
+    A3B pool is freed);
+  - the host link measured over the whole pool, with the pool's memory node.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -21,6 +33,7 @@ line with value = tokens of all ranks / the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -38,22 +51,27 @@ if ROOT not in sys.path:
 import ftsynth  # noqa: E402
 
 METRIC = "MoE decode tok/s (A3B-style, batch 1, GPU side; CPU-routed experts arrive as a partial sum)"
-V4 = dict(L=43, E=256, k=6, d=4096, f=2048, dtype=1, S=2393, K_max=256, T=1, rho=0.9, r=(1, 1),
+V4 = dict(L=43, E=256, k=6, d=4096, f=2048, dtype=1, S=2393, K_max=256, T=1, rho=0.9, r=(1, 1), seq=256,
           desc="V4-Flash-style decode: 43 layers, d=4096, E=256, top-6, f=2048, MXFP4 experts (147 GB pool), "
                "S=2393 (32 GB budget), BP/BH=1, K_max=256, AR(1) rho=0.9")
-A3B = dict(L=48, E=128, k=8, d=2048, f=768, dtype=0, S=1536, K_max=128, T=1, rho=0.9, r=(1, 1),
+A3B = dict(L=48, E=128, k=8, d=2048, f=768, dtype=0, S=1536, K_max=128, T=1, rho=0.9, r=(1, 1), seq=512,
            desc="A3B-style decode: 48 layers, d=2048, E=128, top-8, f=768, bf16, batch 1, "
                 "S=1536 (25% of 6144), BP/BH=1, K_max=128, AR(1) rho=0.9")
 L2_BYTES = 129 * 2 ** 20
 
-# DRAM bytes per launch from ncu captures (profiles/); None once the kernel changed.
-# dram__bytes_read + dram__bytes_write / algorithmic bytes of the decode expert
-# kernels over the launches captured with ncu (--set full): three A3B bf16
-# launches (6 + 2 + 5 experts) and two V4 MXFP4 launches (4 + 2 experts); the
-# traffic reported per launch is this ratio times the launch's algorithmic bytes
-NCU_TRAFFIC_RATIO = {
-    "decode_experts": 123_111_424 / 122_683_392,
-    "decode_experts_mxfp4": 80_432_896 / 80_216_064,
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) over algorithmic
+# bytes for the launches of one ncu capture, with the kernel source it was
+# taken from (first 16 hex digits of its sha256) and the summary that records
+# it.  A launch's traffic is reported as ratio x its algorithmic bytes only
+# while the source is unchanged; otherwise traffic is null.
+NCU_TRAFFIC = {
+    "decode_experts": dict(ratio=123_111_424 / 122_683_392, src="expert_cache_host_gb300/csrc/expert_decode.cu",
+                           sha16="e5a4dc8ca19734a8", profile="profiles/decode_experts_a3b.md"),
+    "decode_experts_mxfp4": dict(ratio=80_432_896 / 80_216_064, src="expert_cache_host_gb300/csrc/expert_decode_mxfp4.cu",
+                                 sha16="c69e88ed9f44398c", profile="profiles/decode_experts_mxfp4_v4.md"),
+    # not captured yet: traffic is null
+    "decode_layer": dict(ratio=None, src="expert_cache_host_gb300/csrc/decode_layer.cu", sha16=None,
+                         profile="profiles/decode_layer_a3b.md"),
 }
 
 
@@ -86,6 +104,19 @@ def measured_peaks():
         return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
                     bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def ncu_traffic(kernel: str, algorithmic_bytes: float):
+    """(traffic bytes or None, note) for one launch of `kernel`."""
+    t = NCU_TRAFFIC[kernel]
+    if t["ratio"] is None:
+        return None, f"no ncu capture of {t['src']} yet"
+    with open(os.path.join(ROOT, t["src"]), "rb") as fh:
+        sha = hashlib.sha256(fh.read()).hexdigest()[:16]
+    if sha != t["sha16"]:
+        return None, f"{t['src']} changed since the ncu capture in {t['profile']}"
+    return round(t["ratio"] * algorithmic_bytes), f"ncu DRAM bytes / algorithmic bytes = {t['ratio']:.4f} " \
+                                                  f"({t['profile']}, source sha256 {sha}) x algorithmic bytes per launch"
 
 
 class ClockSampler:
@@ -160,15 +191,69 @@ def timed(stream, fn, reps=1):
     return e0.elapsed_time(e1) / 1e3
 
 
-def link_peak_gbs(pool, nbytes):
-    """Best of three host->device copies of `nbytes` of the pinned pool (copy engine)."""
+def pool_placement(pool):
+    """Host-side record of where the pool's pages live: the memory nodes this
+    process sees, the GPU's nearest node, and the pages of the pool's mapping
+    per node (/proc/self/numa_maps)."""
     import torch
-    src = torch.from_numpy(pool[:nbytes])
-    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    rec = {}
+    try:
+        with open("/sys/devices/system/node/online") as fh:
+            rec["nodes_online"] = fh.read().strip()
+    except OSError:
+        rec["nodes_online"] = None
+    try:
+        bus = torch.cuda.get_device_properties(torch.cuda.current_device()).pci_bus_id.lower()
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as fh:
+            rec["gpu_numa_node"] = int(fh.read().strip())
+    except (OSError, AttributeError, ValueError):
+        rec["gpu_numa_node"] = None
+    base = pool.ctypes.data
+    try:
+        with open("/proc/self/numa_maps") as fh:
+            for line in fh:
+                parts = line.split()
+                start = int(parts[0], 16)
+                if start <= base < start + pool.nbytes and start >= base - (1 << 30):
+                    rec["pool_pages_per_node"] = {p.split("=")[0]: int(p.split("=")[1]) for p in parts
+                                                  if p.startswith("N") and "=" in p}
+                    rec["page_kb"] = next((int(p.split("=")[1]) for p in parts if p.startswith("kernelpagesize_kB")), None)
+                    rec["policy"] = parts[1]
+                    break
+    except OSError:
+        pass
+    return rec
+
+
+def host_link_profile(pool, chunk=1 << 30):
+    """Host -> device copy-engine rate over the WHOLE pool: every 1 GiB chunk
+    copied once, each timed with CUDA events (the rate the pool can stream at,
+    which prefill uploads and decode fills see), plus the best of three copies
+    of the first 1.21 GB (a burst from a region touched just before)."""
+    import torch
+    n = pool.nbytes // chunk
+    src = torch.from_numpy(pool[:n * chunk]).view(n, chunk)
+    dst = torch.empty(chunk, dtype=torch.uint8, device="cuda")
     s = torch.cuda.current_stream()
-    best = min(timed(s, lambda: dst.copy_(src, non_blocking=True)) for _ in range(3))
-    del dst
-    return nbytes / best / 1e9
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    s.synchronize()
+    ev[0].record(s)
+    for i in range(n):
+        dst.copy_(src[i], non_blocking=True)
+        ev[i + 1].record(s)
+    ev[n].synchronize()
+    per = [chunk / (ev[i].elapsed_time(ev[i + 1]) / 1e3) / 1e9 for i in range(n)]
+    whole = n * chunk / (ev[0].elapsed_time(ev[n]) / 1e3) / 1e9
+    burst_bytes = min(pool.nbytes, 1_207_959_552)
+    b = torch.from_numpy(pool[:burst_bytes])
+    bd = torch.empty(burst_bytes, dtype=torch.uint8, device="cuda")
+    burst = burst_bytes / min(timed(s, lambda: bd.copy_(b, non_blocking=True)) for _ in range(3)) / 1e9
+    del dst, bd
+    per.sort()
+    return {"whole_pool_gbs": round(whole, 1), "chunks": n, "chunk_gbs_min": round(per[0], 1),
+            "chunk_gbs_median": round(per[n // 2], 1), "chunk_gbs_max": round(per[-1], 1),
+            "burst_first_1p21gb_gbs": round(burst, 1),
+            "how": "pinned H2D cudaMemcpyAsync of every 1 GiB chunk of the pool once, CUDA events"}
 
 
 def experts_alone(w, pool, hid, reps=40):
@@ -207,9 +292,78 @@ def experts_alone(w, pool, hid, reps=40):
     return res
 
 
-# ----------------------------------------------------------------------------- decode (headline)
+# ----------------------------------------------------------------------------- decode
 
-def run_decode_leg(args, w, world, local, pool, hid, lg):
+class DecodeRun:
+    """One context over the decode workload, its per-token CUDA graph, and the
+    device copies of the step inputs."""
+
+    def __init__(self, w, pool, d_hid, d_lg):
+        import torch
+
+        import expert_cache_host_gb300 as ft
+        self.ft, self.w = ft, w
+        L, E, k, d, f, T = w["L"], w["E"], w["k"], w["d"], w["f"], w["T"]
+        cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, dtype=w["dtype"],
+                             num_slots=w["S"], k_max=w["K_max"], t_max=T, r_num=w["r"][0], r_den=w["r"][1],
+                             decode_path=w.get("decode_path", 0), fill_ctas=w.get("fill_ctas", 0))
+        t0 = time.time()
+        self.ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
+        self.t_init = time.time() - t0
+        self.d_hid, self.d_lg = d_hid, d_lg
+        self.cur_hid = torch.empty((L, T, d), dtype=torch.int16, device="cuda")
+        self.cur_lg = torch.empty((L, T, E), dtype=torch.float32, device="cuda")
+        self.out = torch.empty((L, T, d), dtype=torch.float32, device="cuda")
+        self.stream = torch.cuda.Stream()
+        self.graph = None
+
+    def token(self, st):
+        ft, L, T = self.ft, self.w["L"], self.w["T"]
+        for l in range(L):
+            ft.ft_cache_step(self.ctx, l, self.cur_lg[l].data_ptr(), T, st)
+            ft.ft_moe_forward(self.ctx, l, ft.FT_DECODE_CACHED, 0, self.cur_hid[l].data_ptr(), T, 0,
+                              self.out[l].data_ptr(), st)
+
+    def begin(self):
+        """Token 0 eagerly (kernel attributes are set outside any capture), then
+        capture one token as a graph.  Returns the next token index."""
+        import torch
+        with torch.cuda.stream(self.stream):
+            self.cur_hid.copy_(self.d_hid[0])
+            self.cur_lg.copy_(self.d_lg[0])
+            self.token(self.stream.cuda_stream)
+            self.stream.synchronize()
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=self.stream):
+                self.token(torch.cuda.current_stream().cuda_stream)
+        return 1
+
+    def step(self, s):
+        self.cur_hid.copy_(self.d_hid[s])
+        self.cur_lg.copy_(self.d_lg[s])
+        self.graph.replay()
+
+    def counters(self):
+        return self.ft.ft_get_counters(self.ctx, self.w["L"])
+
+    def destroy(self):
+        if self.ctx:
+            self.ft.ft_moe_destroy(self.ctx)
+            self.ctx = None
+
+
+def _window(c0, c1):
+    dc = (c1 - c0).astype(np.float64)
+    hits, misses, fills, cpu = (dc[:, i].sum() for i in range(4))
+    return hits, misses, fills, cpu
+
+
+def run_decode_leg(args, w, world, local, pool, hid, lg, with_e2e=True, seq=True, profile=True):
+    """Headline decode measurement.  Context A times tokens W..W+K-1 (device
+    inputs, graph replays); context B, which stepped through the same W warm-up
+    tokens, times the same K tokens end to end (pinned host inputs in, every
+    layer's output out).  A then runs P profiled tokens eagerly (per-kernel
+    CUDA events) and, from a cold rebuild, the whole decode sequence."""
     import torch
 
     import expert_cache_host_gb300 as ft
@@ -217,108 +371,230 @@ def run_decode_leg(args, w, world, local, pool, hid, lg):
     L, E, k, d, f, T = w["L"], w["E"], w["k"], w["d"], w["f"], w["T"]
     bx = ftsynth.expert_bytes(d, f, w["dtype"])
     W, K = args.warmup, args.steps
-    P, E2E = min(K, args.profile_steps), min(K, args.e2e_steps)
-    cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, dtype=w["dtype"],
-                         num_slots=w["S"], k_max=w["K_max"], t_max=T, r_num=w["r"][0], r_den=w["r"][1])
-    t0 = time.time()
-    ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
-    t_init = time.time() - t0
+    P = min(K, args.profile_steps) if profile else 0
+    d_hid = torch.from_numpy(hid.view(np.int16)).cuda()
+    d_lg = torch.from_numpy(lg).cuda()
+    A = DecodeRun(w, pool, d_hid, d_lg)
+    B = DecodeRun(w, pool, d_hid, d_lg) if with_e2e else None
+    res = {}
     try:
         if args.cpu_exec:
-            ft.ft_cpu_executor(ctx, args.cpu_exec)
-        d_hid = torch.from_numpy(hid.view(np.int16)).cuda()
-        d_lg = torch.from_numpy(lg).cuda()
-        cur_hid = torch.empty((L, T, d), dtype=torch.int16, device="cuda")
-        cur_lg = torch.empty((L, T, E), dtype=torch.float32, device="cuda")
-        out = torch.empty((L, T, d), dtype=torch.float32, device="cuda")
-        stream = torch.cuda.Stream()
-        h_hid = torch.from_numpy(hid.view(np.int16)).pin_memory()
-        h_lg = torch.from_numpy(lg).pin_memory()
-        h_out = torch.empty((L, T, d), dtype=torch.float32).pin_memory()
-
-        def token(st):
-            for l in range(L):
-                ft.ft_cache_step(ctx, l, cur_lg[l].data_ptr(), T, st)
-                ft.ft_moe_forward(ctx, l, ft.FT_DECODE_CACHED, 0, cur_hid[l].data_ptr(), T, 0, out[l].data_ptr(), st)
-
-        with torch.cuda.stream(stream):
-            st = stream.cuda_stream
-            cur_hid.copy_(d_hid[0])
-            cur_lg.copy_(d_lg[0])
-            token(st)  # one eager token (step 0): kernel attributes are set outside the capture
-            stream.synchronize()
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                token(torch.cuda.current_stream().cuda_stream)
-            s = 1
-
-            def step():
-                nonlocal s
-                cur_hid.copy_(d_hid[s])
-                cur_lg.copy_(d_lg[s])
-                graph.replay()
-                s += 1
-
-            for _ in range(W - 1):
-                step()
-            stream.synchronize()
-            if world > 1:
-                torch.distributed.barrier()
-            c0 = ft.ft_get_counters(ctx, L)
+            ft.ft_cpu_executor(A.ctx, args.cpu_exec)
+            if B:
+                ft.ft_cpu_executor(B.ctx, args.cpu_exec)
+        s = A.begin()
+        if B:
+            B.begin()
+        with torch.cuda.stream(A.stream):
+            for i in range(s, W):
+                A.step(i)
+                if B:
+                    with torch.cuda.stream(B.stream):
+                        B.step(i)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        c0 = A.counters()
+        ft.ft_decode_meters(A.ctx, reset=True)
+        it = iter(range(W, W + K))
+        with torch.cuda.stream(A.stream):
             with ClockSampler(local) as clk:
-                elapsed = timed(stream, step, K)
-            if world > 1:
-                torch.distributed.barrier()
-            c1 = ft.ft_get_counters(ctx, L)
-            clocks = clk.summary()
+                elapsed = timed(A.stream, lambda: A.step(next(it)), K)
+        if world > 1:
+            torch.distributed.barrier()
+        c1 = A.counters()
+        res["meters"] = ft.ft_decode_meters(A.ctx, reset=True)  # fill and resident-expert phases of the window
+        res["path"] = "fused" if ft.ft_decode_path(A.ctx) == ft.FT_DECODE_FUSED else "split"
+        clocks = clk.summary()
+        hits, misses, fills, cpu = _window(c0, c1)
 
-            # per-kernel durations: the following steps run eagerly with event timing
-            ft.ft_profile_enable(ctx, True)
-            ft.ft_profile_read(ctx, reset=True)
-            cp0 = ft.ft_get_counters(ctx, L)
-            for _ in range(P):
-                cur_hid.copy_(d_hid[s])
-                cur_lg.copy_(d_lg[s])
-                token(st)
-                s += 1
-            prof = ft.ft_profile_read(ctx, reset=True)
-            cp1 = ft.ft_get_counters(ctx, L)
-            ft.ft_profile_enable(ctx, False)
+        e2e_elapsed = None
+        if B:
+            h_hid = torch.from_numpy(hid.view(np.int16)).pin_memory()
+            h_lg = torch.from_numpy(lg).pin_memory()
+            h_out = torch.empty((L, T, d), dtype=torch.float32).pin_memory()
+            cb0 = B.counters()
+            it2 = iter(range(W, W + K))
 
-            # end to end: pinned host inputs in, every layer's output back, per token
             def e2e_step():
-                nonlocal s
-                cur_hid.copy_(h_hid[s], non_blocking=True)
-                cur_lg.copy_(h_lg[s], non_blocking=True)
-                graph.replay()
-                h_out.copy_(out, non_blocking=True)
-                s += 1
+                i = next(it2)
+                B.cur_hid.copy_(h_hid[i], non_blocking=True)
+                B.cur_lg.copy_(h_lg[i], non_blocking=True)
+                B.graph.replay()
+                h_out.copy_(B.out, non_blocking=True)
 
-            e2e_elapsed = timed(stream, e2e_step, E2E)
-        status = ft.ft_get_status(ctx)
+            with torch.cuda.stream(B.stream):
+                e2e_elapsed = timed(B.stream, e2e_step, K)
+            cb1 = B.counters()
+            # same tokens from the same cache state: the control streams agree
+            res["e2e_same_window"] = bool(np.array_equal(cb1 - cb0, c1 - c0))
+            B.destroy()
+            B = None
+
+        prof = None
+        if P:
+            ft.ft_profile_enable(A.ctx, True)
+            ft.ft_profile_read(A.ctx, reset=True)
+            cp0 = A.counters()
+            with torch.cuda.stream(A.stream):
+                for i in range(W + K, W + K + P):
+                    A.cur_hid.copy_(d_hid[i])
+                    A.cur_lg.copy_(d_lg[i])
+                    A.token(A.stream.cuda_stream)
+            prof = ft.ft_profile_read(A.ctx, reset=True)
+            cp1 = A.counters()
+            ft.ft_profile_enable(A.ctx, False)
+            dp = (cp1 - cp0).astype(np.float64)
+            groups_p, fills_p = dp[:, 0].sum() + dp[:, 2].sum(), dp[:, 2].sum()
+
+        if seq:
+            res["sequence"] = _sequence(A, w, hid.shape[0])
+        status = ft.ft_get_status(A.ctx)
+        t_init = A.t_init
     finally:
-        ft.ft_moe_destroy(ctx)
+        A.destroy()
+        if B:
+            B.destroy()
 
-    dc = (c1 - c0).astype(np.float64)
-    hits, misses, fills, cpu = (dc[:, i].sum() for i in range(4))
     elapsed_max, units = replica_reduce(elapsed, K * T, world)
-    dp = (cp1 - cp0).astype(np.float64)
-    groups_p, fills_p = dp[:, 0].sum() + dp[:, 2].sum(), dp[:, 2].sum()
-    tot_ms = sum(v[0] for v in prof.values())
-    ex_ms, ex_n = prof["experts"]
-    fill_ms, fill_n = prof["fill"]
-    return dict(
-        value=units / elapsed_max, elapsed=elapsed_max, K=K, W=W, T=T, clocks=clocks, status=status,
-        t_init=t_init, hits=hits, misses=misses, fills=fills, cpu=cpu, P=P,
-        shares={n: round(v[0] / tot_ms, 4) for n, v in prof.items() if v[1]},
-        ms_per_token={n: round(v[0] / P, 4) for n, v in prof.items() if v[1]},
-        launches={n: v[1] for n, v in prof.items() if v[1]},
-        ex_bytes=groups_p * bx, ex_ms=ex_ms, ex_n=ex_n, fill_bytes=fills_p * bx, fill_ms=fill_ms, fill_n=fill_n,
-        control_us=prof["control"][0] / max(1, prof["control"][1]) * 1e3,
-        route_us=prof["route"][0] / max(1, prof["route"][1]) * 1e3,
-        eager_ms=tot_ms / P if P else None,
-        e2e=E2E * T / e2e_elapsed, h2d=int(lg[0].nbytes + hid[0].nbytes), d2h=int(L * T * d * 4),
-    )
+    res.update(value=units / elapsed_max, elapsed=elapsed_max, K=K, W=W, T=T, clocks=clocks, status=status,
+               t_init=t_init, hits=hits, misses=misses, fills=fills, cpu=cpu, P=P)
+    if B is None and e2e_elapsed is not None:
+        res.update(e2e=K * T / e2e_elapsed, h2d=int(lg[0].nbytes + hid[0].nbytes), d2h=int(L * T * d * 4))
+    if prof:
+        tot_ms = sum(v[0] for v in prof.values())
+        ex_ms, ex_n = prof["experts"]
+        fill_ms, fill_n = prof["fill"]
+        res.update(shares={n: round(v[0] / tot_ms, 4) for n, v in prof.items() if v[1]},
+                   ms_per_token={n: round(v[0] / P, 4) for n, v in prof.items() if v[1]},
+                   launches={n: v[1] for n, v in prof.items() if v[1]},
+                   ex_bytes=groups_p * bx, ex_ms=ex_ms, ex_n=ex_n, fill_bytes=fills_p * bx, fill_ms=fill_ms,
+                   fill_n=fill_n, control_us=prof["control"][0] / max(1, prof["control"][1]) * 1e3,
+                   eager_ms=tot_ms / P)
+    return res
+
+
+def _sequence(A, w, n_avail):
+    """The configured decode sequence from a cold cache (ft_cache_rebuild
+    resets the table; the graph is captured again): tokens [0, 64) and [64, N)
+    timed separately, with the hit rate of each part."""
+    import torch
+    ft = A.ft
+    N = min(w["seq"], n_avail)
+    ft.ft_cache_rebuild(A.ctx, w["S"])
+    A.begin()  # token 0 eagerly and a new capture (the rebuild changed the epoch)
+    cut = min(64, N)
+    out = {}
+    with torch.cuda.stream(A.stream):
+        c_prev = None
+        for name, lo, hi in (("first", 1, cut), ("rest", cut, N)):
+            if hi <= lo:
+                continue
+            c0 = A.counters() if c_prev is None else c_prev
+            it = iter(range(lo, hi))
+            el = timed(A.stream, lambda: A.step(next(it)), hi - lo)
+            c1 = A.counters()
+            c_prev = c1
+            h, m, fi, _ = _window(c0, c1)
+            out[name] = dict(tokens=[lo, hi], tok_s=round((hi - lo) * w["T"] / el, 3),
+                             hit_rate=round(h / max(1.0, h + m), 4), fills_per_token=round(fi / ((hi - lo) * w["T"]), 3))
+    tot = sum(v["tokens"][1] - v["tokens"][0] for v in out.values())
+    t_all = sum((v["tokens"][1] - v["tokens"][0]) * w["T"] / v["tok_s"] for v in out.values())
+    return dict(tokens=N, tok_s_tokens_1_to_N=round(tot * w["T"] / t_all, 3), **out,
+                note="token 0 runs eagerly before the capture and is not timed")
+
+
+def run_adaptive_leg(args, w, pool, hid, lg, threads=8, every=4):
+    """Run-time r = BP/BH: A3B decode with the context's CPU expert executor,
+    starting from r = 1/2; every `every` tokens ft_adapt_ratio reads the
+    measured fill rate (BP) and CPU expert rate (BH) and sets r (graphs pick
+    it up from device memory).  The adaptation calls are inside the timed
+    region (they synchronise)."""
+    import torch
+
+    import expert_cache_host_gb300 as ft
+    wr = dict(w, r=(1, 2))
+    d_hid = torch.from_numpy(hid.view(np.int16)).cuda()
+    d_lg = torch.from_numpy(lg).cuda()
+    A = DecodeRun(wr, pool, d_hid, d_lg)
+    try:
+        ft.ft_cpu_executor(A.ctx, threads)
+        a = ft.ft_ratio_adapter_init(0.5, 256, 256 * 64)
+        r_seq = []
+        s = A.begin()
+        W, K = args.warmup, args.steps
+
+        def tok(i):
+            if i % every == 0:
+                ft.ft_adapt_ratio(A.ctx, a, A.stream.cuda_stream)
+            r_seq.append(a.r_num)
+            A.step(i)
+
+        with torch.cuda.stream(A.stream):
+            for i in range(s, W):
+                tok(i)
+            c0 = A.counters()
+            it = iter(range(W, W + K))
+            el = timed(A.stream, lambda: tok(next(it)), K)
+            c1 = A.counters()
+        h, m, fi, cpu = _window(c0, c1)
+        return dict(workload=wr["desc"].replace("BP/BH=1", "BP/BH adapted at run time from 1/2") +
+                    f", CPU expert executor ({threads} host threads), r updated every {every} tokens",
+                    tok_s=round(K * w["T"] / el, 3), timed_tokens=K, warmup_tokens=W,
+                    r_den=a.r_den, r_num_at_tokens={str(i + s): x for i, x in enumerate(r_seq) if
+                                                    i == 0 or x != r_seq[i - 1]},
+                    bp_gbs_estimate=round(a.bp_gbs, 1), bh_gbs_estimate=round(a.bh_gbs, 1),
+                    hit_rate=round(h / max(1.0, h + m), 4), fills_per_token=round(fi / (K * w["T"]), 3),
+                    cpu_routes_per_token=round(cpu / (K * w["T"]), 3), device_status=ft.ft_get_status(A.ctx))
+    finally:
+        A.destroy()
+
+
+def run_route_control_leg(w, batches=(1, 16), n=128):
+    """Route + control (one fused kernel per layer step) alone, graph-timed:
+    one CUDA graph of the L ft_cache_step calls replayed over n decode steps
+    with new logits, CUDA events around the replays; microseconds per layer
+    step.  The cache state follows the same route stream as in decode."""
+    import torch
+
+    import expert_cache_host_gb300 as ft
+    L, E, k, d, f = w["L"], w["E"], w["k"], w["d"], w["f"]
+    pool = np.zeros(L * E * ftsynth.expert_bytes(256, 128, 0), dtype=np.uint8)  # never read by the control path
+    out = []
+    for T in batches:
+        _, lg = decode_inputs(dict(w, T=T), n)
+        d_lg = torch.from_numpy(lg).cuda()
+        cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=256, inter=128, num_slots=w["S"],
+                             k_max=w["K_max"], t_max=T)
+        ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
+        try:
+            cur = torch.empty((L, T, E), dtype=torch.float32, device="cuda")
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                cur.copy_(d_lg[0])
+                for l in range(L):
+                    ft.ft_cache_step(ctx, l, cur[l].data_ptr(), T, st.cuda_stream)
+                st.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=st):
+                    for l in range(L):
+                        ft.ft_cache_step(ctx, l, cur[l].data_ptr(), T, torch.cuda.current_stream().cuda_stream)
+                i = 1
+
+                def step():
+                    nonlocal i
+                    cur.copy_(d_lg[i])
+                    g.replay()
+                    i += 1
+
+                for _ in range(8):
+                    step()
+                el = timed(st, step, n - 9)
+            out.append(dict(T=T, S=w["S"], K_max=w["K_max"], us_per_layer_step=round(el / ((n - 9) * L) * 1e6, 3),
+                            layer_steps=(n - 9) * L, status=ft.ft_get_status(ctx)))
+        finally:
+            ft.ft_moe_destroy(ctx)
+    return out
 
 
 # ----------------------------------------------------------------------------- prefill chunk
@@ -440,49 +716,146 @@ def run_control_leg(args):
     return out
 
 
+# ----------------------------------------------------------------------------- tiny model
+
+def run_tiny_leg():
+    """The tiny single-layer model: d=256, E=16, top-2, f=128, bf16, S=8,
+    BP/BH=1.  One 64-token prefill chunk (median of 20, events), then 32
+    batch-1 decode steps from a cold cache as graph replays (AR(1) hidden)."""
+    import torch
+
+    import expert_cache_host_gb300 as ft
+    L, E, k, d, f, S, Tp, n_dec = 1, 16, 2, 256, 128, 8, 64, 32
+    pool = ftsynth.make_pool(0, L, E, d, f, 0, 0.02, threads=4)
+    wr = ftsynth.router_weights(0, L, E, d)
+    hp = ftsynth.prefill_hidden(0, 0, Tp, d)
+    lp = ftsynth.router_logits(hp, wr[0])
+    hd = ftsynth.ar1_hidden(0, 0, 0, n_dec + 1, d)
+    ld = ftsynth.router_logits(hd, wr[0])
+    cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, num_slots=S, k_max=16, t_max=1,
+                         prefill_buffers=1, prefill_t_max=Tp)
+    ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
+    try:
+        st = torch.cuda.Stream()
+        d_hp, d_lp = torch.from_numpy(hp.view(np.int16)).cuda(), torch.from_numpy(lp).cuda()
+        d_hd, d_ld = torch.from_numpy(hd.view(np.int16)).cuda(), torch.from_numpy(ld).cuda()
+        out_p = torch.empty((Tp, d), dtype=torch.float32, device="cuda")
+        out = torch.empty((1, d), dtype=torch.float32, device="cuda")
+        cur_h, cur_l = torch.empty((1, d), dtype=torch.int16, device="cuda"), torch.empty((1, E), device="cuda")
+        with torch.cuda.stream(st):
+            pf = lambda: ft.ft_moe_forward(ctx, 0, ft.FT_PREFILL_LAYER, d_lp.data_ptr(), d_hp.data_ptr(), Tp, 0,
+                                           out_p.data_ptr(), st.cuda_stream)
+            pf()
+            pre = statistics.median(timed(st, pf) for _ in range(20))
+
+            def tok(s):
+                ft.ft_cache_step(ctx, 0, cur_l.data_ptr(), 1, s)
+                ft.ft_moe_forward(ctx, 0, ft.FT_DECODE_CACHED, 0, cur_h.data_ptr(), 1, 0, out.data_ptr(), s)
+
+            cur_h.copy_(d_hd[0:1])
+            cur_l.copy_(d_ld[0:1])
+            tok(st.cuda_stream)
+            st.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                tok(torch.cuda.current_stream().cuda_stream)
+            i = 1
+
+            def step():
+                nonlocal i
+                cur_h.copy_(d_hd[i:i + 1])
+                cur_l.copy_(d_ld[i:i + 1])
+                g.replay()
+                i += 1
+
+            el = timed(st, step, n_dec)
+        c = ft.ft_get_counters(ctx, 1)[0]
+        return dict(workload="tiny: 1 layer, d=256, E=16, top-2, f=128, bf16, S=8, BP/BH=1",
+                    prefill_chunk_64_us=round(pre * 1e6, 2), decode_us_per_step=round(el / n_dec * 1e6, 2),
+                    decode_steps=n_dec + 1, hits=int(c[0]), misses=int(c[1]), fills=int(c[2]),
+                    status=ft.ft_get_status(ctx))
+    finally:
+        ft.ft_moe_destroy(ctx)
+
+
 # ----------------------------------------------------------------------------- oracle (CPU baseline / reference arm)
 
-def oracle_decode_rate(w, pool, hid, lg, budget_s, min_tokens=1, max_tokens=None):
-    """Time the oracle on the decode workload from a cold cache: whole tokens
-    (routing, cache step and fp64 experts for every layer) until budget_s.
-    Returns (tokens/s, tokens, seconds, threads used)."""
+def oracle_decode_rate(w, pool, hid, lg, budget_s, min_layer_steps=1, warmup_tokens=0, steps=None,
+                       layers_per_step=None):
+    """Time the oracle on the decode workload (routing, cache step and fp64
+    experts of every layer step), after warmup_tokens untimed tokens from a
+    cold cache.  steps=None: layer steps in token order until budget_s has
+    passed (at least min_layer_steps); else exactly `steps` steps, each the
+    first layers_per_step layers of one token.  Returns (tokens/s, tokens
+    timed -- fractional when a step covers part of a token, seconds, threads)."""
     import oracle
     L, E, k, d, f, T = w["L"], w["E"], w["k"], w["d"], w["f"], w["T"]
     bx = ftsynth.expert_bytes(d, f, w["dtype"])
-    n_tok = min(hid.shape[0], max_tokens or hid.shape[0])
     cache = oracle.Cache(L * E, w["S"])
-    layer_steps, t_spent = 0, 0.0
-    for s in range(n_tok):
-        for l in range(L):
+
+    def layer_step(s, l):
+        ids, wt = oracle.route(lg[s, l], k)
+        ref = cache.step(l, E, ids, w["r"][0], w["r"][1], w["K_max"])
+        oracle.moe_forward(pool[l * E * bx:(l + 1) * E * bx], bx, w["dtype"], d, f, ids, wt, hid[s, l],
+                           slot_ids=ref.slot_ids.reshape(T, k))
+
+    Ls = layers_per_step or L
+    for s in range(warmup_tokens):
+        for l in range(Ls):
+            layer_step(s, l)
+    done, t_spent = 0, 0.0
+    for s in range(warmup_tokens, hid.shape[0] if steps is None else warmup_tokens + steps):
+        for l in range(Ls):
             t0 = time.time()
-            ids, wt = oracle.route(lg[s, l], k)
-            ref = cache.step(l, E, ids, w["r"][0], w["r"][1], w["K_max"])
-            oracle.moe_forward(pool[l * E * bx:(l + 1) * E * bx], bx, w["dtype"], d, f, ids, wt, hid[s, l],
-                               slot_ids=ref.slot_ids.reshape(T, k))
+            layer_step(s, l)
             t_spent += time.time() - t0
-            layer_steps += 1
-            if layer_steps >= min_tokens * L and t_spent >= budget_s:
+            done += 1
+            if steps is None and done >= min_layer_steps and t_spent >= budget_s:
                 break
         else:
             continue
         break
     # the expert evaluations of one layer run in parallel over its T*k routes
     threads = min(oracle.threads(), T * k)
-    tokens = layer_steps / L
+    tokens = done / L
     return tokens * T / t_spent, tokens, t_spent, threads
 
 
-def run_reference(args, w):
-    """The oracle as the reference arm: same metric and unit, host cores."""
+def line_config(args, w, world):
+    """The `config` object both arms print (the same workload, in the same words)."""
+    bx = ftsynth.expert_bytes(w["d"], w["f"], w["dtype"])
+    return {"workload": w["desc"], "batch": w["T"], "graph": "one CUDA graph per token",
+            "l2": "inputs larger than L2: %.2f GB of expert weights per token" % (w["L"] * w["k"] * bx / 1e9),
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+
+
+def run_reference(args, w, world):
+    """The oracle as the reference arm: same metric, unit, config and step
+    counts -- W untimed warm-up steps from a cold cache, then exactly K timed
+    steps -- on the host cores.  A step is one decode token through all
+    layers, or, when W + K whole tokens would take longer than --ref-budget-s,
+    the first layers of one token (the oracle's cost per layer step does not
+    depend on the layer), and tok/s counts the layers actually run."""
+    import oracle
     pool = ftsynth.make_pool(0, w["L"], w["E"], w["d"], w["f"], w["dtype"], 0.02)
-    hid, lg = decode_inputs(w, max(2, min(args.steps, 64)))
-    rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, args.ref_budget_s, min_tokens=max(1, min(args.steps, 2)),
-                                              max_tokens=max(1, args.steps))
-    sample = f"{n:.2f} decode tokens x {w['L']} layers from a cold cache ({t:.1f} s of oracle work)"
+    W, K = args.warmup, args.steps
+    hid, lg = decode_inputs(w, W + K)
+    # cost of one layer step, from a throwaway one
+    bx = ftsynth.expert_bytes(w["d"], w["f"], w["dtype"])
+    ids, wt = oracle.route(lg[0, 0], w["k"])
+    t0 = time.time()
+    oracle.moe_forward(pool[:w["E"] * bx], bx, w["dtype"], w["d"], w["f"], ids, wt, hid[0, 0])
+    per_layer = time.time() - t0
+    Ls = max(1, min(w["L"], int(args.ref_budget_s / max(1e-9, (W + K) * per_layer))))
+    rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, args.ref_budget_s, warmup_tokens=W, steps=K,
+                                              layers_per_step=Ls)
+    what = "decode tokens" if Ls == w["L"] else f"steps of the first {Ls} of {w['L']} layers of a decode token"
+    sample = f"{K} timed {what} after {W} warm-up steps from a cold cache ({t:.1f} s of oracle work)"
     return {
-        "impl": "reference", "metric": METRIC, "value": round(rate, 5), "unit": "tok/s", "n_gpus": 1, "steps": n,
-        "warmup": 0, "ms_per_step": round(t / max(1, n) * 1e3, 2), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": w["desc"]},
+        "impl": "reference", "metric": metric_name(args, w), "value": round(rate, 5), "unit": "tok/s", "n_gpus": world,
+        "steps": int(K), "warmup": int(W), "ms_per_step": round(t / K * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": line_config(args, w, world),
         "cpu_baseline": {"value": round(rate, 5), "unit": "tok/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(rate, 5), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -499,11 +872,10 @@ def run_sweep(args, w, world, local):
     try:
         if args.sweep == "capacity":
             e_tot = w["L"] * w["E"]
-            hid, lg = decode_inputs(w, args.warmup + args.steps + min(args.steps, args.profile_steps)
-                                    + min(args.steps, args.e2e_steps))
+            hid, lg = decode_inputs(w, args.warmup + args.steps + min(args.steps, args.profile_steps))
             for pct in (5, 10, 25, 50):
                 ws = dict(w, S=max(w["k"] * w["T"], e_tot * pct // 100))
-                dec = run_decode_leg(args, ws, world, local, pool, hid, lg)
+                dec = run_decode_leg(args, ws, world, local, pool, hid, lg, with_e2e=False, seq=False, profile=False)
                 routes = dec["hits"] + dec["misses"]
                 print(json.dumps({
                     "sweep": "capacity", "workload": w["desc"].split(":")[0], "slots": ws["S"],
@@ -511,6 +883,23 @@ def run_sweep(args, w, world, local):
                     "expert_miss_rate": round(dec["misses"] / max(1.0, routes), 4),
                     "fills_per_token": round(dec["fills"] / (dec["K"] * dec["T"]), 3),
                     "timed_tokens": dec["K"], "warmup_tokens": dec["W"], "device_status": dec["status"]}), flush=True)
+        elif args.sweep == "fill":
+            hid, lg = decode_inputs(w, args.warmup + args.steps + min(args.steps, args.profile_steps))
+            peaks = measured_peaks()
+            points = [("split", 0)] + [("fused", n) for n in (19, 38, 57, 76)]
+            for rep in range(2):  # the link varies over minutes: every point twice, interleaved
+                for path, n in points:
+                    ws = dict(w, decode_path=0 if path == "fused" else 1, fill_ctas=n)
+                    dec = run_decode_leg(args, ws, world, local, pool, hid, lg, with_e2e=False, seq=False,
+                                         profile=path == "split")
+                    ex, _ = experts_rate(dec)
+                    print(json.dumps({
+                        "sweep": "fill", "workload": w["desc"].split(":")[0], "decode_path": dec["path"],
+                        "fill_ctas": n, "rep": rep, "tok_s": round(dec["value"], 3),
+                        "fill_gbs": round(fill_rate(dec), 1), "experts_gbs": round(ex, 1),
+                        "experts_frac_of_hbm": round(ex / peaks["hbm_gbs"], 4),
+                        "timed_tokens": dec["K"], "warmup_tokens": dec["W"], "device_status": dec["status"]}),
+                        flush=True)
         else:
             w = dict(w, dtype=0)
             for tokens in (4096, 8192, 16384):
@@ -542,6 +931,14 @@ def make_host_pool(args, w):
     return hp, pool, time.time() - t0
 
 
+def host_available() -> int:
+    with open("/proc/meminfo") as fh:
+        for line in fh:
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    return 0
+
+
 def metric_name(args, w):
     m = METRIC.replace("batch 1", f"batch {w['T']}") if w["dtype"] == 0 else \
         METRIC.replace("A3B-style, batch 1", f"V4-Flash-style MXFP4, batch {w['T']}")
@@ -550,58 +947,142 @@ def metric_name(args, w):
     return m
 
 
-def build_line(args, w, world, dec, link_gbs, pre, ctl, peaks):
-    ex_gbs = dec["ex_bytes"] / (dec["ex_ms"] / 1e3) / 1e9 if dec["ex_ms"] else 0.0
-    fill_gbs = dec["fill_bytes"] / (dec["fill_ms"] / 1e3) / 1e9 if dec["fill_ms"] else 0.0
+def fill_rate(dec):
+    """GB/s of the decode fill over the timed window: bytes over the summed
+    spans of the fill launches (device clock; the fused kernel's fill CTAs or
+    the split path's fill kernel)."""
+    m = dec.get("meters")
+    if m and m["fill_s"] > 0:
+        return m["fill_bytes"] / m["fill_s"] / 1e9
+    if dec.get("fill_ms"):
+        return dec["fill_bytes"] / (dec["fill_ms"] / 1e3) / 1e9
+    return 0.0
+
+
+def experts_rate(dec):
+    """(GB/s, how) of the decode experts.  Fused path: the experts resident
+    before the step, over the span from the first compute CTA start to the
+    last resident work item end, summed over the timed window's launches
+    (device clock).  Split path: every executed expert over the expert
+    launches' CUDA-event durations (profiled tokens)."""
+    m = dec.get("meters")
+    if dec.get("path") == "fused" and m and m["resident_s"] > 0:
+        return (m["resident_bytes"] / m["resident_s"] / 1e9,
+                "fused path: resident experts' bytes / resident phase span (first compute CTA start to last "
+                "resident item end), device clock, timed window")
+    if dec.get("ex_ms"):
+        return dec["ex_bytes"] / (dec["ex_ms"] / 1e3) / 1e9, "expert launches' bytes / CUDA-event durations, profiled tokens"
+    return 0.0, None
+
+
+def decode_summary(w, dec, peaks, link_gbs):
+    """Per-workload decode figures (component form)."""
     bx = ftsynth.expert_bytes(w["d"], w["f"], w["dtype"])
+    r = dict(workload=w["desc"], tok_s=round(dec["value"], 3), timed_tokens=dec["K"], warmup_tokens=dec["W"],
+             hit_rate=round(dec["hits"] / max(1.0, dec["hits"] + dec["misses"]), 4),
+             fills_per_token=round(dec["fills"] / (dec["K"] * dec["T"]), 3),
+             cpu_routes_per_token=round(dec["cpu"] / (dec["K"] * dec["T"]), 3), device_status=dec["status"])
+    ex_gbs, ex_how = experts_rate(dec)
+    if ex_gbs:
+        r["experts_gbs"] = round(ex_gbs, 1)
+        r["experts_frac_of_hbm"] = round(ex_gbs / peaks["hbm_gbs"], 4)
+        r["experts_how"] = ex_how
+    fill_gbs = fill_rate(dec)
+    if fill_gbs:
+        r["fill_gbs"] = round(fill_gbs, 1)
+        r["fill_frac_of_link"] = round(fill_gbs / link_gbs, 4) if link_gbs else None
+    r["decode_path"] = dec.get("path")
+    if "sequence" in dec:
+        r["sequence"] = dec["sequence"]
+    return r
+
+
+def build_line(args, w, world, dec, link, pre, ctl, peaks, comps=None):
+    """The bench line.  `link` is the host-link record (host_link_profile);
+    its whole-pool rate is the peak of the host-link fractions."""
+    link_gbs = link["whole_pool_gbs"] if link else 0.0
+    ex_gbs, ex_how = experts_rate(dec)
+    fill_gbs = fill_rate(dec)
+    fused = dec.get("path") == "fused"
+    m = dec.get("meters") or {}
+    if fused:
+        ex_per_launch = m.get("resident_bytes", 0.0) / max(1, m.get("resident_launches", 0))
+        ex_us = m.get("resident_s", 0.0) / max(1, m.get("resident_launches", 0)) * 1e6
+        traffic, traffic_src = ncu_traffic("decode_layer", ex_per_launch)
+    else:
+        ex_per_launch = dec.get("ex_bytes", 0.0) / max(1, dec.get("ex_n", 0))
+        ex_us = dec["ex_ms"] / max(1, dec.get("ex_n", 0)) * 1e3 if dec.get("ex_ms") else None
+        traffic, traffic_src = ncu_traffic("decode_experts" if w["dtype"] == 0 else "decode_experts_mxfp4",
+                                           ex_per_launch)
+    hits, misses = dec["hits"], dec["misses"]
+    cfg = line_config(args, w, world)
     line = {
         "metric": metric_name(args, w),
         "value": round(dec["value"], 3), "unit": "tok/s", "n_gpus": world, "steps": dec["K"],
         "warmup": dec["W"], "ms_per_step": round(dec["elapsed"] / dec["K"] * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w["dtype"] == 0 else "e2m1*e8m0 x bf16 -> f16/f32",
-        "data": "synthetic",
-        "config": {"workload": w["desc"], "graph": "one CUDA graph per token", "batch": dec["T"],
-                   "l2": "inputs larger than L2: %.2f GB of expert weights per token" % (w["L"] * w["k"] * bx / 1e9),
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "data": "synthetic", "config": cfg,
+        "timed_window": {"tokens": [dec["W"], dec["W"] + dec["K"]], "of_sequence": w["seq"],
+                         "hit_rate": round(hits / max(1.0, hits + misses), 4),
+                         "fills_per_token": round(dec["fills"] / (dec["K"] * dec["T"]), 3)},
         # the dominant kernel by time is the fill: host-link bound
-        "roofline": {"bound": "host_link", "kernel": "decode fill (host pool -> slots)", "achieved": round(fill_gbs, 1),
-                     "peak": round(link_gbs, 1), "unit": "GB/s", "frac": round(fill_gbs / link_gbs, 4) if link_gbs else None,
-                     "traffic": None, "peak_source": "measured in this run: 1.21 GB pinned H2D cudaMemcpyAsync, best of 3",
-                     "share": dec["shares"].get("fill")},
-        "roofline_experts": {"bound": "hbm", "kernel": "decode experts", "achieved": round(ex_gbs, 1),
-                             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ex_gbs / peaks["hbm_gbs"], 4),
-                             "traffic": round(NCU_TRAFFIC_RATIO["decode_experts" if w["dtype"] == 0 else "decode_experts_mxfp4"]
-                                              * dec["ex_bytes"] / max(1, dec["ex_n"])),
-                             "traffic_source": "ncu ratio x algorithmic bytes per launch", "peak_source": peaks["source"],
-                             "bytes_per_launch": round(dec["ex_bytes"] / max(1, dec["ex_n"])),
-                             "avg_launch_us": round(dec["ex_ms"] / max(1, dec["ex_n"]) * 1e3, 2),
-                             "share": dec["shares"].get("experts")},
+        "roofline": {"bound": "host_link",
+                     "kernel": "decode fill (host pool -> slots)" + (": the fill CTAs of the fused decode layer kernel"
+                                                                     if fused else ""),
+                     "achieved": round(fill_gbs, 1), "peak": link_gbs, "unit": "GB/s",
+                     "frac": round(fill_gbs / link_gbs, 4) if link_gbs else None, "traffic": None,
+                     "achieved_how": "bytes filled / summed fill spans (first fill CTA start to last fill CTA end, "
+                                     "device clock) over the timed window",
+                     "peak_source": "measured in this run: the whole pool streamed host -> device once in 1 GiB "
+                                    "copy-engine chunks",
+                     "share": dec.get("shares", {}).get("experts" if fused else "fill")},
+        "roofline_experts": {"bound": "hbm",
+                             "kernel": ("decode experts resident before the step (fused decode layer kernel, compute "
+                                        "CTAs)" if fused else "decode experts (in the step, beside the fill)"),
+                             "achieved": round(ex_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": round(ex_gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+                             "traffic_source": traffic_src, "peak_source": peaks["source"], "achieved_how": ex_how,
+                             "bytes_per_launch": round(ex_per_launch),
+                             "avg_us_per_launch": round(ex_us, 2) if ex_us else None,
+                             "share": dec.get("shares", {}).get("experts")},
         "components": {
-            "kernel_share": dec["shares"],
-            "kernel_ms_per_token": {n: round(v / dec["T"], 4) for n, v in dec["ms_per_token"].items()},
-            "route_control_us_per_layer_step": round(dec["control_us"], 3),
-            "hit_rate": round(dec["hits"] / max(1.0, dec["hits"] + dec["misses"]), 4),
+            "kernel_share": dec.get("shares"),
+            "kernel_ms_per_token": {n: round(v / dec["T"], 4) for n, v in dec.get("ms_per_token", {}).items()},
+            "route_control_us_per_layer_step_eager": round(dec["control_us"], 3) if "control_us" in dec else None,
+            "hit_rate": round(hits / max(1.0, hits + misses), 4),
             "fills_per_token": round(dec["fills"] / (dec["K"] * dec["T"]), 3),
             "cpu_routes_per_token": round(dec["cpu"] / (dec["K"] * dec["T"]), 3),
             "fills_per_step": round(dec["fills"] / dec["K"], 3), "tokens_per_step": dec["T"],
-            "eager_ms_per_token_profiled": round(dec["eager_ms"] / dec["T"], 4) if dec["eager_ms"] else None,
+            "eager_ms_per_token_profiled": round(dec["eager_ms"] / dec["T"], 4) if dec.get("eager_ms") else None,
             "init_pin_s": round(dec["t_init"], 2), "device_status": dec["status"],
         },
         "clocks": dec["clocks"],
-        "e2e": {"value": round(dec["e2e"], 3), "unit": "tok/s", "h2d_bytes_per_step": dec["h2d"],
-                "d2h_bytes_per_step": dec["d2h"]},
-        # per layer: route + control (one kernel), fill, resident experts, installed experts, merge
-        "gpu_launches": int(dec["K"] * w["L"] * 5),
+        # per layer: route + control (one kernel), then the fused decode layer kernel (fill + experts) and the
+        # merge, or on the split path the fill, the resident and installed expert launches and the merge
+        "gpu_launches": int(dec["K"] * w["L"] * (3 if fused else 5)),
     }
+    if "e2e" in dec:
+        line["e2e"] = {"value": round(dec["e2e"], 3), "unit": "tok/s", "h2d_bytes_per_step": dec["h2d"],
+                       "d2h_bytes_per_step": dec["d2h"]}
+        line["components"]["e2e_how"] = ("a twin context stepped through the same warm-up tokens times the same K "
+                                         "tokens with host copies; control streams identical: %s"
+                                         % dec.get("e2e_same_window"))
+    if "sequence" in dec:
+        line["components"]["sequence"] = dec["sequence"]
+    if link:
+        line["host_link"] = link
     if pre:
+        pre_link = pre.get("link_profile_gbs") or link_gbs
         line["prefill"] = {
             "workload": f"{pre['T']}-token chunk, A3B-style, {pre['L']} layers, full-layer double buffer",
             "chunk_s": round(pre["chunk_s"], 4), "chunk_s_single_buffer": round(pre["chunk_s_single_buffer"], 4),
             "loss_without_double_buffer": round(pre["overlap_loss_without_double_buffer"], 4),
             "tok_s": round(pre["T"] / pre["chunk_s"], 1), "pool_gb": round(pre["pool_bytes"] / 1e9, 2),
             "link_gbs_effective": round(pre["link_gbs"], 1), "upload_gbs": round(pre["upload_gbs"], 1),
-            "link_frac": round(pre["link_gbs"] / link_gbs, 4) if link_gbs else None,
-            "device_status": pre["status"],
+            "link_frac": round(pre["link_gbs"] / pre_link, 4) if pre_link else None,
+            "link_peak_gbs": pre_link, "device_status": pre["status"],
+            "link_peak_how": "the larger of two whole-pool host -> device streams, just before and just after the "
+                             "prefill leg", "link_around": pre.get("link_around"),
             "roofline_gemm": {"bound": "tensor", "kernel": "grouped SwiGLU GEMMs (tcgen05), weights resident",
                               "achieved": round(pre["gemm_tflops"], 1), "peak": peaks["bf16_tflops"],
                               "unit": "TFLOP/s", "frac": round(pre["gemm_tflops"] / peaks["bf16_tflops"], 4),
@@ -613,6 +1094,8 @@ def build_line(args, w, world, dec, link_gbs, pre, ctl, peaks):
             "workload": "control kernel alone, 48 layers x 64 tokens x top-8, E=128, Zipf routes, graph replay",
             "steps": args.control_steps, "cases": ctl,
         }
+    if comps:
+        line["components"].update(comps)
     return line
 
 
@@ -623,12 +1106,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--profile-steps", type=int, default=32)
-    ap.add_argument("--e2e-steps", type=int, default=128)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
-    ap.add_argument("--ref-budget-s", type=float, default=90.0)
+    ap.add_argument("--ref-budget-s", type=float, default=150.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-control", action="store_true")
+    ap.add_argument("--no-components", action="store_true", help="the headline decode leg only")
+    ap.add_argument("--no-v4", action="store_true", help="skip the V4 MXFP4 components")
     ap.add_argument("--prefill-tokens", type=int, default=8192)
     ap.add_argument("--prefill-layers", type=int, default=0)
     ap.add_argument("--control-steps", type=int, default=10000)
@@ -638,14 +1122,19 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="decode tokens per step (default 1)")
     ap.add_argument("--layers", type=int, default=0, help="override L (small profiling cases, not a bench line)")
     ap.add_argument("--slots", type=int, default=0, help="override S (small profiling cases, not a bench line)")
-    ap.add_argument("--sweep", choices=("capacity", "prompt"), default=None,
+    ap.add_argument("--sweep", choices=("capacity", "prompt", "fill"), default=None,
                     help="report mode (not the bench line): decode miss rate and tok/s over cache capacities of "
                          "5/10/25/50%% of the pool, or prefill chunk time over prompt lengths 4k/8k/16k with and "
-                         "without the double buffer")
+                         "without the double buffer; or decode on the split path and on the fused path with 19 to 76 "
+                         "fill CTAs")
     ap.add_argument("--ratio", default=None, help="r = BP/BH as NUM/DEN for the decode workload (default 1/1: every "
                     "miss filled)")
     ap.add_argument("--cpu-exec", type=int, default=0, help="variant: the context's CPU expert executor with this many "
                     "host threads computes the misses that are not filled (not the bench line)")
+    ap.add_argument("--decode-path", choices=("fused", "split"), default="fused",
+                    help="fused: one cooperative kernel per layer runs the fill and the experts (bf16); split: a "
+                         "fill kernel beside two expert launches")
+    ap.add_argument("--fill-ctas", type=int, default=0, help="fused path: CTAs that fill (0 = the library's choice)")
     ap.add_argument("--pool", choices=("pinned", "registered"), default="pinned",
                     help="pinned: pool written into ft_host_alloc memory; registered: pageable pool pinned by "
                          "ft_moe_init after the write")
@@ -659,26 +1148,26 @@ def main():
         w["desc"] = w["desc"].replace("batch 1, ", "") + f", batch {args.batch}"
     if args.workload == "v4":
         # keep the per-layer shapes; drop layers only if the host cannot hold the pinned pool
-        avail = 0
-        with open("/proc/meminfo") as fh:
-            for line in fh:
-                if line.startswith("MemAvailable:"):
-                    avail = int(line.split()[1]) * 1024
         per_layer = w["E"] * ftsynth.expert_bytes(w["d"], w["f"], 1)
-        fit = int(max(0, avail - (24 << 30)) // per_layer)
+        fit = int(max(0, host_available() - (24 << 30)) // per_layer)
         if fit < w["L"]:
             w["L"] = max(1, fit)
             w["desc"] += f" [host RAM holds {w['L']} of the 43 layers]"
-        args.no_prefill = args.no_control = True
+        args.no_prefill = args.no_control = args.no_components = True
     if args.ratio:
         num, den = (int(x) for x in args.ratio.split("/"))
         w["r"] = (num, den)
         w["desc"] = w["desc"].replace("BP/BH=1", f"BP/BH={num}/{den}")
     if args.cpu_exec:
         w["desc"] += f", CPU executor with {args.cpu_exec} host threads for the unfilled misses"
+    w["decode_path"] = 0 if args.decode_path == "fused" else 1
+    w["fill_ctas"] = args.fill_ctas
+    if args.decode_path == "split" or args.fill_ctas:
+        w["desc"] += f" [decode path {args.decode_path}" + (f", {args.fill_ctas} fill CTAs]" if args.fill_ctas else "]")
     if args.layers or args.slots:
         w["L"], w["S"] = args.layers or w["L"], args.slots or w["S"]
         w["desc"] += f" [profiling case: L={w['L']}, S={w['S']}]"
+        args.no_components = True
 
     if world > 1:
         import torch
@@ -689,7 +1178,7 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args, w)), flush=True)
+            print(json.dumps(run_reference(args, w, world)), flush=True)
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
@@ -714,11 +1203,15 @@ def main():
         run_sweep(args, w, world, local)
         return
     hp, pool, t_pool = make_host_pool(args, w)
-    hid, lg = decode_inputs(w, args.warmup + args.steps + min(args.steps, args.profile_steps)
-                            + min(args.steps, args.e2e_steps))
-    dec = run_decode_leg(args, w, world, local, pool, hid, lg)
-    pre = ctl = alone = None
-    link = 0.0
+    n_in = max(args.warmup + args.steps + min(args.steps, args.profile_steps), w["seq"])
+    hid, lg = decode_inputs(w, n_in)
+    seq = rank == 0 and not args.no_components
+    dec = run_decode_leg(args, w, world, local, pool, hid, lg, with_e2e=True, seq=seq)
+    # components time at most 128 tokens after at most 32 warm-up tokens
+    cargs = argparse.Namespace(**vars(args))
+    cargs.steps, cargs.warmup = min(args.steps, 128), min(args.warmup, 32)
+    pre = ctl = alone = link = None
+    comps = {}
     if rank == 0:
         import expert_cache_host_gb300 as ft
         # the pool is registered (pinned, mapped) for the measurement below by a throwaway context
@@ -726,18 +1219,35 @@ def main():
                              dtype=w["dtype"], num_slots=1, k_max=1, t_max=1)
         ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
         try:
-            link = link_peak_gbs(pool, w["E"] * ftsynth.expert_bytes(w["d"], w["f"], w["dtype"]))
+            link = host_link_profile(pool)
+            link["placement"] = pool_placement(pool)
         finally:
             ft.ft_moe_destroy(ctx)
-        if w["dtype"] == 0:
+        if w["dtype"] == 0 and not args.no_components:
             alone = experts_alone(w, pool, hid)
-        if not args.no_prefill and not args.layers:
-            pre = run_prefill_leg(args, w, pool)
-        if not args.no_control and not args.layers:
+            for rr in ((1, 2), (2, 1)):
+                wr_ = dict(w, r=rr, desc=w["desc"].replace("BP/BH=1", f"BP/BH={rr[0]}/{rr[1]}"))
+                d_r = run_decode_leg(cargs, wr_, 1, local, pool, hid, lg, with_e2e=False, seq=False)
+                comps[f"decode_r_{rr[0]}_{rr[1]}"] = decode_summary(wr_, d_r, measured_peaks(), link["whole_pool_gbs"])
+            comps["decode_adaptive_r"] = run_adaptive_leg(cargs, w, pool, hid, lg)
+            comps["route_control_graph"] = run_route_control_leg(w)
+            comps["tiny"] = run_tiny_leg()
+        if not args.no_prefill and not args.no_components:
+            ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
+            try:
+                before = host_link_profile(pool)
+                pre = run_prefill_leg(args, w, pool)
+                after = host_link_profile(pool)
+            finally:
+                ft.ft_moe_destroy(ctx)
+            pre["link_profile_gbs"] = max(before["whole_pool_gbs"], after["whole_pool_gbs"])
+            pre["link_around"] = {"before": before, "after": after}
+        if not args.no_control and not args.no_components:
             ctl = run_control_leg(args)
     peaks = measured_peaks()
+    line = None
     if rank == 0:
-        line = build_line(args, w, world, dec, link, pre, ctl, peaks)
+        line = build_line(args, w, world, dec, link, pre, ctl, peaks, comps)
         if alone:
             bx = ftsynth.expert_bytes(w["d"], w["f"], 0)
             t8 = alone[w["k"]]
@@ -748,19 +1258,66 @@ def main():
                 "frac": round(w["k"] * bx / t8 / 1e9 / peaks["hbm_gbs"], 4), "us": round(t8 * 1e6, 2),
                 "us_2_experts": round(alone[2] * 1e6, 2), "peak_source": peaks["source"]}
         if not args.no_cpu_baseline:
-            rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, args.cpu_budget_s,
-                                                     min_tokens=1.0 if w["T"] == 1 else 1.0 / w["L"])
+            rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, args.cpu_budget_s, min_layer_steps=1)
             line["cpu_baseline"] = {"value": round(rate, 5), "unit": "tok/s", "cores": threads, "kind": "oracle",
                                     "sample": f"{n:.2f} decode tokens x {w['L']} layers from a cold cache, "
                                               f"{t:.1f} s of oracle work"}
-        line["config"]["pool"] = (f"{args.pool}: {pool.nbytes / 1e9:.2f} GB, allocated and written in {t_pool:.1f} s")
-        print(json.dumps(line), flush=True)
+        line["components"]["pool"] = (f"{args.pool}: {pool.nbytes / 1e9:.2f} GB, allocated and written in "
+                                      f"{t_pool:.1f} s")
+    del hid, lg
     if hp:
         del pool
         hp.free()
+    if rank == 0 and not args.no_components and not args.no_v4:
+        line["components"]["v4"] = run_v4_components(cargs, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_v4_components(args, local):
+    """V4-Flash-style MXFP4 decode at batch 1 and 16, after the A3B pool is
+    freed: the 147 GB pool in ft_host_alloc memory (fewer layers only if the
+    host cannot hold it, said in the workload)."""
+    w = dict(V4)
+    per_layer = w["E"] * ftsynth.expert_bytes(w["d"], w["f"], 1)
+    fit = int(max(0, host_available() - (24 << 30)) // per_layer)
+    if fit < 1:
+        return {"unavailable": "host memory cannot hold one V4 layer"}
+    if fit < w["L"]:
+        w["L"] = fit
+        w["desc"] += f" [host RAM holds {w['L']} of the 43 layers]"
+    hp, pool, t_pool = make_host_pool(args, w)
+    out = {"pool": f"{pool.nbytes / 1e9:.2f} GB, allocated and written in {t_pool:.1f} s"}
+    try:
+        peaks = measured_peaks()
+        import expert_cache_host_gb300 as ft
+        cfg = ft.make_config(num_layers=w["L"], num_experts=w["E"], top_k=w["k"], hidden=w["d"], inter=w["f"],
+                             dtype=1, num_slots=1, k_max=1, t_max=1)
+        ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
+        try:
+            link = host_link_profile(pool)
+        finally:
+            ft.ft_moe_destroy(ctx)
+        out["host_link"] = link
+        for T in (1, 16):
+            wt = dict(w, T=T)
+            if T > 1:
+                wt["desc"] = wt["desc"] + f", batch {T}"
+            n_in = max(args.warmup + args.steps + min(args.steps, args.profile_steps), w["seq"] if T == 1 else 0)
+            hid, lg = decode_inputs(wt, n_in)
+            d = run_decode_leg(args, wt, 1, local, pool, hid, lg, with_e2e=False, seq=(T == 1))
+            s = decode_summary(wt, d, peaks, link["whole_pool_gbs"])
+            tr, note = ncu_traffic("decode_experts_mxfp4", d["ex_bytes"] / max(1, d["ex_n"]))
+            s["experts_traffic_per_launch"], s["experts_traffic_source"] = tr, note
+            out[f"batch_{T}"] = s
+            del hid, lg
+    finally:
+        del pool
+        hp.free()
+    return out
 
 
 if __name__ == "__main__":

@@ -23,6 +23,7 @@ FT_DTYPE_BF16, FT_DTYPE_MXFP4 = 0, 1
 FT_DECODE_CACHED, FT_PREFILL_LAYER = 0, 1
 FT_FILL_KERNEL, FT_FILL_COPY_ENGINE = 0, 1
 FT_FILL_ORDER_ID, FT_FILL_ORDER_MOST_ROUTED = 0, 1
+FT_DECODE_FUSED, FT_DECODE_SPLIT = 0, 1
 COUNTS = ("n", "hits", "m", "q", "cpu", "n_groups", "now")
 
 # Every symbol include/ft_moe.h declares.
@@ -31,6 +32,8 @@ EXPORTS = (
     "ft_get_status", "ft_get_counters", "ft_get_table", "ft_slot_ptr", "ft_get_epoch", "ft_num_slots", "ft_route",
     "ft_profile_enable", "ft_profile_read", "ft_decode_experts_noalloc", "ft_host_alloc", "ft_host_free", "ft_set_ratio",
     "ft_cache_rebuild_retain", "ft_cpu_executor", "ft_cpu_experts",
+    "ft_ratio_adapter_init", "ft_ratio_adapter_update", "ft_report_host_rate", "ft_measured_bandwidths",
+    "ft_adapt_ratio", "ft_decode_meters", "ft_decode_path",
     "ft_last_error",
 )
 FT_K_ROUTE, FT_K_CONTROL, FT_K_FILL, FT_K_EXPERTS, FT_K_MERGE, FT_K_UPLOAD, FT_K_PREFILL, FT_K_GEMM, FT_K_CPU = range(9)
@@ -51,8 +54,14 @@ class ft_config(ctypes.Structure):
         ("num_slots", ctypes.c_int32), ("k_max", ctypes.c_int32), ("t_max", ctypes.c_int32),
         ("r_num", ctypes.c_int32), ("r_den", ctypes.c_int32), ("prefill_buffers", ctypes.c_int32),
         ("prefill_t_max", ctypes.c_int32), ("fill_mode", ctypes.c_int32), ("fill_order", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("decode_path", ctypes.c_int32), ("fill_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1),
     ]
+
+
+class ft_ratio_adapter(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_double), ("r_den", ctypes.c_int32), ("r_num_max", ctypes.c_int32),
+                ("bp_gbs", ctypes.c_double), ("bh_gbs", ctypes.c_double), ("r_num", ctypes.c_int32),
+                ("updates", ctypes.c_int32)]
 
 
 class ft_step_out(ctypes.Structure):
@@ -98,6 +107,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "ft_cpu_executor": ([vp, i32], i32),
             "ft_cpu_experts": ([vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32], i32),
             "ft_host_free": ([vp], i32),
+            "ft_ratio_adapter_init": ([ctypes.POINTER(ft_ratio_adapter), ctypes.c_double, i32, i32], i32),
+            "ft_ratio_adapter_update": ([ctypes.POINTER(ft_ratio_adapter), ctypes.c_double, ctypes.c_double], i32),
+            "ft_report_host_rate": ([vp, ctypes.c_double, ctypes.c_double], i32),
+            "ft_measured_bandwidths": ([vp, vp, vp, i32], i32),
+            "ft_adapt_ratio": ([vp, ctypes.POINTER(ft_ratio_adapter), vp, vp], i32),
+            "ft_decode_meters": ([vp, vp, i32], i32),
+            "ft_decode_path": ([vp], i32),
             "ft_last_error": ([], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -195,6 +211,54 @@ def ft_slot_ptr(ctx: int, slot: int) -> int:
 
 def ft_set_ratio(ctx: int, r_num: int, r_den: int, stream: int = 0) -> None:
     _chk(load().ft_set_ratio(ctypes.c_void_p(ctx), r_num, r_den, ctypes.c_void_p(stream)))
+
+
+def ft_ratio_adapter_init(alpha: float, r_den: int = 256, r_num_max: int = 256 * 64) -> ft_ratio_adapter:
+    a = ft_ratio_adapter()
+    _chk(load().ft_ratio_adapter_init(ctypes.byref(a), alpha, r_den, r_num_max))
+    return a
+
+
+def ft_ratio_adapter_update(a: ft_ratio_adapter, bp_gbs: float, bh_gbs: float) -> int:
+    """1 if r_num changed, 0 if not."""
+    rc = load().ft_ratio_adapter_update(ctypes.byref(a), bp_gbs, bh_gbs)
+    if rc < 0:
+        _chk(rc)
+    return rc
+
+
+def ft_report_host_rate(ctx: int, nbytes: float, seconds: float) -> None:
+    _chk(load().ft_report_host_rate(ctypes.c_void_p(ctx), nbytes, seconds))
+
+
+def ft_measured_bandwidths(ctx: int, reset: bool = False):
+    """(BP, BH) in GB/s measured since the last reset (0 = no sample)."""
+    bp, bh = ctypes.c_double(), ctypes.c_double()
+    _chk(load().ft_measured_bandwidths(ctypes.c_void_p(ctx), ctypes.byref(bp), ctypes.byref(bh), int(reset)))
+    return bp.value, bh.value
+
+
+def ft_decode_meters(ctx: int, reset: bool = False) -> dict:
+    """Device-side decode meters since the last reset: fill bytes / seconds /
+    launches and resident-expert bytes / seconds / launches (fused path)."""
+    a = (ctypes.c_double * 6)()
+    _chk(load().ft_decode_meters(ctypes.c_void_p(ctx), a, int(reset)))
+    return dict(fill_bytes=a[0], fill_s=a[1], fill_launches=int(a[2]), resident_bytes=a[3], resident_s=a[4],
+                resident_launches=int(a[5]))
+
+
+def ft_decode_path(ctx: int) -> int:
+    rc = load().ft_decode_path(ctypes.c_void_p(ctx))
+    if rc < 0:
+        _chk(rc)
+    return rc
+
+
+def ft_adapt_ratio(ctx: int, a: ft_ratio_adapter, stream: int = 0) -> int:
+    """One adaptation step; 1 if r changed (and was set on `stream`), else 0."""
+    ch = ctypes.c_int()
+    _chk(load().ft_adapt_ratio(ctypes.c_void_p(ctx), ctypes.byref(a), ctypes.c_void_p(stream), ctypes.byref(ch)))
+    return ch.value
 
 
 def ft_cpu_executor(ctx: int, threads: int) -> None:

@@ -181,9 +181,10 @@ struct CpuScratch {
 namespace {
 
 // partial [T, d] (written) for the routes with slot_ids < 0 and an expert id
-// in [0, E); the other routes are the GPU's.
-void cpu_partial(const CpuModel& m, int layer, int T, const int32_t* ids, const float* w, const int32_t* slot_ids,
-                 const uint16_t* hidden, float* partial, WorkerPool& pool, CpuScratch& s) {
+// in [0, E); the other routes are the GPU's.  Returns the number of routes
+// computed (each reads its expert's B_x bytes once).
+int cpu_partial(const CpuModel& m, int layer, int T, const int32_t* ids, const float* w, const int32_t* slot_ids,
+                const uint16_t* hidden, float* partial, WorkerPool& pool, CpuScratch& s) {
   const int d = m.d, f = m.f, k = m.k;
   const size_t df = (size_t)d * f;
   s.rt.clear();
@@ -200,7 +201,7 @@ void cpu_partial(const CpuModel& m, int layer, int T, const int32_t* ids, const 
   const int nc = (int)s.rt.size();
   if (nc == 0) {
     memset(partial, 0, sizeof(float) * (size_t)T * d);
-    return;
+    return 0;
   }
   s.x.resize((size_t)T * d);
   for (size_t i = 0; i < (size_t)T * d; ++i) s.x[i] = bf16_value(hidden[i]);
@@ -253,6 +254,7 @@ void cpu_partial(const CpuModel& m, int layer, int T, const int32_t* ids, const 
       }
     }
   });
+  return nc;
 }
 
 }  // namespace
@@ -283,6 +285,9 @@ struct CpuExec {
   float* h_partial = nullptr;
   float* d_partial = nullptr;  // device view of h_partial
   std::vector<CpuJob> jobs;    // [L][t_max]: the host function's argument per (layer, T)
+  // host-side rate (the BH of the split): expert bytes read and compute time
+  // of the host functions that had routes to compute
+  std::atomic<unsigned long long> meter_bytes{0}, meter_ns{0}, meter_calls{0};
 };
 
 namespace {
@@ -290,7 +295,15 @@ namespace {
 void CUDART_CB cpu_job_fn(void* p) {
   const CpuJob* j = static_cast<const CpuJob*>(p);
   CpuExec* ex = j->ex;
-  cpu_partial(ex->m, j->layer, j->T, ex->h_ids, ex->h_w, ex->h_slot, ex->h_hidden, ex->h_partial, ex->pool, ex->s);
+  const auto t0 = std::chrono::steady_clock::now();
+  const int nc =
+      cpu_partial(ex->m, j->layer, j->T, ex->h_ids, ex->h_w, ex->h_slot, ex->h_hidden, ex->h_partial, ex->pool, ex->s);
+  if (nc > 0) {
+    const auto ns = std::chrono::duration_cast<std::chrono::nanoseconds>(std::chrono::steady_clock::now() - t0);
+    ex->meter_bytes += (unsigned long long)nc * ex->m.Bx;
+    ex->meter_ns += (unsigned long long)ns.count();
+    ex->meter_calls += 1;
+  }
 }
 
 }  // namespace
@@ -366,6 +379,19 @@ cudaError_t cpu_exec_fork(CpuExec* ex, int layer, int T, const int32_t* slot_ids
 cudaError_t cpu_exec_join(CpuExec* ex, cudaStream_t st) { return cudaStreamWaitEvent(st, ex->ev_join, 0); }
 
 const float* cpu_exec_partial(const CpuExec* ex) { return ex->d_partial; }
+
+void cpu_exec_meter(CpuExec* ex, unsigned long long* bytes, unsigned long long* ns, unsigned long long* calls,
+                    int reset) {
+  if (reset) {
+    *bytes = ex->meter_bytes.exchange(0);
+    *ns = ex->meter_ns.exchange(0);
+    *calls = ex->meter_calls.exchange(0);
+  } else {
+    *bytes = ex->meter_bytes.load();
+    *ns = ex->meter_ns.load();
+    *calls = ex->meter_calls.load();
+  }
+}
 
 }  // namespace ft
 

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -89,6 +90,16 @@ struct ft_ctx {
   PrefillState* prefill = nullptr;
   CpuExec* cpu = nullptr;  // host expert executor, or none
   Profiler prof;
+
+  FillMeter* meter = nullptr;  // device: [0] the decode fill's link rate, [1] the fused path's resident-expert phase
+
+  // fused decode path (FT_DECODE_FUSED): one CTA per SM, fill_ctas of them fill
+  bool fused = false;
+  int fused_ns = 0, fused_fill = 0, fused_groups = 0;
+  uint32_t* ready = nullptr;         // [K_max] clock stamp of each fetch entry's completed fill
+  unsigned int* fill_done = nullptr;  // [K_max] fill CTAs done with each entry
+  // host expert rate reported by the caller (ft_report_host_rate) since the last reset
+  double host_bytes = 0.0, host_s = 0.0;
 };
 
 namespace {
@@ -109,8 +120,9 @@ int check_config(const ft_config& c) {
     return fail(FT_E_ARG, "prefill_t_max must be in [1, 65536] when prefill_buffers > 0");
   if (c.fill_mode != FT_FILL_KERNEL && c.fill_mode != FT_FILL_COPY_ENGINE) return fail(FT_E_ARG, "bad fill_mode");
   if (c.fill_order != FT_FILL_ORDER_ID && c.fill_order != FT_FILL_ORDER_MOST_ROUTED) return fail(FT_E_ARG, "bad fill_order");
-  for (int i = 0; i < 3; ++i)
-    if (c.reserved[i]) return fail(FT_E_ARG, "reserved fields must be zero");
+  if (c.decode_path != FT_DECODE_FUSED && c.decode_path != FT_DECODE_SPLIT) return fail(FT_E_ARG, "bad decode_path");
+  if (c.fill_ctas < 0 || c.fill_ctas > 1024) return fail(FT_E_ARG, "fill_ctas must be in [0, 1024]");
+  if (c.reserved[0]) return fail(FT_E_ARG, "reserved fields must be zero");
   if ((long long)c.num_layers * c.num_experts > 0x7fffffffLL) return fail(FT_E_ARG, "too many experts");
   return FT_OK;
 }
@@ -169,6 +181,8 @@ int reset_table(ft_ctx* c) {
   CU(cudaMemset(c->expert_of, 0xFF, sizeof(int32_t) * c->S));
   CU(cudaMemset(c->last_use, 0, sizeof(uint32_t) * c->S));
   CU(cudaMemset(c->now, 0, sizeof(uint32_t)));
+  // the fused path's fill stamps hold clock values: the clock restarts, so must they
+  if (c->ready) CU(cudaMemset(c->ready, 0, sizeof(uint32_t) * c->cfg.k_max));
   CU(cudaMemset(c->counters, 0, sizeof(unsigned long long) * kCountersPerLayer * c->cfg.num_layers));
   for (auto& lb : c->layers) lb.last_T = -1;
   return FT_OK;
@@ -187,6 +201,9 @@ void free_all(ft_ctx* c) {
   cudaFree(c->counters);
   cudaFree(c->layer_mem);
   cudaFree(c->ypart);
+  cudaFree(c->meter);
+  cudaFree(c->ready);
+  cudaFree(c->fill_done);
   if (c->h_counts) cudaFreeHost(c->h_counts);
   if (c->h_fetch) cudaFreeHost(c->h_fetch);
   if (c->h_victims) cudaFreeHost(c->h_victims);
@@ -277,7 +294,7 @@ int enqueue_fill(ft_ctx* c, int layer, cudaStream_t st) {
     // one CTA per SM saturates the host link and leaves room on every SM for
     // the resident experts that run meanwhile
     CU(launch_fill(c->pool_dev, c->arena, lb.counts, lb.fetch, lb.victims, c->Bx, c->S, c->E_tot, c->status,
-                   c->sm_count, c->xfer));
+                   &c->meter[0], c->sm_count, c->xfer));
   } else {
     // Copy-engine fills need the fetch list on the host: this reads it back.
     CU(cudaMemcpyAsync(c->h_counts, lb.counts, sizeof(int32_t) * kCountsLen, cudaMemcpyDeviceToHost, c->xfer));
@@ -405,6 +422,36 @@ int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx
   if (cudaMemset(c->layer_mem, 0, per_layer * cfg->num_layers) != cudaSuccess ||
       cudaMemset(c->status, 0, sizeof(uint32_t)) != cudaSuccess)
     return bail(fail(FT_E_CUDA, "memset failed"));
+  {
+    const FillMeter m0[2] = {{~0ull, 0ull, 0ull, 0ull, 0ull, 0u, 0u}, {~0ull, 0ull, 0ull, 0ull, 0ull, 0u, 0u}};
+    if (cudaMalloc(&c->meter, sizeof(m0)) != cudaSuccess ||
+        cudaMemcpy(c->meter, m0, sizeof(m0), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMalloc(&c->ready, sizeof(uint32_t) * K) != cudaSuccess ||
+        cudaMalloc(&c->fill_done, sizeof(unsigned int) * K) != cudaSuccess ||
+        cudaMemset(c->ready, 0, sizeof(uint32_t) * K) != cudaSuccess ||
+        cudaMemset(c->fill_done, 0, sizeof(unsigned int) * K) != cudaSuccess) {
+      cudaGetLastError();
+      return bail(fail(FT_E_NOMEM, "meter / fill stamp allocation failed"));
+    }
+  }
+  // The fused decode path needs one CTA per SM with a ring of at least four
+  // stages; where that does not fit, the split path serves the context.
+  if (cfg->dtype == FT_DTYPE_BF16 && cfg->fill_mode == FT_FILL_KERNEL && cfg->decode_path == FT_DECODE_FUSED &&
+      cfg->hidden <= 8192) {
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+    const int mg = std::min(TK, E);
+    const int ns = decode_layer_ring_stages(cfg->hidden, mg, optin);
+    int per_sm = 0;
+    if (ns >= 4 && decode_layer_max_blocks_per_sm(cfg->hidden, ns, mg, &per_sm) == cudaSuccess && per_sm >= 1) {
+      c->fused = true;
+      c->fused_ns = ns;
+      c->fused_groups = mg;
+      const int want = cfg->fill_ctas ? cfg->fill_ctas : std::max(4, c->sm_count / 8);
+      c->fused_fill = std::min(want, c->sm_count - 1);
+    }
+    cudaGetLastError();
+  }
   if ((rc = reset_table(c))) return bail(rc);
 
   int lo = 0, hi = 0;
@@ -427,6 +474,12 @@ int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx
     c->prefill = prefill_create(pc, msg, sizeof(msg));
     if (!c->prefill) return bail(fail(FT_E_NOMEM, "prefill buffers: %s", msg));
   }
+  // Touch every 4 KB of the pool from the GPU once: the first GPU access to a
+  // host page can be far slower than the next ones, and fills and uploads
+  // should not pay it.  The meter's unused pad word is the loads' sink.
+  if (launch_touch(c->pool_dev, (size_t)c->E_tot * c->Bx, reinterpret_cast<int*>(&c->meter[0].pad), 2 * c->sm_count,
+                   0) != cudaSuccess)
+    return bail(fail(FT_E_CUDA, "pool touch launch failed"));
   if (cudaDeviceSynchronize() != cudaSuccess) return bail(fail(FT_E_CUDA, "initialisation failed"));
   *out = c;
   return FT_OK;
@@ -606,6 +659,51 @@ int ft_moe_forward(ft_ctx* c, int layer, int mode, const float* logits, const ui
     if (partial) return fail(FT_E_ARG, "partial_dev must be NULL while the CPU executor is enabled");
     CU(cpu_exec_fork(c->cpu, layer, T, lb.slot_ids, lb.ids_src, lb.w, hidden, st, c->prof));
   }
+  if (c->fused) {
+    LayerArgs la{};
+    DecodeArgs& a = la.d;
+    a.arena = c->arena;
+    a.Bx = c->Bx;
+    a.S = c->S;
+    a.d = c->cfg.hidden;
+    a.f = c->cfg.inter;
+    a.k = c->cfg.top_k;
+    a.dtype = c->cfg.dtype;
+    a.max_groups = c->fused_groups;
+    a.T = T;
+    a.counts = lb.counts;
+    a.group_slot = lb.group_slot;
+    a.group_off = lb.group_off;
+    a.group_routes = lb.group_routes;
+    a.group_new = lb.group_new;
+    a.hidden = hidden;
+    a.ypart = c->ypart;
+    a.status = c->status;
+    a.tmap_wd = &c->tmap_wd;
+    a.tmap_gu = &c->tmap_gu;
+    la.pool = reinterpret_cast<const int4*>(c->pool_dev);
+    la.fetch = lb.fetch;
+    la.victims = lb.victims;
+    la.E_tot = c->E_tot;
+    la.n_fill = c->fused_fill;
+    la.ns = c->fused_ns;
+    la.ready = c->ready;
+    la.fill_done = c->fill_done;
+    la.meter = &c->meter[0];
+    la.xmeter = &c->meter[1];
+    cudaEvent_t pb = c->prof.begin(st);
+    cudaError_t e = launch_decode_layer(la, c->sm_count, st);
+    if (e != cudaSuccess) return fail(FT_E_CUDA, "fused decode layer launch failed: %s", cudaGetErrorString(e));
+    c->prof.end(st, FT_K_EXPERTS, pb);
+    if (c->cpu) {
+      CU(cpu_exec_join(c->cpu, st));
+      partial = cpu_exec_partial(c->cpu);
+    }
+    pb = c->prof.begin(st);
+    CU(launch_merge(c->ypart, c->n_chunks, lb.slot_ids, lb.w, partial, out, T, c->cfg.top_k, c->cfg.hidden, st));
+    c->prof.end(st, FT_K_MERGE, pb);
+    return FT_OK;
+  }
   if ((rc = enqueue_fill(c, layer, st))) return rc;
   DecodeArgs a{};
   a.arena = c->arena;
@@ -700,6 +798,97 @@ int ft_get_table(ft_ctx* c, int32_t* slot_of, int32_t* expert_of, uint32_t* last
 void* ft_slot_ptr(ft_ctx* c, int slot) {
   if (!c || slot < 0 || slot >= c->S) return nullptr;
   return c->arena + (size_t)slot * c->Bx;
+}
+
+int ft_ratio_adapter_init(ft_ratio_adapter* a, double alpha, int32_t r_den, int32_t r_num_max) {
+  if (!a) return fail(FT_E_ARG, "null adapter");
+  if (!(alpha > 0.0 && alpha <= 1.0)) return fail(FT_E_ARG, "alpha must be in (0, 1]");
+  if (r_den < 1 || r_num_max < 0) return fail(FT_E_ARG, "r_den must be >= 1 and r_num_max >= 0");
+  *a = ft_ratio_adapter{};
+  a->alpha = alpha;
+  a->r_den = r_den;
+  a->r_num_max = r_num_max;
+  a->r_num = -1;
+  return FT_OK;
+}
+
+int ft_ratio_adapter_update(ft_ratio_adapter* a, double bp, double bh) {
+  if (!a || !(a->alpha > 0.0 && a->alpha <= 1.0) || a->r_den < 1 || a->r_num_max < 0)
+    return fail(FT_E_ARG, "adapter not initialised");
+  auto blend = [&](double est, double x) { return est > 0.0 ? a->alpha * x + (1.0 - a->alpha) * est : x; };
+  if (bp > 0.0) a->bp_gbs = blend(a->bp_gbs, bp);
+  if (bh > 0.0) a->bh_gbs = blend(a->bh_gbs, bh);
+  if (!(a->bp_gbs > 0.0 && a->bh_gbs > 0.0)) return 0;
+  // r = BP/BH on the grid 1/r_den, rounded half up, capped
+  const double x = (double)a->r_den * (a->bp_gbs / a->bh_gbs);
+  const double cap = (double)a->r_num_max;
+  const int32_t r = x + 0.5 >= cap ? a->r_num_max : (int32_t)floor(x + 0.5);
+  ++a->updates;
+  if (r == a->r_num) return 0;
+  a->r_num = r;
+  return 1;
+}
+
+int ft_report_host_rate(ft_ctx* c, double bytes, double seconds) {
+  if (!c) return fail(FT_E_ARG, "null context");
+  if (!(bytes >= 0.0) || !(seconds > 0.0)) return fail(FT_E_ARG, "bytes must be >= 0 and seconds > 0");
+  c->host_bytes += bytes;
+  c->host_s += seconds;
+  return FT_OK;
+}
+
+int ft_measured_bandwidths(ft_ctx* c, double* bp_gbs, double* bh_gbs, int reset) {
+  if (!c) return fail(FT_E_ARG, "null context");
+  CU(cudaDeviceSynchronize());
+  FillMeter m{};
+  CU(cudaMemcpy(&m, &c->meter[0], sizeof(m), cudaMemcpyDeviceToHost));
+  unsigned long long cb = 0, cns = 0, calls = 0;
+  if (c->cpu) cpu_exec_meter(c->cpu, &cb, &cns, &calls, reset);
+  const double hb = c->host_bytes + (double)cb, hs = c->host_s + (double)cns * 1e-9;
+  if (bp_gbs) *bp_gbs = m.ns ? (double)m.bytes / (double)m.ns : 0.0;  // bytes per ns = GB/s
+  if (bh_gbs) *bh_gbs = hs > 0.0 ? hb / hs / 1e9 : 0.0;
+  if (reset) {
+    // the three sums only: t0 / t1 / done hold their between-launch values here
+    const unsigned long long z[3] = {0ull, 0ull, 0ull};
+    CU(cudaMemcpy(&c->meter[0].bytes, z, sizeof(z), cudaMemcpyHostToDevice));
+    c->host_bytes = c->host_s = 0.0;
+  }
+  return FT_OK;
+}
+
+int ft_decode_meters(ft_ctx* c, double* out, int reset) {
+  if (!c || !out) return fail(FT_E_ARG, "null argument");
+  CU(cudaDeviceSynchronize());
+  FillMeter m[2];
+  CU(cudaMemcpy(m, c->meter, sizeof(m), cudaMemcpyDeviceToHost));
+  for (int i = 0; i < 2; ++i) {
+    out[3 * i + 0] = (double)m[i].bytes;
+    out[3 * i + 1] = (double)m[i].ns * 1e-9;
+    out[3 * i + 2] = (double)m[i].launches;
+  }
+  if (reset) {
+    const unsigned long long z[3] = {0ull, 0ull, 0ull};
+    for (int i = 0; i < 2; ++i) CU(cudaMemcpy(&c->meter[i].bytes, z, sizeof(z), cudaMemcpyHostToDevice));
+  }
+  return FT_OK;
+}
+
+int ft_decode_path(ft_ctx* c) { return c ? (c->fused ? FT_DECODE_FUSED : FT_DECODE_SPLIT) : fail(FT_E_ARG, "null context"); }
+
+int ft_adapt_ratio(ft_ctx* c, ft_ratio_adapter* a, void* stream, int* changed) {
+  if (!c || !a) return fail(FT_E_ARG, "null context or adapter");
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess ||
+      cs != cudaStreamCaptureStatusNone)
+    return fail(FT_E_STATE, "ft_adapt_ratio reads measurements back and cannot be captured");
+  double bp = 0.0, bh = 0.0;
+  int rc = ft_measured_bandwidths(c, &bp, &bh, 1);
+  if (rc) return rc;
+  rc = ft_ratio_adapter_update(a, bp, bh);
+  if (rc < 0) return rc;
+  if (changed) *changed = rc;
+  if (rc == 1) return ft_set_ratio(c, a->r_num, a->r_den, stream);
+  return FT_OK;
 }
 
 int ft_get_epoch(ft_ctx* c) { return c ? c->epoch : fail(FT_E_ARG, "null context"); }

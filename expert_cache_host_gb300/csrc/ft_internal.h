@@ -85,11 +85,24 @@ cudaError_t launch_control(const ControlArgs& a, cudaStream_t st);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, uint32_t* status,
                          int32_t* hist, cudaStream_t st);
 
+// Link rate of the decode fill, accumulated on the device: bytes copied and
+// the summed spans (first CTA start to last CTA end, ns) of the launches that
+// copied something.  t0 / t1 / done are one launch's working values (t0 =
+// ~0, t1 = 0, done = 0 between launches).
+struct FillMeter {
+  unsigned long long t0, t1, bytes, ns, launches;
+  unsigned int done, pad;
+};
+
 // Fill: copy counts[3] experts fetch[i] (global ids, pool offset id*Bx) into
-// arena slot victims[i].
+// arena slot victims[i]; adds the launch to *meter.
 cudaError_t launch_fill(const uint8_t* pool_dev, uint8_t* arena, const int32_t* counts, const int32_t* fetch,
-                        const int32_t* victims, size_t Bx, int S, int E_tot, uint32_t* status, int grid,
-                        cudaStream_t st);
+                        const int32_t* victims, size_t Bx, int S, int E_tot, uint32_t* status, FillMeter* meter,
+                        int grid, cudaStream_t st);
+
+// Read one 16-byte word of every 4 KB of the mapped host pool from the GPU
+// (pays the first-access cost of every page at start-up).
+cudaError_t launch_touch(const uint8_t* pool_dev, size_t bytes, int* sink, int grid, cudaStream_t st);
 
 struct DecodeArgs {
   const uint8_t* arena;  // slot s at arena + s*Bx
@@ -116,6 +129,29 @@ struct DecodeArgs {
 cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st);
 // MXFP4 experts; ypart is [T*k][f/kDecodeChunkFp4][d]; tokens = T of the step.
 cudaError_t launch_decode_experts_mxfp4(const DecodeArgs& a, int tokens, cudaStream_t st);
+
+// Fused decode layer (bf16): the step's fill and all of its experts in one
+// cooperative launch (decode_layer.cu).  CTAs [0, n_fill) fill, the rest
+// compute; ready[i] receives the step's clock once fetch entry i is in its
+// slot; fill_done[i] counts the fill CTAs done with entry i (0 between
+// launches).
+struct LayerArgs {
+  DecodeArgs d;
+  const int4* pool;  // device view of the mapped host pool
+  const int32_t* fetch;
+  const int32_t* victims;
+  int E_tot;
+  int n_fill;  // fill CTAs
+  int ns;      // ring stages of a compute CTA
+  uint32_t* ready;
+  unsigned int* fill_done;
+  FillMeter* meter;   // the fill CTAs' link rate
+  FillMeter* xmeter;  // the resident-expert phase: bytes, span from the first compute CTA start to the last resident item end
+};
+// Ring stages that fit one CTA per SM at hidden size d (0: none).
+int decode_layer_ring_stages(int d, int max_groups, int smem_optin);
+cudaError_t decode_layer_max_blocks_per_sm(int d, int ns, int max_groups, int* out);
+cudaError_t launch_decode_layer(const LayerArgs& la, int grid, cudaStream_t st);
 
 // out[t] = partial[t] + sum_j [slot_ids >= 0] w[t,j] * sum_c ypart[t*k+j][c]
 // Launch attributes for programmatic dependent launch: the kernel may start
@@ -204,5 +240,9 @@ cudaError_t cpu_exec_fork(CpuExec* ex, int layer, int T, const int32_t* slot_ids
                           const uint16_t* hidden, cudaStream_t st, Profiler& prof);
 cudaError_t cpu_exec_join(CpuExec* ex, cudaStream_t st);
 const float* cpu_exec_partial(const CpuExec* ex);
+// Expert bytes the executor's host functions read and the nanoseconds they
+// spent computing, since the last call with reset != 0.
+void cpu_exec_meter(CpuExec* ex, unsigned long long* bytes, unsigned long long* ns, unsigned long long* calls,
+                    int reset);
 
 }  // namespace ft

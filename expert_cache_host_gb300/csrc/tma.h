@@ -72,15 +72,23 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
   return done != 0;
 }
 
-// Bounded wait for the phase with parity `parity` to complete.
+// Bounded wait for the phase with parity `parity` to complete.  The clock is
+// read once every 64 tries only, so a wait that ends soon costs no timer reads.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, bool give_up = false) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try(a, parity)) return true;
   if (give_up) return false;
-  const uint64_t t0 = global_ns();
-  for (;;) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try(a, parity)) return true;
-    if (global_ns() - t0 > kWaitNs) return false;
+    if ((it & 63u) == 0) {
+      const uint64_t t = global_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > kWaitNs) {
+        return false;
+      }
+    }
   }
 }
 

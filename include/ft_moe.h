@@ -94,6 +94,18 @@ extern "C" {
 #define FT_FILL_KERNEL 0      /* SM copy from the mapped pool; graph capturable */
 #define FT_FILL_COPY_ENGINE 1 /* cudaMemcpyAsync per expert; reads the fetch list back (host sync) */
 
+/* How a decode step's fill and experts are launched (bf16 experts with
+ * FT_FILL_KERNEL; other configurations always take the split path):
+ *  FUSED  one cooperative kernel per layer, one CTA per SM: fill_ctas CTAs copy
+ *         the fetched experts from the host pool, the others run the experts
+ *         resident before the step and then each installed expert as soon as
+ *         its bytes are in its slot;
+ *  SPLIT  a fill kernel on the context's transfer stream beside an expert
+ *         launch for the resident experts, then a second expert launch for the
+ *         installed ones after the fill. */
+#define FT_DECODE_FUSED 0
+#define FT_DECODE_SPLIT 1
+
 typedef struct ft_config {
   int32_t num_layers;    /* L: MoE layers sharing the cache */
   int32_t num_experts;   /* E: routed experts per layer (<= 1024) */
@@ -109,7 +121,9 @@ typedef struct ft_config {
   int32_t prefill_t_max; /* tokens per prefill chunk (0 if no prefill) */
   int32_t fill_mode;     /* FT_FILL_KERNEL or FT_FILL_COPY_ENGINE */
   int32_t fill_order;    /* FT_FILL_ORDER_ID or FT_FILL_ORDER_MOST_ROUTED: which q of the m misses are filled */
-  int32_t reserved[3];   /* must be zero */
+  int32_t decode_path;   /* FT_DECODE_FUSED (default) or FT_DECODE_SPLIT */
+  int32_t fill_ctas;     /* fused path: CTAs that fill (0 = the library's choice) */
+  int32_t reserved[1];   /* must be zero */
 } ft_config;
 
 /* Per-layer results of ft_cache_step / ft_cache_control.  All pointers are
@@ -242,6 +256,76 @@ int ft_cache_rebuild_retain(ft_ctx* ctx, int new_slots);
  * by ft_profile_read or its own timing) and chooses r.
  * Errors: FT_E_ARG (r_num < 0 or r_den < 1), FT_E_CUDA. */
 int ft_set_ratio(ft_ctx* ctx, int32_t r_num, int32_t r_den, void* stream);
+
+/* ---- Run-time adaptation of r = BP/BH ----
+ * FreeToken article, section "设计：三大机制" 1, Decode bullet: the split of
+ * the misses between GPU fills and CPU execution follows the two bandwidths
+ * as measured while the system runs.  The context measures both itself:
+ *   BP  the decode fill kernel's link rate: bytes it copied from the host
+ *       pool over the summed spans of its launches (first CTA start to last
+ *       CTA end, device clock), launches that copied nothing excluded;
+ *   BH  the host expert rate: expert bytes the CPU executor read (B_x per
+ *       CPU route) over the time its host functions spent computing, plus
+ *       whatever the caller reports with ft_report_host_rate.
+ * The adapter below turns successive measurements into r; it is plain host
+ * state owned by the caller. */
+typedef struct ft_ratio_adapter {
+  double alpha;      /* weight of a new sample in the running estimates, in (0, 1] */
+  int32_t r_den;     /* r = r_num / r_den: the grid r is quantised to (>= 1) */
+  int32_t r_num_max; /* upper bound of r_num (>= 0) */
+  double bp_gbs;     /* running estimate of BP in GB/s, 0 = no sample yet */
+  double bh_gbs;     /* running estimate of BH in GB/s, 0 = no sample yet */
+  int32_t r_num;     /* r in effect is r_num / r_den; -1 until both estimates exist */
+  int32_t updates;   /* how many times r_num has been computed */
+} ft_ratio_adapter;
+
+/* Initialise an adapter: no estimates, r_num = -1.  Pure host code.
+ * Errors: FT_E_ARG (alpha outside (0, 1], r_den < 1 or r_num_max < 0). */
+int ft_ratio_adapter_init(ft_ratio_adapter* a, double alpha, int32_t r_den, int32_t r_num_max);
+
+/* Feed one measurement window.  A sample <= 0 means the window had none and
+ * leaves that estimate as it is; otherwise the estimate becomes the sample
+ * (the first one) or alpha*sample + (1 - alpha)*estimate.  Once both
+ * estimates exist, r_num = min(r_num_max, floor(r_den * bp/bh + 1/2)).
+ * Pure host code (no context, no GPU).  Returns 1 if r_num changed, 0 if not,
+ * FT_E_ARG for an adapter that was not initialised. */
+int ft_ratio_adapter_update(ft_ratio_adapter* a, double bp_sample_gbs, double bh_sample_gbs);
+
+/* Report host expert work done outside the context's CPU executor (a
+ * caller's own CPU engine): `bytes` of expert weights read in `seconds`.
+ * It counts toward BH until the next reset.  Errors: FT_E_ARG. */
+int ft_report_host_rate(ft_ctx* ctx, double bytes, double seconds);
+
+/* BP and BH (GB/s) measured since the last reset; 0 where the window had no
+ * sample (no fill copied anything, e.g. all hits or FT_FILL_COPY_ENGINE, which
+ * is not measured; no CPU route and nothing reported).  reset != 0 starts a
+ * new window.  Synchronises the device (reads device counters). */
+int ft_measured_bandwidths(ft_ctx* ctx, double* bp_gbs, double* bh_gbs, int reset);
+
+/* Device-side meters of the decode step since the last reset, as
+ * out[6] = {fill bytes, fill seconds, fill launches, resident-expert bytes,
+ * resident-expert seconds, fused launches with resident experts}.  The fill
+ * figures are those of BP above (first fill CTA start to last fill CTA end per
+ * launch that copied something).  The resident-expert figures come from the
+ * fused path only: per launch, the bytes of the experts resident before the
+ * step and the span from the first compute CTA start to the end of the last
+ * resident work item -- the experts' HBM-bound phase, which shares no SM with
+ * the fill.  reset != 0 clears them.  Synchronises.  Errors: FT_E_ARG,
+ * FT_E_CUDA. */
+int ft_decode_meters(ft_ctx* ctx, double* out, int reset);
+
+/* The decode path the context runs: FT_DECODE_FUSED, or FT_DECODE_SPLIT when
+ * that was asked for or the configuration has no fused kernel (MXFP4 experts,
+ * FT_FILL_COPY_ENGINE, a hidden size whose ring does not fit one CTA per SM). */
+int ft_decode_path(ft_ctx* ctx);
+
+/* One adaptation step, for use between decode steps: ft_measured_bandwidths
+ * with reset, ft_ratio_adapter_update, and -- if r_num changed --
+ * ft_set_ratio(ctx, a->r_num, a->r_den, stream), which graphs captured
+ * earlier see.  *changed (may be NULL) receives 1 or 0.  Synchronises; not
+ * allowed while `stream` is capturing (FT_E_STATE).  Errors: FT_E_ARG,
+ * FT_E_STATE, FT_E_CUDA. */
+int ft_adapt_ratio(ft_ctx* ctx, ft_ratio_adapter* a, void* stream, int* changed);
 
 /* Cache epoch: starts at 0, +1 per ft_cache_rebuild. */
 int ft_get_epoch(ft_ctx* ctx);

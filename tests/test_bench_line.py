@@ -28,11 +28,13 @@ def _dec(T=1, K=100):
 
 
 PEAKS = dict(hbm_gbs=6750.0, bf16_tflops=1960.0, bf16_tflops_sustained=1700.0, source="measured")
+LINK = {"whole_pool_gbs": 211.0, "chunks": 54, "chunk_gbs_min": 200.0, "chunk_gbs_median": 210.0,
+        "chunk_gbs_max": 211.5, "burst_first_1p21gb_gbs": 211.3}
 
 
 def test_line_has_the_contract_keys():
     w = dict(bench.A3B)
-    line = bench.build_line(_args(), w, 1, _dec(), 211.0, None, None, PEAKS)
+    line = bench.build_line(_args(), w, 1, _dec(), LINK, None, None, PEAKS)
     for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
               "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks"):
         assert k in line, k
@@ -51,7 +53,7 @@ def test_line_has_the_contract_keys():
 
 def test_per_token_counters_divide_by_the_batch():
     w = dict(bench.A3B, T=16)
-    line = bench.build_line(_args(), w, 1, _dec(T=16), 211.0, None, None, PEAKS)
+    line = bench.build_line(_args(), w, 1, _dec(T=16), LINK, None, None, PEAKS)
     c = line["components"]
     assert c["fills_per_step"] == pytest.approx(1.5)
     assert c["fills_per_token"] == pytest.approx(1.5 / 16, abs=1e-3)
@@ -64,3 +66,32 @@ def test_metric_names():
     v4 = bench.metric_name(_args(), dict(bench.V4))
     assert "V4-Flash-style MXFP4" in v4 and "batch 1" in v4
     assert "CPU expert executor" in bench.metric_name(_args(cpu_exec=8), dict(bench.A3B))
+
+
+def test_timed_window_and_host_link_are_reported():
+    w = dict(bench.A3B)
+    line = bench.build_line(_args(), w, 1, _dec(), LINK, None, None, PEAKS)
+    tw = line["timed_window"]
+    assert tw["tokens"] == [8, 108] and tw["hit_rate"] == pytest.approx(0.8)
+    assert line["host_link"]["whole_pool_gbs"] == 211.0 and line["roofline"]["peak"] == 211.0
+    # the config object is the workload alone (the reference arm prints the same one)
+    assert line["config"] == bench.line_config(_args(), w, 1)
+
+
+def test_traffic_is_null_once_the_kernel_source_changes(monkeypatch):
+    t, note = bench.ncu_traffic("decode_experts", 1.0e8)
+    assert t is None or t == round(bench.NCU_TRAFFIC["decode_experts"]["ratio"] * 1.0e8)
+    monkeypatch.setitem(bench.NCU_TRAFFIC, "decode_experts", dict(bench.NCU_TRAFFIC["decode_experts"], sha16="0" * 16))
+    t, note = bench.ncu_traffic("decode_experts", 1.0e8)
+    assert t is None and "changed" in note
+
+
+def test_reference_arm_prints_the_same_config_and_integer_steps():
+    """The oracle as the reference arm, on a tiny workload so it runs here."""
+    w = dict(bench.A3B, L=2, E=16, k=2, d=256, f=128, S=8, K_max=16, desc="tiny decode")
+    args = _args(steps=4, warmup=3, ref_budget_s=30.0)
+    ref = bench.run_reference(args, w, 1)
+    assert ref["impl"] == "reference" and ref["steps"] == 4 and isinstance(ref["steps"], int)
+    assert ref["warmup"] == 3 and ref["config"] == bench.line_config(args, w, 1)
+    assert ref["metric"] == bench.metric_name(args, w) and ref["unit"] == "tok/s" and ref["value"] > 0
+    assert set(ref["e2e"]) == {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}

@@ -90,7 +90,7 @@ def test_cache_step_routes_and_nan(ft, T, E, k):
 # ------------------------------------------------------------------ decode steps
 
 def run_decode(ft, model, S, K_max, r, steps, T=1, fill_mode=0, check_every=1, out_tokens=None, rho=0.9,
-               rebuild_at=None, graph=False, r_at=None, fill_order=0, cpu_exec=0):
+               rebuild_at=None, graph=False, r_at=None, fill_order=0, cpu_exec=0, decode_path=0, fill_ctas=0):
     """Decode `steps` steps over all layers through the library and the oracle
     side by side; compare control state every step and outputs every
     `check_every` steps.  r_at: {step: (r_num, r_den)} changes r (ft_set_ratio)
@@ -98,9 +98,12 @@ def run_decode(ft, model, S, K_max, r, steps, T=1, fill_mode=0, check_every=1, o
     many threads) computes the CPU routes' partial sum; no partial is passed."""
     L, E, k, d, f = model.L, model.E, model.k, model.d, model.f
     cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, dtype=model.dtype, num_slots=S,
-                         k_max=K_max, t_max=T, r_num=r[0], r_den=r[1], fill_mode=fill_mode, fill_order=fill_order)
+                         k_max=K_max, t_max=T, r_num=r[0], r_den=r[1], fill_mode=fill_mode, fill_order=fill_order,
+                         decode_path=decode_path, fill_ctas=fill_ctas)
     ctx = ft.ft_moe_init(cfg, model.pool.ctypes.data, model.pool.nbytes)
     try:
+        if model.dtype == 0 and fill_mode == 0:
+            assert ft.ft_decode_path(ctx) == decode_path
         if cpu_exec:
             ft.ft_cpu_executor(ctx, cpu_exec)
             check_every = 1
@@ -169,11 +172,15 @@ def test_tiny_decode_all_fill(ft):
     ft.ft_moe_destroy(ctx)
 
 
+PATHS = [0, 1]  # FT_DECODE_FUSED, FT_DECODE_SPLIT
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("r,K_max", [((1, 2), 16), ((1, 1), 1), ((0, 1), 4)])
-def test_tiny_decode_cpu_split(ft, r, K_max):
+def test_tiny_decode_cpu_split(ft, r, K_max, path):
     """Misses left to the CPU arrive as an external partial sum and merge exactly."""
     model = make_model(2, 16, 2, 256, 128, seed=1)
-    ctx, cache, worst = run_decode(ft, model, S=6, K_max=K_max, r=r, steps=20)
+    ctx, cache, worst = run_decode(ft, model, S=6, K_max=K_max, r=r, steps=20, decode_path=path)
     cnt = ft.ft_get_counters(ctx, 2)
     assert cnt[:, 3].sum() > 0  # some routes did go to the CPU
     ft.ft_moe_destroy(ctx)
@@ -205,19 +212,22 @@ def test_tiny_decode_copy_engine_fill(ft):
     ft.ft_moe_destroy(ctx)
 
 
-def test_batch16_decode_groups(ft):
+@pytest.mark.parametrize("path", PATHS)
+def test_batch16_decode_groups(ft, path):
     """16 tokens per step: tokens share experts, so groups hold several routes."""
     model = make_model(2, 16, 4, 256, 256, seed=3)
-    ctx, _, _ = run_decode(ft, model, S=12, K_max=8, r=(1, 1), steps=6, T=16)
+    ctx, _, _ = run_decode(ft, model, S=12, K_max=8, r=(1, 1), steps=6, T=16, decode_path=path)
     ft.ft_moe_destroy(ctx)
 
 
-@pytest.mark.parametrize("d,f,T,k", [(512, 256, 1, 2), (1024, 128, 16, 4), (768, 128, 4, 2), (2048, 128, 16, 8)])
-def test_decode_shapes(ft, d, f, T, k):
-    """Hidden sizes of 2, 3, 4 and 8 column blocks, f of 4 to 8 chunks, and
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("d,f,T,k", [(512, 256, 1, 2), (1024, 128, 16, 4), (768, 128, 4, 2), (2048, 128, 16, 8),
+                                     (8192, 128, 2, 2)])
+def test_decode_shapes(ft, d, f, T, k, path):
+    """Hidden sizes of 2, 3, 4, 8 and 32 column blocks, f of 4 to 8 chunks, and
     T = 16, which puts several token batches through one CTA."""
     model = make_model(2, 16, k, d, f, seed=7 + d)
-    ctx, _, _ = run_decode(ft, model, S=max(6, 2 * k), K_max=16, r=(1, 1), steps=5, T=T)
+    ctx, _, _ = run_decode(ft, model, S=max(6, 2 * k), K_max=16, r=(1, 1), steps=5, T=T, decode_path=path)
     ft.ft_moe_destroy(ctx)
 
 
@@ -242,10 +252,13 @@ def test_rebuild_retain_mid_run(ft, new_S):
     ft.ft_moe_destroy(ctx)
 
 
-def test_ragged_shapes_and_larger_model(ft):
-    """d=2048, f=768 (24 chunks), E=128, top-8: the A3B expert shape, 3 layers."""
+@pytest.mark.parametrize("path,fill_ctas", [(0, 0), (0, 1), (0, 150), (1, 0)])
+def test_ragged_shapes_and_larger_model(ft, path, fill_ctas):
+    """d=2048, f=768 (24 chunks), E=128, top-8: the A3B expert shape, 3 layers;
+    the fused path with the default number of fill CTAs, with one, and with
+    all but one or two of the grid."""
     model = make_model(3, 128, 8, 2048, 768, seed=5)
-    ctx, _, worst = run_decode(ft, model, S=20, K_max=128, r=(1, 2), steps=4)
+    ctx, _, worst = run_decode(ft, model, S=20, K_max=128, r=(1, 2), steps=4, decode_path=path, fill_ctas=fill_ctas)
     ft.ft_moe_destroy(ctx)
 
 
@@ -336,12 +349,18 @@ def test_mxfp4_decode_v4_expert_shape(ft):
 
 # ------------------------------------------------------------------ mixed hit / fill steps
 
-def test_mixed_steps_a3b_expert_shape(ft):
+@pytest.mark.parametrize("path", PATHS)
+def test_mixed_steps_a3b_expert_shape(ft, path):
     """A3B expert shape over steps that both hit and fill: the resident experts
-    stream from HBM through the TMA ring while the fill kernel shares their SMs
-    (a ring stage must not be refilled before its ordinary loads are done)."""
+    stream from HBM through the TMA ring while the fill shares the GPU (split
+    path: the same SMs; fused path: installed experts start as soon as their
+    own bytes are in the slot), and every slot's bytes equal the pool's."""
     model = make_model(2, 128, 8, 2048, 768, seed=32)
-    ctx, cache, _ = run_decode(ft, model, S=20, K_max=128, r=(1, 1), steps=6)
+    ctx, cache, _ = run_decode(ft, model, S=20, K_max=128, r=(1, 1), steps=6, decode_path=path)
+    if path == 0:
+        m = ft.ft_decode_meters(ctx)
+        assert m["fill_launches"] > 0 and m["fill_bytes"] > 0 and m["fill_s"] > 0
+        assert m["resident_launches"] > 0 and m["resident_bytes"] > 0 and m["resident_s"] > 0
     so, eo, lu, now = ft.ft_get_table(ctx, 256, 20)
     bx = model.bx
     for s in range(20):
@@ -371,15 +390,17 @@ def test_decode_from_host_alloc_pool(ft):
 
 # ------------------------------------------------------------------ CUDA graph replay
 
-def test_graph_replay_matches_oracle(ft):
+@pytest.mark.parametrize("path", PATHS)
+def test_graph_replay_matches_oracle(ft, path):
     """One decode step of every layer captured once as a CUDA graph and
     replayed with new inputs: control state and outputs equal the oracle's at
-    every replay; an ft_set_ratio between replays is seen by the graph."""
+    every replay; an ft_set_ratio between replays is seen by the graph (the
+    fused path is a cooperative kernel node)."""
     L, E, k, d, f, T, S, K_max = 2, 16, 2, 256, 128, 1, 6, 16
     model = make_model(L, E, k, d, f, seed=9)
     steps, r = 8, (1, 1)
     cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, num_slots=S, k_max=K_max, t_max=T,
-                         r_num=r[0], r_den=r[1])
+                         r_num=r[0], r_den=r[1], decode_path=path)
     ctx = ft.ft_moe_init(cfg, model.pool.ctypes.data, model.pool.nbytes)
     try:
         cache = oracle.Cache(L * E, S)
