@@ -1131,6 +1131,9 @@ def main():
                     "miss filled)")
     ap.add_argument("--cpu-exec", type=int, default=0, help="variant: the context's CPU expert executor with this many "
                     "host threads computes the misses that are not filled (not the bench line)")
+    ap.add_argument("--repeat-tokens", action="store_true",
+                    help="profiling case (not a bench line): every decode token's inputs twice in a row, so the "
+                         "second pass hits on every expert and runs with no fill")
     ap.add_argument("--decode-path", choices=("fused", "split"), default="fused",
                     help="fused: one cooperative kernel per layer runs the fill and the experts (bf16); split: a "
                          "fill kernel beside two expert launches")
@@ -1205,6 +1208,11 @@ def main():
     hp, pool, t_pool = make_host_pool(args, w)
     n_in = max(args.warmup + args.steps + min(args.steps, args.profile_steps), w["seq"])
     hid, lg = decode_inputs(w, n_in)
+    if args.repeat_tokens:
+        hid = np.ascontiguousarray(np.repeat(hid[:(n_in + 1) // 2], 2, axis=0)[:n_in])
+        lg = np.ascontiguousarray(np.repeat(lg[:(n_in + 1) // 2], 2, axis=0)[:n_in])
+        w["desc"] += " [profiling case: every token twice]"
+        args.no_components = True
     seq = rank == 0 and not args.no_components
     dec = run_decode_leg(args, w, world, local, pool, hid, lg, with_e2e=True, seq=seq)
     # components time at most 128 tokens after at most 32 warm-up tokens

@@ -3,28 +3,30 @@
 //
 // FreeToken article, section "设计：三大机制" 1, Decode bullet: the q filled
 // experts are copied from the host pool into their cache slots and then run on
-// the GPU beside the experts that were already resident.  Here the two happen
-// in one grid with the SMs split by role:
-//  - fill CTAs (the first n_fill) stream the fetched experts from the mapped
+// the GPU beside the experts that were already resident.  Here both happen in
+// one grid:
+//  - fill: the first n_fill CTAs stream the fetched experts from the mapped
 //    pinned pool into their victim slots, expert after expert; when the last
-//    fill CTA finishes its share of fetch entry i it publishes ready[i] = the
+//    of them finishes its share of fetch entry i it publishes ready[i] = the
 //    step's clock (release);
-//  - compute CTAs (the rest) run the same per-(expert, 32-row chunk) SwiGLU
-//    GEMV as the split decode kernel -- TMA ring of 16 KB tiles, fp32
-//    accumulation, one partial sum per (route, chunk) for the merge -- over a
-//    persistent list of work items: first every chunk of every expert that was
-//    resident before the step, then the chunks of each installed expert in
-//    fill order.  Before the first tile of an installed expert the producer
-//    warp waits (bounded, %globaltimer) for its ready stamp, so an installed
-//    expert starts as soon as its own bytes have landed, from L2.
-// The control kernel lists groups by ascending expert and the fetch list is
-// ascending too, so the j-th installed group is fetch entry j.
-//
-// The ring keeps running across a CTA's items, so only the first tile of the
-// launch pays the TMA latency; one CTA per SM leaves room for a deep ring.
-// Blocks of one cooperative launch are resident together, so the waits of
-// compute CTAs on fill CTAs always end; every wait is also bounded in time
-// and a wait that runs out records FT_ST_TIMEOUT and carries on.
+//  - experts: every CTA (the fill CTAs once their share is written) takes work
+//    items from a device-wide counter.  An item is one expert and 32 rows of
+//    f: the same per-chunk SwiGLU GEMV as the split decode kernel --
+//        h[t, i] = silu(W_gate[i] . x_t) * (W_up[i] . x_t)   i in the chunk
+//        ypart[route(t), chunk, :] = W_down[:, chunk] . h[t, chunk]
+//    -- with fp32 accumulation and one partial sum per (route, chunk) for the
+//    merge.  Items come in the order: every chunk of every expert resident
+//    before the step, then the chunks of each installed expert in fill order
+//    (the control kernel lists groups by ascending expert and the fetch list
+//    is ascending too, so the j-th installed group is fetch entry j).  Before
+//    the first tile of an installed expert's item the producer waits (bounded,
+//    %globaltimer) for its ready stamp, so it starts as soon as its own bytes
+//    have landed, from L2.  Fill CTAs do not wait on anything, so every wait
+//    ends; a wait that runs out records FT_ST_TIMEOUT and carries on.
+// Each CTA's producer warp takes the next item when its ring has room and
+// passes the index to the consumers through shared memory, published by the
+// mbarrier of the item's first stage; the TMA ring (up to 12 16 KB stages)
+// runs across a CTA's items, two stages per consumer iteration.
 #include <math.h>
 
 #include "decode_bf16.cuh"
@@ -37,10 +39,12 @@ namespace {
 constexpr int FC = kDecodeChunk;           // 32 rows of f per item
 constexpr int kConsumers = 512;            // 16 consumer warps
 constexpr int kThreads = kConsumers + 32;  // + 1 producer warp
-constexpr int kTokBatch = 4;               // tokens per pass over the weights
+constexpr int kQueue = 16;                 // item indices in flight between producer and consumers (> stages)
+constexpr int kMaxGroupsWarp = 64;         // groups whose values warp 0 fetches in its first round trip
 constexpr int kTile = 16384;               // bytes per ring stage
 constexpr int kXPre = 2;                   // uint4 of a hidden row per consumer (d <= 8192)
 constexpr int kFillUnroll = 16;            // 16-byte host loads in flight per fill thread
+constexpr int kCtasPerSm = 1;              // CTAs of the grid on each SM (two measured no faster, with spills)
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
@@ -59,20 +63,21 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
 __device__ __forceinline__ void proxy_fence_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 struct Layout {
-  size_t ring, full, empty, xs, gu, hs, rs, lists, total;
+  size_t ring, full, empty, xs, gu, hs, queue, lists, total;
 };
 
-__host__ __device__ inline Layout smem_layout(int d, int ns, int max_groups) {
+// TB: tokens per pass over the weights (1 for one-token steps, else 4).
+__host__ __device__ inline Layout smem_layout(int d, int ns, int max_groups, int TB) {
   Layout L{};
   L.ring = 0;
   L.full = L.ring + (size_t)ns * kTile;
   L.empty = L.full + 8 * (size_t)ns;
-  L.xs = (L.empty + 8 * (size_t)ns + 15) / 16 * 16;
-  L.gu = L.xs + (size_t)kTokBatch * d * 2;           // [2][FC][kTokBatch] row sums
-  L.hs = L.gu + sizeof(float) * 2 * FC * kTokBatch;  // [kTokBatch][FC]
-  L.rs = L.hs + sizeof(float) * kTokBatch * FC;      // [kTokBatch]
-  L.lists = L.rs + sizeof(int) * kTokBatch;          // [2] counts, then resident / installed group lists
-  L.total = L.lists + sizeof(int) * (2 + 2 * (size_t)max_groups);
+  L.xs = (L.empty + 8 * (size_t)ns + 15) / 16 * 16;  // [TB][d] bf16 hidden rows
+  L.gu = L.xs + (size_t)TB * d * 2;                   // [2][FC][TB] row sums
+  L.hs = L.gu + sizeof(float) * 2 * FC * TB;          // [TB][FC] h of the chunk
+  L.queue = L.hs + sizeof(float) * TB * FC;           // [kQueue] items, producer -> consumers
+  L.lists = L.queue + sizeof(int) * kQueue;           // [2] counts, group lists, group slots, group offsets
+  L.total = L.lists + sizeof(int) * (2 + 4 * (size_t)max_groups + 1);
   return L;
 }
 
@@ -135,41 +140,29 @@ __device__ void fill_role(const LayerArgs& la) {
 
 // ---------------------------------------------------------------- the kernel
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int TB>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     decode_layer_bf16_kernel(const __grid_constant__ CUtensorMap tmap_gu, const __grid_constant__ CUtensorMap tmap_wd,
                              const LayerArgs la) {
-  if ((int)blockIdx.x < la.n_fill) {
-    fill_role(la);
-    return;
-  }
   const DecodeArgs& a = la.d;
   extern __shared__ __align__(1024) unsigned char dyn[];
   const int d = a.d, f = a.f, ns = la.ns;
-  const Layout Ly = smem_layout(d, ns, a.max_groups);
+  const Layout Ly = smem_layout(d, ns, a.max_groups, TB);
   unsigned char* ring = dyn + Ly.ring;
   uint64_t* full = reinterpret_cast<uint64_t*>(dyn + Ly.full);
   uint64_t* empty = reinterpret_cast<uint64_t*>(dyn + Ly.empty);
-  uint16_t* xs = reinterpret_cast<uint16_t*>(dyn + Ly.xs);  // [kTokBatch][d]
-  float* gu = reinterpret_cast<float*>(dyn + Ly.gu);        // [2][FC][kTokBatch]
-  float* hs = reinterpret_cast<float*>(dyn + Ly.hs);        // [kTokBatch][FC]
-  int* rs = reinterpret_cast<int*>(dyn + Ly.rs);            // [kTokBatch]
-  int* nlist = reinterpret_cast<int*>(dyn + Ly.lists);      // [0] resident, [1] installed
-  int* res = nlist + 2;                                     // resident groups, ascending
-  int* inst = res + a.max_groups;                           // installed groups = fetch order
+  uint16_t* xs = reinterpret_cast<uint16_t*>(dyn + Ly.xs);  // [TB][d]
+  float* gu = reinterpret_cast<float*>(dyn + Ly.gu);        // [2][FC][TB]
+  float* hs = reinterpret_cast<float*>(dyn + Ly.hs);        // [TB][FC]
+  volatile int* queue = reinterpret_cast<int*>(dyn + Ly.queue);
+  int* nlist = reinterpret_cast<int*>(dyn + Ly.lists);  // [0] resident, [1] installed
+  int* res = nlist + 2;                                 // resident groups, ascending
+  int* inst = res + a.max_groups;                       // installed groups = fetch order
+  int* gslot = inst + a.max_groups;                     // [max_groups] slot of each group
+  int* goff = gslot + a.max_groups;                     // [max_groups + 1] route offsets of the groups
 
   const int tid = threadIdx.x, lane = tid & 31;
-  const int C = gridDim.x - la.n_fill, ci = blockIdx.x - la.n_fill;
   if (tid == 0) atomicMin(&la.xmeter->t0, (unsigned long long)global_ns());
-  const bool one_tok = a.T == 1;
-  uint4 xpre[kXPre];
-  if (one_tok && tid < kConsumers) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.hidden);
-#pragma unroll
-    for (int j = 0; j < kXPre; ++j) {
-      const int i = tid + j * kConsumers;
-      if (i < d / 8) xpre[j] = ld_nc_early(src + i);
-    }
-  }
   if (tid == kConsumers) {
     for (int s = 0; s < ns; ++s) {
       mbar_init(&full[s], 1);
@@ -177,62 +170,118 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init_fence();
   }
-  // work lists: warp 0 splits the groups into resident and installed, in order
+  if ((int)blockIdx.x < la.n_fill) {
+    fill_role(la);  // then join the expert work below
+    __syncthreads();
+  }
+  // the producer's first item: taken now, so the counter's round trip overlaps the prologue
+  int first_item = 0;
+  if (tid == kConsumers) first_item = (int)atomicAdd(&la.sched[0], 1u);
+  // one token: every route reads hidden row 0, fetched while the lists are built
+  uint4 xpre[kXPre];
+  if (TB == 1 && tid < kConsumers) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.hidden);
+#pragma unroll
+    for (int j = 0; j < kXPre; ++j) {
+      const int i = tid + j * kConsumers;
+      if (i < d / 8) xpre[j] = ld_nc_early(src + i);
+    }
+  }
+  // work lists: warp 0 splits the groups into resident and installed, in order,
+  // and keeps each group's slot and route offsets in shared memory.  The group
+  // arrays hold max_groups (+1) entries, so every group's values are read in
+  // the same round trip as the group count.
   if (tid < 32) {
-    const int n_groups = min(a.counts[5], a.max_groups);
+    constexpr int NW = kMaxGroupsWarp / 32;
+    const int mg = a.max_groups;
+    int cnt = 0, nw[NW], sl[NW], of[NW];
+    if (lane == 0) cnt = a.counts[5];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      const int g = i * 32 + lane;
+      nw[i] = g < mg ? a.group_new[g] : 0;
+      sl[i] = g < mg ? a.group_slot[g] : 0;
+      of[i] = g <= mg ? a.group_off[g] : 0;
+    }
+    const int n_groups = min(__shfl_sync(0xffffffffu, cnt, 0), mg);
     int nr = 0, ni = 0;
-    for (int base = 0; base < n_groups; base += 32) {
-      const int g = base + lane;
+    auto place = [&](int g, int isn, int slot, int off) {
       const bool in = g < n_groups;
-      const bool isnew = in && a.group_new[g] != 0;
+      const bool isnew = in && isn != 0;
       const unsigned bn = __ballot_sync(0xffffffffu, isnew), br = __ballot_sync(0xffffffffu, in && !isnew);
       const unsigned below = (1u << lane) - 1u;
       if (isnew) inst[ni + __popc(bn & below)] = g;
       else if (in) res[nr + __popc(br & below)] = g;
       ni += __popc(bn);
       nr += __popc(br);
+      if (in) {
+        gslot[g] = slot;
+        goff[g] = off;
+      }
+    };
+#pragma unroll
+    for (int i = 0; i < NW; ++i)
+      if (i * 32 < n_groups) place(i * 32 + lane, nw[i], sl[i], of[i]);
+    for (int base = NW * 32; base < n_groups; base += 32) {  // more groups than the first round trip fetched
+      const int g = base + lane;
+      const bool in = g < n_groups;
+      place(g, in ? a.group_new[g] : 0, in ? a.group_slot[g] : 0, in ? a.group_off[g] : 0);
+    }
+    // the end offset of the last group: already held by lane n_groups % 32 of the first fetch
+    int end_off = 0;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      const int v = __shfl_sync(0xffffffffu, of[i], n_groups & 31);
+      if ((n_groups >> 5) == i) end_off = v;
     }
     if (lane == 0) {
       nlist[0] = nr;
       nlist[1] = ni;
+      goff[n_groups] = n_groups < NW * 32 ? end_off : a.group_off[n_groups];
     }
   }
   __syncthreads();
   const int nr = nlist[0], ni = nlist[1];
   const int n_chunks = f / FC;
+  const int n_res_items = nr * n_chunks;
   const int total_items = (nr + ni) * n_chunks;
   const int q = a.counts[3];
   const uint32_t now = (uint32_t)a.counts[6];
-  const int cb_n = d / 256;      // column blocks per gate (or up) matrix
-  const int P1 = 2 * cb_n;       // gate/up tiles per token batch
-  const int NTL = P1 + d / 256;  // + down tiles (256 rows each)
+  const int cb_n = d / 256;   // column blocks of a gate (or up) row; down tiles per batch
+  const int P1 = 2 * cb_n;    // gate/up tiles per token batch
+  const int NTL = P1 + cb_n;  // + down tiles (256 rows each)
 
   // item j -> group, chunk, fill index (-1 = resident before the step)
   auto item = [&](int j, int& g, int& c, int& fi) {
-    if (j < nr * n_chunks) {
-      g = res[j / n_chunks];
-      c = j % n_chunks;
+    if (j < n_res_items) {
+      const int e = j / n_chunks;
+      g = res[e];
+      c = j - e * n_chunks;
       fi = -1;
     } else {
-      const int jj = j - nr * n_chunks;
+      const int jj = j - n_res_items;
       fi = jj / n_chunks;
       g = inst[fi];
-      c = jj % n_chunks;
+      c = jj - fi * n_chunks;
     }
   };
 
   if (tid >= kConsumers) {
-    // ---------------- producer warp: one ring across all of the CTA's items ----------------
+    // ---------------- producer warp: takes items from the device-wide counter ----------------
     if (tid == kConsumers) {
       bool late = false;
       int s = 0, n = 0;
       uint32_t ph = 0;
-      for (int j = ci; j < total_items; j += C) {
-        int g, c, fi;
-        item(j, g, c, fi);
-        const int slot = a.group_slot[g];
-        if ((unsigned)slot >= (unsigned)a.S) continue;  // consumers skip it too
-        if (fi >= 0 && fi < q) {
+      for (int k = 0;; ++k) {
+        const int j = k == 0 ? first_item : (int)atomicAdd(&la.sched[0], 1u);
+        int g = 0, c = 0, fi = -1, slot = 0;
+        const bool last = j >= total_items;
+        if (!last) {
+          item(j, g, c, fi);
+          slot = gslot[g];
+        }
+        const bool bad = !last && (unsigned)slot >= (unsigned)a.S;
+        if (!last && !bad && fi >= 0 && fi < q) {
           // the installed expert's bytes: wait for the fill CTAs' stamp
           if (ld_acquire(&la.ready[fi]) != now) {
             const uint64_t t0 = global_ns();
@@ -241,14 +290,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 late = true;
                 break;
               }
-              __nanosleep(200);
+              __nanosleep(128);
             }
           }
-          proxy_fence_global();
+          proxy_fence_global();  // fill-written bytes, read by TMA
         }
-        const int n_batches = (a.group_off[g + 1] - a.group_off[g] + kTokBatch - 1) / kTokBatch;
+        // the item's first stage: free it, then publish the item before the
+        // stage can complete (the consumers read it after waiting on the stage)
+        if (n >= ns && !mbar_wait(&empty[s], ph ^ 1u, late)) late = true;
+        queue[k % kQueue] = last ? -1 : (bad ? -2 - j : j);
+        if (last || bad) {
+          mbar_arrive_cta(&full[s]);  // no bytes: completes the stage at once
+          if (++s == ns) {
+            s = 0;
+            ph ^= 1u;
+          }
+          ++n;
+          if (last) break;
+          continue;
+        }
+        const int n_batches = (goff[g + 1] - goff[g] + TB - 1) / TB;
         for (int t = 0, i = 0; t < n_batches * NTL; ++t) {
-          if (n >= ns && !mbar_wait(&empty[s], ph ^ 1u, late)) late = true;
+          if (t > 0 && n >= ns && !mbar_wait(&empty[s], ph ^ 1u, late)) late = true;
           unsigned char* dst = ring + s * kTile;
           mbar_expect_tx(&full[s], kTile);
           if (i < P1) {
@@ -281,43 +344,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool late = false;
   int s = 0;
   uint32_t ph = 0;
-  auto release = [&]() {
-    proxy_fence_reads();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+  auto advance = [&]() {
     if (++s == ns) {
       s = 0;
       ph ^= 1u;
     }
   };
-  if (one_tok) {
-    for (int t = 0; t < kTokBatch; ++t) {
-      uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)t * d);
+  auto release = [&]() {
+    proxy_fence_reads();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    advance();
+  };
+  if (TB == 1) {
+    uint4* dst = reinterpret_cast<uint4*>(xs);
 #pragma unroll
-      for (int j = 0; j < kXPre; ++j) {
-        const int i = tid + j * kConsumers;
-        if (i < d / 8) dst[i] = xpre[j];
-      }
+    for (int j = 0; j < kXPre; ++j) {
+      const int i = tid + j * kConsumers;
+      if (i < d / 8) dst[i] = xpre[j];
     }
   }
-  // End of this CTA's share of the resident experts: the last compute CTA to
-  // get there adds the phase (first compute CTA start to last resident item
-  // end) and the resident bytes to xmeter.
-  bool resident_done = false;
+  // resident-phase meter: CTAs that ran resident items stamp the end of their
+  // last one; the last CTA of the grid to close adds the phase
+  bool resident_done = false, ran_resident = false;
+  unsigned long long res_end = 0;
   auto close_resident = [&]() {
     resident_done = true;
-    consumer_sync();
     if (tid == 0) {
       FillMeter* m = la.xmeter;
+      if (ran_resident) atomicMax(&m->t1, res_end);
       __threadfence();
-      atomicMax(&m->t1, (unsigned long long)global_ns());
-      __threadfence();
-      if (atomicAdd(&m->done, 1u) == (unsigned)C - 1) {
+      if (atomicAdd(&m->done, 1u) == gridDim.x - 1) {
         __threadfence();
         const unsigned long long t0 = atomicAdd(&m->t0, 0ull), t1 = atomicAdd(&m->t1, 0ull);
-        if (nr > 0) {
+        if (nr > 0 && t1 > t0) {
           atomicAdd(&m->bytes, (unsigned long long)nr * a.Bx);
-          atomicAdd(&m->ns, t1 > t0 ? t1 - t0 : 0ull);
+          atomicAdd(&m->ns, t1 - t0);
           atomicAdd(&m->launches, 1ull);
         }
         atomicExch(&m->t0, ~0ull);
@@ -326,37 +388,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   };
-  for (int j = ci; j < total_items; j += C) {
-    if (!resident_done && j >= nr * n_chunks) close_resident();
-    int g, c, fi;
-    item(j, g, c, fi);
-    const int slot = a.group_slot[g];
-    if ((unsigned)slot >= (unsigned)a.S) {
+  for (int k = 0;; ++k) {
+    // the item's first stage carries its index (or the end of the work)
+    if (!mbar_wait(&full[s], ph, late)) late = true;
+    const int j = queue[k % kQueue];
+    if (j < -1) {  // an item whose slot id is out of range: no tiles
       if (tid == 0) atomicOr(a.status, FT_ST_BAD_SLOT);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      advance();
       continue;
     }
-    const int r0 = a.group_off[g], r1 = a.group_off[g + 1];
-    const int n_batches = (r1 - r0 + kTokBatch - 1) / kTokBatch;
+    if (!resident_done && (j < 0 || j >= n_res_items)) close_resident();
+    if (j < 0) break;
+    int g, c, fi;
+    item(j, g, c, fi);
+    const int r0 = goff[g], r1 = goff[g + 1];
+    const int n_batches = (r1 - r0 + TB - 1) / TB;
     for (int b = 0; b < n_batches; ++b) {
-      const int tb = r0 + b * kTokBatch;
-      const int nt = min(kTokBatch, r1 - tb);
-      const int my_route = tid < nt ? a.group_routes[tb + tid] : 0;
-      consumer_sync();  // the previous batch (or item) is done with xs / rs / hs
-      if (!one_tok) {
+      const int tb = r0 + b * TB;
+      const int nt = TB == 1 ? 1 : min(TB, r1 - tb);
+      int rt[TB];  // the batch's route ids (every consumer thread holds them)
+#pragma unroll
+      for (int t = 0; t < TB; ++t) rt[t] = t < nt ? __ldg(a.group_routes + tb + t) : 0;
+      consumer_sync();  // the previous batch (or item) is done with xs / hs
+      if (TB > 1) {
         for (int t = 0; t < nt; ++t) {
-          const int tok = a.group_routes[tb + t] / a.k;
+          const int tok = rt[t] / a.k;
           const uint4* src = reinterpret_cast<const uint4*>(a.hidden + (size_t)tok * d);
           uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)t * d);
           for (int i = tid; i < d / 8; i += kConsumers) dst[i] = src[i];
         }
+        consumer_sync();
       }
-      consumer_sync();
 
-      // gate/up: tiles 0 .. P1-1 (tile i: matrix i / cb_n, column block i % cb_n), two per
+      // gate/up: tiles 0 .. P1-1 (tile i: matrix i >= cb_n, column block i mod cb_n), two per
       // iteration (P1 is even) with independent product chains
-      float accg[kTokBatch], accu[kTokBatch];
+      float accg[TB], accu[TB];
 #pragma unroll
-      for (int t = 0; t < kTokBatch; ++t) accg[t] = accu[t] = 0.f;
+      for (int t = 0; t < TB; ++t) accg[t] = accu[t] = 0.f;
+      int cba = 0;  // column block of the first tile of the pair
 #pragma unroll 1
       for (int i = 0; i < P1; i += 2) {
         const int s1 = s + 1 == ns ? 0 : s + 1;
@@ -369,11 +440,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint4 wb0 = *reinterpret_cast<const uint4*>(b1), wb1 = *reinterpret_cast<const uint4*>(b1 + 256);
         release();
         release();
-        const int ma = i / cb_n, mb = (i + 1) / cb_n;
-        const uint16_t* xa = xs + (i - ma * cb_n) * 256 + cq * 8;
-        const uint16_t* xb = xs + (i + 1 - mb * cb_n) * 256 + cq * 8;
+        const bool ua = i >= cb_n, ub = i + 1 >= cb_n;
+        const int cbb = cba + 1 == cb_n ? 0 : cba + 1;
+        const uint16_t* xa = xs + cba * 256 + cq * 8;
+        const uint16_t* xb = xs + cbb * 256 + cq * 8;
+        cba = cbb + 1 == cb_n ? 0 : cbb + 1;
 #pragma unroll
-        for (int t = 0; t < kTokBatch; ++t) {
+        for (int t = 0; t < TB; ++t) {
           if (t < nt) {
             const uint4 xa0 = *reinterpret_cast<const uint4*>(xa + (size_t)t * d);
             const uint4 xa1 = *reinterpret_cast<const uint4*>(xa + (size_t)t * d + 128);
@@ -381,14 +454,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint4 xb1 = *reinterpret_cast<const uint4*>(xb + (size_t)t * d + 128);
             const float pa = dot8(wa1, xa1, dot8(wa0, xa0, 0.f));
             const float pb = dot8(wb1, xb1, dot8(wb0, xb0, 0.f));
-            accg[t] += (ma == 0 ? pa : 0.f) + (mb == 0 ? pb : 0.f);
-            accu[t] += (ma == 1 ? pa : 0.f) + (mb == 1 ? pb : 0.f);
+            accg[t] += (ua ? 0.f : pa) + (ub ? 0.f : pb);
+            accu[t] += (ua ? pa : 0.f) + (ub ? pb : 0.f);
           }
         }
       }
       // row sums: 16 lanes per row
 #pragma unroll
-      for (int t = 0; t < kTokBatch; ++t) {
+      for (int t = 0; t < TB; ++t) {
         float vg = accg[t], vu = accu[t];
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) {
@@ -396,16 +469,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           vu += __shfl_xor_sync(0xffffffffu, vu, o);
         }
         if (cq == 0 && t < nt) {
-          gu[(0 * FC + rl) * kTokBatch + t] = vg;
-          gu[(1 * FC + rl) * kTokBatch + t] = vu;
+          gu[(0 * FC + rl) * TB + t] = vg;
+          gu[(1 * FC + rl) * TB + t] = vu;
         }
       }
-      if (tid < nt) rs[tid] = my_route;
       consumer_sync();
-      if (tid < FC * kTokBatch) {
+      if (tid < FC * TB) {
         const int row = tid % FC, t = tid / FC;
         if (t < nt) {
-          const float gs = gu[(0 * FC + row) * kTokBatch + t], us = gu[(1 * FC + row) * kTokBatch + t];
+          const float gs = gu[(0 * FC + row) * TB + t], us = gu[(1 * FC + row) * TB + t];
           hs[t * FC + row] = gs / (1.f + expf(-gs)) * us;
         }
       }
@@ -429,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         release();
         if (two) release();
 #pragma unroll
-        for (int t = 0; t < kTokBatch; ++t) {
+        for (int t = 0; t < TB; ++t) {
           if (t < nt) {
             const float4* hp = reinterpret_cast<const float4*>(hs + t * FC + qq * 8);
             const float4 h0 = hp[0], h1 = hp[1];
@@ -443,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               v3 += __shfl_xor_sync(0xffffffffu, v3, o);
             }
             if (qq == 0) {
-              float* yp = a.ypart + ((size_t)rs[t] * n_chunks + c) * d + jd * 256 + rowq;
+              float* yp = a.ypart + ((size_t)rt[t] * n_chunks + c) * d + jd * 256 + rowq;
               yp[0] = v0;
               yp[128] = v1;
               if (two) {
@@ -455,33 +527,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (j < n_res_items) {  // stamp the end of a resident item (thread 0 stands for the CTA)
+      ran_resident = true;
+      if (tid == 0) res_end = global_ns();
+    }
   }
-  if (!resident_done) close_resident();
-  if (late) atomicOr(a.status, FT_ST_TIMEOUT);
+  // every item of the launch has been taken (this CTA's producer took its last
+  // one before publishing the end): the last CTA out resets the counter
+  consumer_sync();
+  if (tid == 0) {
+    if (late) atomicOr(a.status, FT_ST_TIMEOUT);
+    __threadfence();
+    if (atomicAdd(&la.sched[1], 1u) == gridDim.x - 1) {
+      atomicExch(&la.sched[0], 0u);
+      atomicExch(&la.sched[1], 0u);
+    }
+  } else if (late) {
+    atomicOr(a.status, FT_ST_TIMEOUT);
+  }
 }
 
 }  // namespace
 
-int decode_layer_ring_stages(int d, int max_groups, int smem_optin) {
-  const size_t fixed = smem_layout(d, 0, max_groups).total + 16 * 16 + 1024;
-  if ((size_t)smem_optin <= fixed) return 0;
-  return (int)std::min<size_t>(12, ((size_t)smem_optin - fixed) / (kTile + 16));
+int decode_layer_ring_stages(int d, int max_groups, int smem_optin, int ctas_per_sm) {
+  // the shared memory of an SM holds ctas_per_sm CTAs (1 KB of it reserved per CTA)
+  const size_t per_cta = (size_t)(smem_optin + 1024) / ctas_per_sm - 1024;
+  const size_t fixed = smem_layout(d, 0, max_groups, 4).total + 16 * 16 + 1024;
+  if (per_cta <= fixed) return 0;
+  return (int)std::min<size_t>(12, (per_cta - fixed) / (kTile + 16));
 }
 
-cudaError_t launch_decode_layer(const LayerArgs& la, int grid, cudaStream_t st) {
+int decode_layer_ctas_per_sm() { return kCtasPerSm; }
+
+namespace {
+template <int TB>
+cudaError_t launch_tb(const LayerArgs& la, int grid, cudaStream_t st) {
   const DecodeArgs& a = la.d;
-  if (a.dtype != FT_DTYPE_BF16) return cudaErrorNotSupported;
-  if (a.d > 8192 || a.d % 256 || a.f % FC || !a.tmap_wd || !a.tmap_gu || la.ns < 2 || la.n_fill < 1 ||
-      la.n_fill >= grid)
-    return cudaErrorInvalidValue;
-  const size_t smem = smem_layout(a.d, la.ns, a.max_groups).total;
+  const size_t smem = smem_layout(a.d, la.ns, a.max_groups, TB).total;
   static thread_local int configured_dev = -1;
   static thread_local size_t configured_smem = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev || configured_smem < smem) {
     cudaError_t e =
-        cudaFuncSetAttribute(decode_layer_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(decode_layer_bf16_kernel<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
     configured_smem = smem;
@@ -492,18 +581,37 @@ cudaError_t launch_decode_layer(const LayerArgs& la, int grid, cudaStream_t st) 
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // the compute CTAs wait on the fill CTAs
+  attr[0].id = cudaLaunchAttributeCooperative;  // CTAs wait on each other's fills
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_layer_bf16_kernel, *a.tmap_gu, *a.tmap_wd, la);
+  return cudaLaunchKernelEx(&cfg, decode_layer_bf16_kernel<TB>, *a.tmap_gu, *a.tmap_wd, la);
+}
+}  // namespace
+
+cudaError_t launch_decode_layer(const LayerArgs& la, int grid, cudaStream_t st) {
+  const DecodeArgs& a = la.d;
+  if (a.dtype != FT_DTYPE_BF16) return cudaErrorNotSupported;
+  if (a.d > 8192 || a.d % 256 || a.f % FC || !a.tmap_wd || !a.tmap_gu || la.ns < 2 || la.ns >= kQueue ||
+      la.n_fill < 1 || la.n_fill >= grid || !la.sched)
+    return cudaErrorInvalidValue;
+  return a.T == 1 ? launch_tb<1>(la, grid, st) : launch_tb<4>(la, grid, st);
 }
 
 cudaError_t decode_layer_max_blocks_per_sm(int d, int ns, int max_groups, int* out) {
-  const size_t smem = smem_layout(d, ns, max_groups).total;
-  cudaError_t e = cudaFuncSetAttribute(decode_layer_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = smem_layout(d, ns, max_groups, 4).total;
+  cudaError_t e =
+      cudaFuncSetAttribute(decode_layer_bf16_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, decode_layer_bf16_kernel, kThreads, smem);
+  int b4 = 0, b1 = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b4, decode_layer_bf16_kernel<4>, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  const size_t smem1 = smem_layout(d, ns, max_groups, 1).total;
+  e = cudaFuncSetAttribute(decode_layer_bf16_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, decode_layer_bf16_kernel<1>, kThreads, smem1);
+  *out = std::min(b1, b4);
+  return e;
 }
 
 }  // namespace ft

@@ -95,9 +95,10 @@ struct ft_ctx {
 
   // fused decode path (FT_DECODE_FUSED): one CTA per SM, fill_ctas of them fill
   bool fused = false;
-  int fused_ns = 0, fused_fill = 0, fused_groups = 0;
+  int fused_ns = 0, fused_fill = 0, fused_groups = 0, fused_grid = 0;
   uint32_t* ready = nullptr;         // [K_max] clock stamp of each fetch entry's completed fill
   unsigned int* fill_done = nullptr;  // [K_max] fill CTAs done with each entry
+  unsigned int* sched = nullptr;      // [2] work-item counter and CTAs done of the fused kernel
   // host expert rate reported by the caller (ft_report_host_rate) since the last reset
   double host_bytes = 0.0, host_s = 0.0;
 };
@@ -204,6 +205,7 @@ void free_all(ft_ctx* c) {
   cudaFree(c->meter);
   cudaFree(c->ready);
   cudaFree(c->fill_done);
+  cudaFree(c->sched);
   if (c->h_counts) cudaFreeHost(c->h_counts);
   if (c->h_fetch) cudaFreeHost(c->h_fetch);
   if (c->h_victims) cudaFreeHost(c->h_victims);
@@ -429,7 +431,9 @@ int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx
         cudaMalloc(&c->ready, sizeof(uint32_t) * K) != cudaSuccess ||
         cudaMalloc(&c->fill_done, sizeof(unsigned int) * K) != cudaSuccess ||
         cudaMemset(c->ready, 0, sizeof(uint32_t) * K) != cudaSuccess ||
-        cudaMemset(c->fill_done, 0, sizeof(unsigned int) * K) != cudaSuccess) {
+        cudaMemset(c->fill_done, 0, sizeof(unsigned int) * K) != cudaSuccess ||
+        cudaMalloc(&c->sched, 2 * sizeof(unsigned int)) != cudaSuccess ||
+        cudaMemset(c->sched, 0, 2 * sizeof(unsigned int)) != cudaSuccess) {
       cudaGetLastError();
       return bail(fail(FT_E_NOMEM, "meter / fill stamp allocation failed"));
     }
@@ -441,14 +445,24 @@ int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
     const int mg = std::min(TK, E);
-    const int ns = decode_layer_ring_stages(cfg->hidden, mg, optin);
+    // as many CTAs per SM as the kernel is built for, if each still gets a ring of four stages; else one
+    int want_per_sm = decode_layer_ctas_per_sm();
+    int ns = decode_layer_ring_stages(cfg->hidden, mg, optin, want_per_sm);
+    if (ns < 4) {
+      want_per_sm = 1;
+      ns = decode_layer_ring_stages(cfg->hidden, mg, optin, 1);
+    }
     int per_sm = 0;
-    if (ns >= 4 && decode_layer_max_blocks_per_sm(cfg->hidden, ns, mg, &per_sm) == cudaSuccess && per_sm >= 1) {
+    if (ns >= 4 && decode_layer_max_blocks_per_sm(cfg->hidden, ns, mg, &per_sm) == cudaSuccess &&
+        per_sm >= want_per_sm) {
       c->fused = true;
       c->fused_ns = ns;
       c->fused_groups = mg;
-      const int want = cfg->fill_ctas ? cfg->fill_ctas : std::max(4, c->sm_count / 8);
-      c->fused_fill = std::min(want, c->sm_count - 1);
+      c->fused_grid = want_per_sm * c->sm_count;
+      // default: 3/8 of the SMs fill (A3B decode, measured: 57 of 152 fill at 0.90-0.92 of the link,
+      // and the other 95 still finish the resident experts well before the fill)
+      const int want = cfg->fill_ctas ? cfg->fill_ctas : std::max(4, c->fused_grid * 3 / 8);
+      c->fused_fill = std::min(want, c->fused_grid - 1);
     }
     cudaGetLastError();
   }
@@ -691,8 +705,9 @@ int ft_moe_forward(ft_ctx* c, int layer, int mode, const float* logits, const ui
     la.fill_done = c->fill_done;
     la.meter = &c->meter[0];
     la.xmeter = &c->meter[1];
+    la.sched = c->sched;
     cudaEvent_t pb = c->prof.begin(st);
-    cudaError_t e = launch_decode_layer(la, c->sm_count, st);
+    cudaError_t e = launch_decode_layer(la, c->fused_grid, st);
     if (e != cudaSuccess) return fail(FT_E_CUDA, "fused decode layer launch failed: %s", cudaGetErrorString(e));
     c->prof.end(st, FT_K_EXPERTS, pb);
     if (c->cpu) {

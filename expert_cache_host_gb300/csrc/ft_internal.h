@@ -131,8 +131,9 @@ cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_experts_mxfp4(const DecodeArgs& a, int tokens, cudaStream_t st);
 
 // Fused decode layer (bf16): the step's fill and all of its experts in one
-// cooperative launch (decode_layer.cu).  CTAs [0, n_fill) fill, the rest
-// compute; ready[i] receives the step's clock once fetch entry i is in its
+// cooperative launch (decode_layer.cu).  CTAs [0, n_fill) fill first, then
+// every CTA takes (expert, 32-row chunk) work items from a device-wide
+// counter; ready[i] receives the step's clock once fetch entry i is in its
 // slot; fill_done[i] counts the fill CTAs done with entry i (0 between
 // launches).
 struct LayerArgs {
@@ -146,10 +147,13 @@ struct LayerArgs {
   uint32_t* ready;
   unsigned int* fill_done;
   FillMeter* meter;   // the fill CTAs' link rate
-  FillMeter* xmeter;  // the resident-expert phase: bytes, span from the first compute CTA start to the last resident item end
+  FillMeter* xmeter;  // the resident-expert phase: bytes, span from the first CTA start to the last resident item end
+  unsigned int* sched;  // [2]: next work item, CTAs done (both 0 between launches; the last CTA out resets them)
 };
 // Ring stages that fit one CTA per SM at hidden size d (0: none).
-int decode_layer_ring_stages(int d, int max_groups, int smem_optin);
+// Ring stages of a fused-kernel CTA when ctas_per_sm of them share an SM (0: none fit).
+int decode_layer_ring_stages(int d, int max_groups, int smem_optin, int ctas_per_sm);
+int decode_layer_ctas_per_sm();  // CTAs per SM the kernel is built for (its register bound)
 cudaError_t decode_layer_max_blocks_per_sm(int d, int ns, int max_groups, int* out);
 cudaError_t launch_decode_layer(const LayerArgs& la, int grid, cudaStream_t st);
 
