@@ -69,9 +69,9 @@ NCU_TRAFFIC = {
                            sha16="e5a4dc8ca19734a8", profile="profiles/decode_experts_a3b.md"),
     "decode_experts_mxfp4": dict(ratio=80_432_896 / 80_216_064, src="expert_cache_host_gb300/csrc/expert_decode_mxfp4.cu",
                                  sha16="c69e88ed9f44398c", profile="profiles/decode_experts_mxfp4_v4.md"),
-    # not captured yet: traffic is null
-    "decode_layer": dict(ratio=None, src="expert_cache_host_gb300/csrc/decode_layer.cu", sha16=None,
-                         profile="profiles/decode_layer_a3b.md"),
+    # two all-hit launches of the fused decode layer kernel (8 resident experts each)
+    "decode_layer": dict(ratio=154_396_672 / 150_994_944, src="expert_cache_host_gb300/csrc/decode_layer.cu",
+                         sha16="bb42b0037a0041e7", profile="profiles/decode_layer_a3b.md"),
 }
 
 
@@ -1081,8 +1081,8 @@ def build_line(args, w, world, dec, link, pre, ctl, peaks, comps=None):
             "link_gbs_effective": round(pre["link_gbs"], 1), "upload_gbs": round(pre["upload_gbs"], 1),
             "link_frac": round(pre["link_gbs"] / pre_link, 4) if pre_link else None,
             "link_peak_gbs": pre_link, "device_status": pre["status"],
-            "link_peak_how": "the larger of two whole-pool host -> device streams, just before and just after the "
-                             "prefill leg", "link_around": pre.get("link_around"),
+            "link_peak_how": "the fastest of three whole-pool host -> device streams: the run's host_link pass and "
+                             "two just before and just after the prefill leg", "link_around": pre.get("link_around"),
             "roofline_gemm": {"bound": "tensor", "kernel": "grouped SwiGLU GEMMs (tcgen05), weights resident",
                               "achieved": round(pre["gemm_tflops"], 1), "peak": peaks["bf16_tflops"],
                               "unit": "TFLOP/s", "frac": round(pre["gemm_tflops"] / peaks["bf16_tflops"], 4),
@@ -1248,7 +1248,8 @@ def main():
                 after = host_link_profile(pool)
             finally:
                 ft.ft_moe_destroy(ctx)
-            pre["link_profile_gbs"] = max(before["whole_pool_gbs"], after["whole_pool_gbs"])
+            # the link drifts within minutes: the peak is the fastest whole-pool pass of the run
+            pre["link_profile_gbs"] = max(before["whole_pool_gbs"], after["whole_pool_gbs"], link["whole_pool_gbs"])
             pre["link_around"] = {"before": before, "after": after}
         if not args.no_control and not args.no_components:
             ctl = run_control_leg(args)
@@ -1306,7 +1307,13 @@ def run_v4_components(args, local):
                              dtype=1, num_slots=1, k_max=1, t_max=1)
         ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
         try:
+            # a freshly written pool can still hold slow pages on the first full pass: two passes, the faster counts
+            first = host_link_profile(pool)
             link = host_link_profile(pool)
+            link["first_pass"] = {k: first[k] for k in ("whole_pool_gbs", "chunk_gbs_min", "chunk_gbs_median")}
+            if first["whole_pool_gbs"] > link["whole_pool_gbs"]:
+                first["first_pass"] = link["first_pass"]
+                link = first
         finally:
             ft.ft_moe_destroy(ctx)
         out["host_link"] = link
