@@ -606,7 +606,8 @@ def run_prefill_leg(args, w, pool):
 
     L = args.prefill_layers or w["L"]
     E, k, d, f, T = w["E"], w["k"], w["d"], w["f"], args.prefill_tokens
-    bx = ftsynth.expert_bytes(d, f, 0)
+    dt = w["dtype"]
+    bx = ftsynth.expert_bytes(d, f, dt)
     wr = ftsynth.router_weights(0, L, E, d)
     hid = np.stack([ftsynth.prefill_hidden(0, l, T, d) for l in range(L)])
     lg = np.stack([ftsynth.router_logits(hid[l], wr[l]) for l in range(L)])
@@ -617,8 +618,8 @@ def run_prefill_leg(args, w, pool):
     stream = torch.cuda.Stream()
     res = {}
     for buffers in (2, 1):
-        cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, num_slots=1, k_max=1, t_max=1,
-                             prefill_buffers=buffers, prefill_t_max=T)
+        cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, dtype=dt, num_slots=1, k_max=1,
+                             t_max=1, prefill_buffers=buffers, prefill_t_max=T)
         ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
         try:
             with torch.cuda.stream(stream):
@@ -1195,7 +1196,6 @@ def main():
     if args.prefill_only:
         # profiling case: the prefill leg alone on the first --prefill-layers layers (not a bench line)
         w["L"] = args.prefill_layers or w["L"]
-        w["dtype"] = 0
         hp, pool, _ = make_host_pool(args, w)
         print(json.dumps({"profiling_case": "prefill", **run_prefill_leg(args, w, pool)}), flush=True)
         if hp:

@@ -119,6 +119,8 @@ int check_config(const ft_config& c) {
   if (c.prefill_buffers < 0 || c.prefill_buffers > 2) return fail(FT_E_ARG, "prefill_buffers must be 0, 1 or 2");
   if (c.prefill_buffers > 0 && (c.prefill_t_max < 1 || c.prefill_t_max > 65536))
     return fail(FT_E_ARG, "prefill_t_max must be in [1, 65536] when prefill_buffers > 0");
+  if (c.prefill_buffers > 0 && c.dtype == FT_DTYPE_MXFP4 && (c.hidden % 512 || c.inter % 512))
+    return fail(FT_E_UNSUPPORTED, "MXFP4 prefill needs hidden and inter multiples of 512");
   if (c.fill_mode != FT_FILL_KERNEL && c.fill_mode != FT_FILL_COPY_ENGINE) return fail(FT_E_ARG, "bad fill_mode");
   if (c.fill_order != FT_FILL_ORDER_ID && c.fill_order != FT_FILL_ORDER_MOST_ROUTED) return fail(FT_E_ARG, "bad fill_order");
   if (c.decode_path != FT_DECODE_FUSED && c.decode_path != FT_DECODE_SPLIT) return fail(FT_E_ARG, "bad decode_path");

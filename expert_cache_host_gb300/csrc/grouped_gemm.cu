@@ -5,21 +5,33 @@
 // rows of each expert form one contiguous segment of the gathered activation
 // matrix; segments are cut into 128-row M tiles (the last one ragged), listed
 // on the device.  An output tile is one (M tile, N tile):
-//   mode 1 (gate/up): G = X W_gate^T and U = X W_up^T for the same 128 N
-//     columns into two tensor-memory accumulators, then H = silu(G) * U,
-//     rounded to bf16 (the operand of the next GEMM);
+//   mode 1 (gate/up): [G | U] = X [W_gate; W_up]^T for the same 128 rows of
+//     W_gate and W_up, stacked into one 256-row B operand (one M=128, N=256
+//     MMA per K step), then H = silu(G) * U, rounded to bf16 (the operand of
+//     the next GEMM);
 //   mode 2 (down):    Y = H W_down^T, 256 N columns, fp32 out.
 // Persistent: one CTA per SM walks the tiles (N tiles of an M tile adjacent,
 // so the activation tile is re-read from L2).  Warp roles: warp 0 lane 0
-// issues TMA loads into a 4-stage ring (A tile 128 x 64 and the B tiles,
+// issues TMA loads into the stage ring (A tile 128 x 64 and the B tile,
 // 128-byte swizzled), running ahead across tile boundaries; warp 1 allocates
 // all 512 tensor-memory columns as two accumulator buffers and its lane 0
-// issues tcgen05.mma (M=128, K=16 steps), committing each stage back to the
-// producer and each finished tile to the epilogue; warps 2-5 drain a buffer
-// with tcgen05.ld (one row per thread), store the rows that belong to the
-// segment and hand the buffer back -- so the epilogue of one tile overlaps
+// issues tcgen05.mma (M=128, N=256, K=16 steps), committing each stage back
+// to the producer and each finished tile to the epilogue; warps 2-5 drain a
+// buffer with tcgen05.ld (one row per thread), store the rows that belong to
+// the segment and hand the buffer back -- so the epilogue of one tile overlaps
 // the MMAs of the next.  All waits are bounded (FT_ST_TIMEOUT).
+//
+// MXFP4 weights (e2m1 codes, one e8m0 scale per 32 elements of a row): the
+// producer loads the B tile's raw codes (32 bytes of each of its 256 rows per
+// K step) and the scale bytes of the next 8 K steps (16 bytes per row) into
+// a staging area of the stage; eight converter warps (6-13) turn every
+// 32-element group into bf16 -- each e2m1 value times 2^(s-127) is exact in
+// bf16 across the e8m0 range, saturating only where the product leaves it
+// (|value| > 3.4e38) -- write it into the B tile in the same 128-byte swizzle
+// layout TMA produces, and arrive on the stage's full barrier.  The MMA is
+// then the bf16 one: activations are never quantised.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "grouped_gemm.h"
@@ -28,38 +40,74 @@
 namespace ft {
 namespace {
 
-constexpr int BM = 128, BK = 64, NSTAGE = 4, kThreads = 192, kEpiWarps = 4;
+constexpr int BM = 128, BK = 64, kEpiWarps = 4, kConvWarps = 8;
+constexpr int kBaseThreads = 192;  // producer, MMA issuer, 4 epilogue warps
 
-template <int MODE>
+template <int MODE, bool FP4>
 struct Cfg {
-  static constexpr int BN = MODE == 1 ? 128 : 256;
-  static constexpr int NB = MODE == 1 ? 2 : 1;  // B tiles per stage
+  static constexpr int BN = MODE == 1 ? 128 : 256;   // output columns of a tile
+  static constexpr int B_ROWS = 256;                  // B operand rows (mode 1: BN gate + BN up rows)
+  static constexpr int NSTAGE = FP4 ? 3 : 4;
+  static constexpr int kThreads = kBaseThreads + (FP4 ? 32 * kConvWarps : 0);
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE = A_BYTES + NB * B_BYTES;
-  static constexpr uint32_t ACC_COLS = 256;          // fp32 columns of one accumulator buffer
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int RAW_CODES = FP4 ? B_ROWS * BK / 2 : 0;  // 32 code bytes per row per K step
+  static constexpr int RAW_SC = FP4 ? B_ROWS * 16 : 0;          // scale bytes of 8 K steps per row
+  static constexpr int STAGE = A_BYTES + B_BYTES + RAW_CODES + RAW_SC;  // a multiple of 1024
+  static constexpr uint32_t ACC_COLS = 256;            // fp32 columns of one accumulator buffer
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // double buffer: all 512 columns
   // epilogue staging (mode 2): per epilogue warp, two 32-row x 128-byte boxes (4 KB each)
   static constexpr int OUT_COLS = MODE == 1 ? 64 : 32;  // output columns per 128-byte row piece (bf16 / fp32)
   static constexpr int STG_BYTES = MODE == 2 ? kEpiWarps * 2 * 4096 : 0;
   static constexpr size_t SMEM = (size_t)NSTAGE * STAGE + STG_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(STAGE % 1024 == 0, "stage tiles must stay 1024-byte aligned for the 128-byte swizzle");
 };
 
-// Position of 16-byte chunk j of row r (0..31) inside a 32 x 128-byte staging
-// box in the 128-byte swizzle layout the store tensor map expects.
+// Exact 2^(s-127) for an e8m0 byte (s = 255 is NaN, s = 0 the fp32 subnormal 2^-127).
+__device__ __forceinline__ float e8m0_scale(unsigned s) {
+  return s == 255u ? __int_as_float(0x7FC00000) : (s ? __int_as_float((int)(s << 23)) : __int_as_float(0x00400000));
+}
+
+// Eight e2m1 codes (four bytes, element 2i in the low nibble of byte i) times
+// the group scale -> eight bf16 values (one 16-byte chunk of a B row).  The
+// code -> f16 conversion and the fp32 product are exact; so is the rounding
+// to bf16, since the product carries at most two significant bits.
+__device__ __forceinline__ uint4 e2m1x8_to_bf16(unsigned w, float sc) {
+  unsigned p[4];
+  asm("{ .reg .b8 a0, a1, a2, a3; mov.b32 {a0, a1, a2, a3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, a0; cvt.rn.f16x2.e2m1x2 %1, a1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, a2; cvt.rn.f16x2.e2m1x2 %3, a3; }"
+      : "=r"(p[0]), "=r"(p[1]), "=r"(p[2]), "=r"(p[3])
+      : "r"(w));
+  unsigned o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&p[i]));
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.x * sc, v.y * sc);
+    o[i] = *reinterpret_cast<unsigned*>(&b);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Position of 16-byte chunk j of row r inside a tile of 128-byte rows in the
+// 128-byte swizzle layout (the one TMA reads and writes and the MMA
+// descriptors name), the tile 1024-byte aligned.
 __device__ __forceinline__ int stg_off(int r, int j) { return r * 128 + ((j ^ (r & 7)) << 4); }
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MODE, bool FP4>
+__global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                        const __grid_constant__ CUtensorMap map_out, GemmArgs a, int n_ntiles) {
-  using C = Cfg<MODE>;
+                        const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_out,
+                        GemmArgs a, int n_ntiles) {
+  using C = Cfg<MODE, FP4>;
+  constexpr int NSTAGE = C::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stg = smem + NSTAGE * C::STAGE;  // epilogue staging (1024-byte aligned)
   uint64_t* full = reinterpret_cast<uint64_t*>(stg + C::STG_BYTES);
   uint64_t* empty = full + NSTAGE;
-  uint64_t* accf = empty + NSTAGE;  // [2] accumulator buffer holds a finished tile
+  uint64_t* rawf = empty + NSTAGE;  // [NSTAGE] MXFP4: the stage's codes and scales have landed
+  uint64_t* accf = rawf + NSTAGE;   // [2] accumulator buffer holds a finished tile
   uint64_t* acce = accf + 2;        // [2] accumulator buffer drained by the epilogue
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
 
@@ -69,8 +117,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&full[s], 1);
+      // MXFP4: the A tile's bytes plus one arrival per converter warp
+      mbar_init(&full[s], FP4 ? 1 + kConvWarps : 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&rawf[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf[b], 1);
@@ -96,20 +146,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (it >= NSTAGE && !mbar_wait(&empty[s], (uint32_t)(((it / NSTAGE) - 1) & 1), late)) late = true;
           uint8_t* sa = smem + s * C::STAGE;
           uint8_t* sb = sa + C::A_BYTES;
-          mbar_expect_tx(&full[s], C::STAGE);
-          tensor_g2s_2d(sa, &map_a, kb * BK, r0, &full[s]);
-          if (MODE == 1) {
-            tensor_g2s_4d(sb, &map_b, kb * BK, n0, 0, e, &full[s]);
-            tensor_g2s_4d(sb + C::B_BYTES, &map_b, kb * BK, n0, 1, e, &full[s]);
+          if (FP4) {
+            uint8_t* rc = sb + C::B_BYTES;  // [256 rows][32 code bytes]
+            uint8_t* rs = rc + C::RAW_CODES;  // [256 rows][16 scale bytes]
+            const int xs = (kb >> 3) * 16;  // the 16 scale bytes that cover K steps 8*(kb/8) .. +7
+            mbar_expect_tx(&rawf[s], C::RAW_CODES + C::RAW_SC);
+            if (MODE == 1) {
+              tensor_g2s_4d(rc, &map_b, kb * (BK / 2), n0, 0, e, &rawf[s]);
+              tensor_g2s_4d(rc + C::RAW_CODES / 2, &map_b, kb * (BK / 2), n0, 1, e, &rawf[s]);
+              tensor_g2s_4d(rs, &map_s, xs, n0, 0, e, &rawf[s]);
+              tensor_g2s_4d(rs + C::RAW_SC / 2, &map_s, xs, n0, 1, e, &rawf[s]);
+            } else {
+              tensor_g2s_3d(rc, &map_b, kb * (BK / 2), n0, e, &rawf[s]);
+              tensor_g2s_3d(rs, &map_s, xs, n0, e, &rawf[s]);
+            }
+            mbar_expect_tx(&full[s], C::A_BYTES);
+            tensor_g2s_2d(sa, &map_a, kb * BK, r0, &full[s]);
           } else {
-            tensor_g2s_3d(sb, &map_b, kb * BK, n0, e, &full[s]);
+            mbar_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
+            tensor_g2s_2d(sa, &map_a, kb * BK, r0, &full[s]);
+            if (MODE == 1) {
+              tensor_g2s_4d(sb, &map_b, kb * BK, n0, 0, e, &full[s]);
+              tensor_g2s_4d(sb + C::B_BYTES / 2, &map_b, kb * BK, n0, 1, e, &full[s]);
+            } else {
+              tensor_g2s_3d(sb, &map_b, kb * BK, n0, e, &full[s]);
+            }
           }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16(BM, C::BN);
+      constexpr uint32_t idesc = umma_idesc_bf16(BM, C::B_ROWS);
       uint32_t it = 0;
       int i = 0;  // tiles of this CTA so far
       for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
@@ -124,18 +192,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * C::STAGE), sb = sa + C::A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = umma_desc_sw128(sa + kk * 32);
-            const uint32_t acc = (kb | kk) ? 1u : 0u;
-            umma_bf16(acc_tm, ad, umma_desc_sw128(sb + kk * 32), idesc, acc);
-            if (MODE == 1) umma_bf16(acc_tm + C::BN, ad, umma_desc_sw128(sb + C::B_BYTES + kk * 32), idesc, acc);
-          }
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(acc_tm, umma_desc_sw128(sa + kk * 32), umma_desc_sw128(sb + kk * 32), idesc,
+                      (kb | kk) ? 1u : 0u);
           umma_commit(&empty[s]);
         }
         umma_commit(&accf[b]);
       }
     }
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 (one row each).
     // Mode 2: a warp whose 32 rows all belong to the segment stages them in
     // shared memory (128-byte swizzle) and writes each 32-row x 128-byte box
@@ -213,6 +278,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive_cta(&acce[b]);
     }
     if (lane == 0) bulk_wait_all();  // every store of this warp has landed before the CTA exits
+  } else if (FP4) {
+    // converters: 256 threads, two (row, 32-element group) units each per K
+    // step; a warp covers 16 rows, so its 16-byte code reads are contiguous
+    // and each quarter-warp's four 16-byte chunk stores hit distinct banks.
+    const int ct = threadIdx.x - kBaseThreads;
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % NSTAGE;
+        if (!mbar_wait(&rawf[s], (uint32_t)((it / NSTAGE) & 1), late)) late = true;
+        uint8_t* sb = smem + s * C::STAGE + C::A_BYTES;
+        const uint8_t* rc = sb + C::B_BYTES;
+        const uint8_t* rs = rc + C::RAW_CODES;
+#pragma unroll
+        for (int u2 = 0; u2 < 2; ++u2) {
+          const int u = ct + 256 * u2, r = u >> 1, h = u & 1;
+          const uint4 cw = *reinterpret_cast<const uint4*>(rc + r * 32 + h * 16);
+          const float sc = e8m0_scale(rs[r * 16 + (kb & 7) * 2 + h]);
+          const unsigned wv[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(sb + stg_off(r, 4 * h + q)) = e2m1x8_to_bf16(wv[q], sc);
+        }
+        // the B tile is read by the tensor core (async proxy), and the codes'
+        // staging is rewritten by TMA once the MMAs have consumed the stage
+        proxy_fence_writes();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cta(&full[s]);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -221,16 +316,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (late) atomicOr(a.status, FT_ST_TIMEOUT);
 }
 
-template <int MODE>
-cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const CUtensorMap* map_out, const GemmArgs& a,
-                   int max_mtiles, int N, cudaStream_t st) {
-  using C = Cfg<MODE>;
-  if (N % C::BN || a.K % BK) return cudaErrorInvalidValue;
+template <int MODE, bool FP4>
+cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const CUtensorMap* map_s,
+                   const CUtensorMap* map_out, const GemmArgs& a, int max_mtiles, int N, cudaStream_t st) {
+  using C = Cfg<MODE, FP4>;
+  if (N % C::BN || a.K % BK || (FP4 && a.K % 512)) return cudaErrorInvalidValue;
   static thread_local int configured = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured != dev) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM);
     if (e != cudaSuccess) return e;
     configured = dev;
@@ -239,7 +334,8 @@ cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const CUt
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int n_ntiles = N / C::BN;
   const int grid = max_mtiles * n_ntiles < sms ? max_mtiles * n_ntiles : sms;  // persistent: one CTA per SM
-  grouped_gemm_kernel<MODE><<<grid, kThreads, C::SMEM, st>>>(*map_a, *map_b, *map_out, a, n_ntiles);
+  grouped_gemm_kernel<MODE, FP4>
+      <<<grid, C::kThreads, C::SMEM, st>>>(*map_a, *map_b, map_s ? *map_s : *map_b, *map_out, a, n_ntiles);
   return cudaGetLastError();
 }
 
@@ -247,12 +343,24 @@ cudaError_t launch(const CUtensorMap* map_a, const CUtensorMap* map_b, const CUt
 
 cudaError_t launch_gemm_gateup(const CUtensorMap* map_x, const CUtensorMap* map_w1, const CUtensorMap* map_h_out,
                                const GemmArgs& a, int max_mtiles, int f, cudaStream_t st) {
-  return launch<1>(map_x, map_w1, map_h_out, a, max_mtiles, f, st);
+  return launch<1, false>(map_x, map_w1, nullptr, map_h_out, a, max_mtiles, f, st);
 }
 
 cudaError_t launch_gemm_down(const CUtensorMap* map_h, const CUtensorMap* map_w2, const CUtensorMap* map_y_out,
                              const GemmArgs& a, int max_mtiles, int d, cudaStream_t st) {
-  return launch<2>(map_h, map_w2, map_y_out, a, max_mtiles, d, st);
+  return launch<2, false>(map_h, map_w2, nullptr, map_y_out, a, max_mtiles, d, st);
+}
+
+cudaError_t launch_gemm_gateup_mxfp4(const CUtensorMap* map_x, const CUtensorMap* map_c1, const CUtensorMap* map_s1,
+                                     const CUtensorMap* map_h_out, const GemmArgs& a, int max_mtiles, int f,
+                                     cudaStream_t st) {
+  return launch<1, true>(map_x, map_c1, map_s1, map_h_out, a, max_mtiles, f, st);
+}
+
+cudaError_t launch_gemm_down_mxfp4(const CUtensorMap* map_h, const CUtensorMap* map_c2, const CUtensorMap* map_s2,
+                                   const CUtensorMap* map_y_out, const GemmArgs& a, int max_mtiles, int d,
+                                   cudaStream_t st) {
+  return launch<2, true>(map_h, map_c2, map_s2, map_y_out, a, max_mtiles, d, st);
 }
 
 }  // namespace ft

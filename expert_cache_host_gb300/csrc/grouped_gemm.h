@@ -33,4 +33,17 @@ cudaError_t launch_gemm_gateup(const CUtensorMap* map_x, const CUtensorMap* map_
 cudaError_t launch_gemm_down(const CUtensorMap* map_h, const CUtensorMap* map_w2, const CUtensorMap* map_y_out,
                              const GemmArgs& a, int max_mtiles, int d, cudaStream_t st);
 
+// MXFP4 weights (e2m1 codes + e8m0 scales, the canonical expert layout),
+// dequantised to bf16 in shared memory; d and f multiples of 512.
+// map_c1: 4-D uint8 (d/2, f, {gate, up}, expert), box 32 x 128 x 1 x 1;
+// map_s1: 4-D uint8 (d/32, f, {gate, up}, expert), box 16 x 128 x 1 x 1.
+cudaError_t launch_gemm_gateup_mxfp4(const CUtensorMap* map_x, const CUtensorMap* map_c1, const CUtensorMap* map_s1,
+                                     const CUtensorMap* map_h_out, const GemmArgs& a, int max_mtiles, int f,
+                                     cudaStream_t st);
+
+// map_c2: 3-D uint8 (f/2, d, expert), box 32 x 256 x 1; map_s2: 3-D uint8 (f/32, d, expert), box 16 x 256 x 1.
+cudaError_t launch_gemm_down_mxfp4(const CUtensorMap* map_h, const CUtensorMap* map_c2, const CUtensorMap* map_s2,
+                                   const CUtensorMap* map_y_out, const GemmArgs& a, int max_mtiles, int d,
+                                   cudaStream_t st);
+
 }  // namespace ft

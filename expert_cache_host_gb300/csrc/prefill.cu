@@ -33,7 +33,8 @@ struct PrefillState {
   bool free_recorded[2] = {false, false};
   uint8_t* lbuf[2] = {nullptr, nullptr};
   int lbuf_layer[2] = {-1, -1};
-  CUtensorMap map_w1[2], map_w2[2], map_x, map_h;
+  CUtensorMap map_w1[2], map_w2[2], map_x, map_h;  // bf16 weights; MXFP4: the code maps
+  CUtensorMap map_s1[2], map_s2[2];                 // MXFP4: the scale maps
   CUtensorMap map_h_out, map_y_out;  // epilogue store maps (32-row boxes)
   int rows_cap = 0, max_mtiles = 0;
   int32_t* ids = nullptr;
@@ -141,21 +142,38 @@ __global__ void combine_kernel(const float4* __restrict__ y, const int32_t* __re
 }
 
 bool make_weight_maps(PrefillState* p, int b, char* msg, size_t n) {
-  const uint64_t d = p->cfg.d, f = p->cfg.f, E = p->cfg.E;
+  const uint64_t d = p->cfg.d, f = p->cfg.f, E = p->cfg.E, Bx = p->cfg.Bx;
+  uint8_t* lb = p->lbuf[b];
+  if (p->cfg.dtype == FT_DTYPE_MXFP4) {
+    // canonical MXFP4 expert: [codes gate | up | down | scales gate | up | down]
+    const uint64_t df = d * f;
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const uint64_t c1_dims[4] = {d / 2, f, 2, E}, c1_str[3] = {d / 2, df / 2, Bx};
+    const uint32_t c1_box[4] = {32, 128, 1, 1};
+    const uint64_t s1_dims[4] = {d / 32, f, 2, E}, s1_str[3] = {d / 32, df / 32, Bx};
+    const uint32_t s1_box[4] = {16, 128, 1, 1};
+    const uint64_t c2_dims[3] = {f / 2, d, E}, c2_str[2] = {f / 2, Bx};
+    const uint32_t c2_box[3] = {32, 256, 1};
+    const uint64_t s2_dims[3] = {f / 32, d, E}, s2_str[2] = {f / 32, Bx};
+    const uint32_t s2_box[3] = {16, 256, 1};
+    return encode_tensor_map(&p->map_w1[b], u8, 4, lb, c1_dims, c1_str, c1_box, msg, n) &&
+           encode_tensor_map(&p->map_s1[b], u8, 4, lb + 3 * df / 2, s1_dims, s1_str, s1_box, msg, n) &&
+           encode_tensor_map(&p->map_w2[b], u8, 3, lb + df, c2_dims, c2_str, c2_box, msg, n) &&
+           encode_tensor_map(&p->map_s2[b], u8, 3, lb + 3 * df / 2 + 2 * df / 32, s2_dims, s2_str, s2_box, msg, n);
+  }
   {
     const uint64_t dims[4] = {d, f, 2, E};
-    const uint64_t strides[3] = {d * 2, d * f * 2, p->cfg.Bx};
+    const uint64_t strides[3] = {d * 2, d * f * 2, Bx};
     const uint32_t box[4] = {64, 128, 1, 1};
-    if (!encode_tensor_map(&p->map_w1[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p->lbuf[b], dims, strides, box, msg, n,
-                           true))
+    if (!encode_tensor_map(&p->map_w1[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, lb, dims, strides, box, msg, n, true))
       return false;
   }
   {
     const uint64_t dims[3] = {f, d, E};
-    const uint64_t strides[2] = {f * 2, p->cfg.Bx};
+    const uint64_t strides[2] = {f * 2, Bx};
     const uint32_t box[3] = {64, 256, 1};
-    if (!encode_tensor_map(&p->map_w2[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->lbuf[b] + 4 * d * f, dims, strides,
-                           box, msg, n, true))
+    if (!encode_tensor_map(&p->map_w2[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, lb + 4 * d * f, dims, strides, box, msg,
+                           n, true))
       return false;
   }
   return true;
@@ -211,8 +229,8 @@ void prefill_destroy(PrefillState* p) {
 }
 
 PrefillState* prefill_create(const PrefillConfig& cfg, char* msg, size_t msg_len) {
-  if (cfg.dtype != FT_DTYPE_BF16) {
-    snprintf(msg, msg_len, "the prefill path is built for bf16 experts only");
+  if (cfg.dtype == FT_DTYPE_MXFP4 ? (cfg.d % 512 || cfg.f % 512) : (cfg.d % 256 || cfg.f % 128)) {
+    snprintf(msg, msg_len, "prefill GEMMs need d %% 256 == 0 and f %% 128 == 0 (bf16), or d and f multiples of 512 (MXFP4)");
     return nullptr;
   }
   PrefillState* p = new (std::nothrow) PrefillState();
@@ -320,13 +338,17 @@ int prefill_forward(PrefillState* p, int layer, const float* logits, const uint1
     ga.out = p->hbuf;
     ga.out_ld = c.f;
     ga.K = c.d;
-    e = launch_gemm_gateup(&p->map_x, &p->map_w1[b], &p->map_h_out, ga, max_mt, c.f, st);
+    e = c.dtype == FT_DTYPE_MXFP4
+            ? launch_gemm_gateup_mxfp4(&p->map_x, &p->map_w1[b], &p->map_s1[b], &p->map_h_out, ga, max_mt, c.f, st)
+            : launch_gemm_gateup(&p->map_x, &p->map_w1[b], &p->map_h_out, ga, max_mt, c.f, st);
   }
   if (e == cudaSuccess) {
     ga.out = p->ybuf;
     ga.out_ld = c.d;
     ga.K = c.f;
-    e = launch_gemm_down(&p->map_h, &p->map_w2[b], &p->map_y_out, ga, max_mt, c.d, st);
+    e = c.dtype == FT_DTYPE_MXFP4
+            ? launch_gemm_down_mxfp4(&p->map_h, &p->map_w2[b], &p->map_s2[b], &p->map_y_out, ga, max_mt, c.d, st)
+            : launch_gemm_down(&p->map_h, &p->map_w2[b], &p->map_y_out, ga, max_mt, c.d, st);
   }
   if (prof) prof->end(st, FT_K_GEMM, pb);
   pb = prof ? prof->begin(st) : nullptr;

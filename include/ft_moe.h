@@ -117,7 +117,8 @@ typedef struct ft_config {
   int32_t k_max;         /* K_max: fixed victim-buffer size (1..1024) */
   int32_t t_max;         /* tokens per decode/control step (1..1024) */
   int32_t r_num, r_den;  /* r = BP/BH as a rational, r_num >= 0, r_den >= 1 */
-  int32_t prefill_buffers; /* 0: no prefill; 1: one layer buffer (no overlap); 2: double buffer */
+  int32_t prefill_buffers; /* 0: no prefill; 1: one layer buffer (no overlap); 2: double buffer
+                              (MXFP4 experts: hidden and inter multiples of 512, else FT_E_UNSUPPORTED) */
   int32_t prefill_t_max; /* tokens per prefill chunk (0 if no prefill) */
   int32_t fill_mode;     /* FT_FILL_KERNEL or FT_FILL_COPY_ENGINE */
   int32_t fill_order;    /* FT_FILL_ORDER_ID or FT_FILL_ORDER_MOST_ROUTED: which q of the m misses are filled */
@@ -201,7 +202,9 @@ int ft_cache_control(ft_ctx* ctx, int layer, const int32_t* ids_dev, int T, ft_s
  *    residency table is untouched), waits for layer `layer` in its layer
  *    buffer (uploading it first if it is not there), runs all routes, and --
  *    with prefill_buffers == 2 -- starts the upload of layer+1 into the other
- *    buffer before returning.  T <= prefill_t_max.
+ *    buffer before returning.  T <= prefill_t_max.  MXFP4 experts are
+ *    dequantised exactly to bf16 on the way into the tensor cores; the
+ *    activations stay bf16.
  *  hidden_dev [T, d] bf16; partial_dev [T, d] float32 or NULL (= 0);
  *  out_dev [T, d] float32, written (not accumulated).
  * Never synchronises (except FT_FILL_COPY_ENGINE, which reads the fetch list

@@ -47,6 +47,17 @@ def test_bad_config_rejected_on_host(lib):
         assert ei.value.code == ft.FT_E_ARG, bad
 
 
+def test_mxfp4_prefill_shape_rejected_on_host(lib):
+    """MXFP4 prefill GEMMs read the scales of 8 K steps per TMA box: hidden and
+    inter must be multiples of 512."""
+    pool = (ctypes.c_uint8 * 16)()
+    for shape in (dict(hidden=768, inter=512), dict(hidden=512, inter=384)):
+        cfg = ft.make_config(dtype=ft.FT_DTYPE_MXFP4, prefill_buffers=2, prefill_t_max=64, **shape)
+        with pytest.raises(ft.FtError) as ei:
+            ft.ft_moe_init(cfg, ctypes.addressof(pool), 16)
+        assert ei.value.code == ft.FT_E_UNSUPPORTED, shape
+
+
 def test_small_pool_rejected(lib):
     pool = (ctypes.c_uint8 * 16)()
     cfg = ft.make_config()
