@@ -887,7 +887,11 @@ def run_sweep(args, w, world, local):
         elif args.sweep == "fill":
             hid, lg = decode_inputs(w, args.warmup + args.steps + min(args.steps, args.profile_steps))
             peaks = measured_peaks()
-            points = [("split", 0)] + [("fused", n) for n in (19, 38, 57, 76)]
+            # split path: the fill kernel on every SM (0) or on fewer; fused path (bf16): fill CTAs of the grid
+            split_n = [int(x) for x in args.split_fill_points.split(",") if x]
+            points = [("split", n) for n in split_n]
+            if w["dtype"] == 0:
+                points += [("fused", n) for n in (19, 38, 57, 76)]
             for rep in range(2):  # the link varies over minutes: every point twice, interleaved
                 for path, n in points:
                     ws = dict(w, decode_path=0 if path == "fused" else 1, fill_ctas=n)
@@ -1138,7 +1142,9 @@ def main():
     ap.add_argument("--decode-path", choices=("fused", "split"), default="fused",
                     help="fused: one cooperative kernel per layer runs the fill and the experts (bf16); split: a "
                          "fill kernel beside two expert launches")
-    ap.add_argument("--fill-ctas", type=int, default=0, help="fused path: CTAs that fill (0 = the library's choice)")
+    ap.add_argument("--fill-ctas", type=int, default=0, help="CTAs that fill (0 = the library's choice)")
+    ap.add_argument("--split-fill-points", default="0,76,57,38",
+                    help="--sweep fill: fill CTA counts of the split path (0 = the library's choice)")
     ap.add_argument("--pool", choices=("pinned", "registered"), default="pinned",
                     help="pinned: pool written into ft_host_alloc memory; registered: pageable pool pinned by "
                          "ft_moe_init after the write")
@@ -1287,9 +1293,10 @@ def main():
 
 
 def run_v4_components(args, local):
-    """V4-Flash-style MXFP4 decode at batch 1 and 16, after the A3B pool is
-    freed: the 147 GB pool in ft_host_alloc memory (fewer layers only if the
-    host cannot hold it, said in the workload)."""
+    """V4-Flash-style MXFP4 decode at batch 1 and 16 and an 8192-token prefill
+    chunk, after the A3B pool is freed: the 147 GB pool in ft_host_alloc
+    memory (fewer layers only if the host cannot hold it, said in the
+    workload)."""
     w = dict(V4)
     per_layer = w["E"] * ftsynth.expert_bytes(w["d"], w["f"], 1)
     fit = int(max(0, host_available() - (24 << 30)) // per_layer)
@@ -1329,6 +1336,23 @@ def run_v4_components(args, local):
             s["experts_traffic_per_launch"], s["experts_traffic_source"] = tr, note
             out[f"batch_{T}"] = s
             del hid, lg
+        if not args.no_prefill:
+            pre = run_prefill_leg(args, w, pool)
+            bf16_peak = peaks["bf16_tflops"]
+            out["prefill"] = {
+                "workload": f"{pre['T']}-token chunk, V4-Flash-style MXFP4, {pre['L']} layers, full-layer double "
+                            "buffer",
+                "chunk_s": round(pre["chunk_s"], 4), "chunk_s_single_buffer": round(pre["chunk_s_single_buffer"], 4),
+                "tok_s": round(pre["T"] / pre["chunk_s"], 1), "pool_gb": round(pre["pool_bytes"] / 1e9, 2),
+                "link_gbs_effective": round(pre["link_gbs"], 1), "upload_gbs": round(pre["upload_gbs"], 1),
+                "link_frac": round(pre["link_gbs"] / link["whole_pool_gbs"], 4), "device_status": pre["status"],
+                "roofline_gemm": {"bound": "tensor", "kernel": "grouped SwiGLU GEMMs (tcgen05 kind::f16), MXFP4 "
+                                  "weights dequantised exactly to bf16 in shared memory, weights resident",
+                                  "achieved": round(pre["gemm_tflops"], 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                                  "frac": round(pre["gemm_tflops"] / bf16_peak, 4),
+                                  "ms_per_layer": round(pre["gemm_ms_per_layer"], 3),
+                                  "peak_source": peaks["source"] + " (burst bf16)"},
+            }
     finally:
         del pool
         hp.free()

@@ -123,7 +123,7 @@ typedef struct ft_config {
   int32_t fill_mode;     /* FT_FILL_KERNEL or FT_FILL_COPY_ENGINE */
   int32_t fill_order;    /* FT_FILL_ORDER_ID or FT_FILL_ORDER_MOST_ROUTED: which q of the m misses are filled */
   int32_t decode_path;   /* FT_DECODE_FUSED (default) or FT_DECODE_SPLIT */
-  int32_t fill_ctas;     /* fused path: CTAs that fill (0 = the library's choice) */
+  int32_t fill_ctas;     /* CTAs that fill, on either decode path (0 = the library's choice) */
   int32_t reserved[1];   /* must be zero */
 } ft_config;
 
