@@ -249,9 +249,12 @@ def host_link_profile(pool, chunk=1 << 30):
     bd = torch.empty(burst_bytes, dtype=torch.uint8, device="cuda")
     burst = burst_bytes / min(timed(s, lambda: bd.copy_(b, non_blocking=True)) for _ in range(3)) / 1e9
     del dst, bd
-    per.sort()
-    return {"whole_pool_gbs": round(whole, 1), "chunks": n, "chunk_gbs_min": round(per[0], 1),
-            "chunk_gbs_median": round(per[n // 2], 1), "chunk_gbs_max": round(per[-1], 1),
+    slow = [i for i, g in enumerate(per) if g < 150.0]
+    srt = sorted(per)
+    return {"whole_pool_gbs": round(whole, 1), "chunks": n, "chunk_gbs_min": round(srt[0], 1),
+            "chunk_gbs_median": round(srt[n // 2], 1), "chunk_gbs_max": round(srt[-1], 1),
+            "slow_chunks": {"count_below_150_gbs": len(slow), "first_indices": slow[:16],
+                            "gbs": [round(per[i], 1) for i in slow[:16]]},
             "burst_first_1p21gb_gbs": round(burst, 1),
             "how": "pinned H2D cudaMemcpyAsync of every 1 GiB chunk of the pool once, CUDA events"}
 
@@ -1127,6 +1130,7 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="decode tokens per step (default 1)")
     ap.add_argument("--layers", type=int, default=0, help="override L (small profiling cases, not a bench line)")
     ap.add_argument("--slots", type=int, default=0, help="override S (small profiling cases, not a bench line)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (small profiling cases, not a bench line)")
     ap.add_argument("--sweep", choices=("capacity", "prompt", "fill"), default=None,
                     help="report mode (not the bench line): decode miss rate and tok/s over cache capacities of "
                          "5/10/25/50%% of the pool, or prefill chunk time over prompt lengths 4k/8k/16k with and "
@@ -1174,9 +1178,9 @@ def main():
     w["fill_ctas"] = args.fill_ctas
     if args.decode_path == "split" or args.fill_ctas:
         w["desc"] += f" [decode path {args.decode_path}" + (f", {args.fill_ctas} fill CTAs]" if args.fill_ctas else "]")
-    if args.layers or args.slots:
-        w["L"], w["S"] = args.layers or w["L"], args.slots or w["S"]
-        w["desc"] += f" [profiling case: L={w['L']}, S={w['S']}]"
+    if args.layers or args.slots or args.experts:
+        w["L"], w["S"], w["E"] = args.layers or w["L"], args.slots or w["S"], args.experts or w["E"]
+        w["desc"] += f" [profiling case: L={w['L']}, S={w['S']}, E={w['E']}]"
         args.no_components = True
 
     if world > 1:
@@ -1315,12 +1319,9 @@ def run_v4_components(args, local):
         ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
         try:
             # a freshly written pool can still hold slow pages on the first full pass: two passes, the faster counts
-            first = host_link_profile(pool)
-            link = host_link_profile(pool)
-            link["first_pass"] = {k: first[k] for k in ("whole_pool_gbs", "chunk_gbs_min", "chunk_gbs_median")}
-            if first["whole_pool_gbs"] > link["whole_pool_gbs"]:
-                first["first_pass"] = link["first_pass"]
-                link = first
+            passes = [host_link_profile(pool) for _ in range(2)]
+            link = dict(max(passes, key=lambda p: p["whole_pool_gbs"]))
+            link["passes_whole_pool_gbs"] = [p["whole_pool_gbs"] for p in passes]
         finally:
             ft.ft_moe_destroy(ctx)
         out["host_link"] = link
