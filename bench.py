@@ -70,8 +70,11 @@ NCU_TRAFFIC = {
     "decode_experts_mxfp4": dict(ratio=80_432_896 / 80_216_064, src="expert_cache_host_gb300/csrc/expert_decode_mxfp4.cu",
                                  sha16="c69e88ed9f44398c", profile="profiles/decode_experts_mxfp4_v4.md"),
     # two all-hit launches of the fused decode layer kernel (8 resident experts each)
-    "decode_layer": dict(ratio=154_396_672 / 150_994_944, src="expert_cache_host_gb300/csrc/decode_layer.cu",
-                         sha16="bb42b0037a0041e7", profile="profiles/decode_layer_a3b.md"),
+    "decode_layer": dict(ratio=154_318_592 / 150_994_944, src="expert_cache_host_gb300/csrc/decode_layer.cu",
+                         sha16="70e03872d494dbd8", profile="profiles/decode_layer_a3b.md"),
+    # four all-hit launches of the fused kernel's MXFP4 instantiation (6 resident V4 experts each)
+    "decode_layer_mxfp4": dict(ratio=331_467_520 / 320_864_256, src="expert_cache_host_gb300/csrc/decode_layer.cu",
+                               sha16="70e03872d494dbd8", profile="profiles/decode_layer_mxfp4_v4.md"),
 }
 
 
@@ -890,11 +893,10 @@ def run_sweep(args, w, world, local):
         elif args.sweep == "fill":
             hid, lg = decode_inputs(w, args.warmup + args.steps + min(args.steps, args.profile_steps))
             peaks = measured_peaks()
-            # split path: the fill kernel on every SM (0) or on fewer; fused path (bf16): fill CTAs of the grid
+            # split path: the fill kernel's CTAs (0 = the library's choice); fused path: fill CTAs of the grid
             split_n = [int(x) for x in args.split_fill_points.split(",") if x]
             points = [("split", n) for n in split_n]
-            if w["dtype"] == 0:
-                points += [("fused", n) for n in (19, 38, 57, 76)]
+            points += [("fused", n) for n in (19, 38, 57, 76)]
             for rep in range(2):  # the link varies over minutes: every point twice, interleaved
                 for path, n in points:
                     ws = dict(w, decode_path=0 if path == "fused" else 1, fill_ctas=n)
@@ -983,6 +985,20 @@ def experts_rate(dec):
     return 0.0, None
 
 
+def experts_traffic(w, dec):
+    """(bytes per launch, bytes from ncu or None, note) of the decode experts:
+    fused path, the resident experts of a launch; split path, an expert launch."""
+    if dec.get("path") == "fused":
+        m = dec.get("meters") or {}
+        per = m.get("resident_bytes", 0.0) / max(1, m.get("resident_launches", 0))
+        key = "decode_layer" if w["dtype"] == 0 else "decode_layer_mxfp4"
+    else:
+        per = dec.get("ex_bytes", 0.0) / max(1, dec.get("ex_n", 0))
+        key = "decode_experts" if w["dtype"] == 0 else "decode_experts_mxfp4"
+    tr, note = ncu_traffic(key, per)
+    return per, tr, note
+
+
 def decode_summary(w, dec, peaks, link_gbs):
     """Per-workload decode figures (component form)."""
     bx = ftsynth.expert_bytes(w["d"], w["f"], w["dtype"])
@@ -1013,15 +1029,11 @@ def build_line(args, w, world, dec, link, pre, ctl, peaks, comps=None):
     fill_gbs = fill_rate(dec)
     fused = dec.get("path") == "fused"
     m = dec.get("meters") or {}
+    ex_per_launch, traffic, traffic_src = experts_traffic(w, dec)
     if fused:
-        ex_per_launch = m.get("resident_bytes", 0.0) / max(1, m.get("resident_launches", 0))
         ex_us = m.get("resident_s", 0.0) / max(1, m.get("resident_launches", 0)) * 1e6
-        traffic, traffic_src = ncu_traffic("decode_layer", ex_per_launch)
     else:
-        ex_per_launch = dec.get("ex_bytes", 0.0) / max(1, dec.get("ex_n", 0))
         ex_us = dec["ex_ms"] / max(1, dec.get("ex_n", 0)) * 1e3 if dec.get("ex_ms") else None
-        traffic, traffic_src = ncu_traffic("decode_experts" if w["dtype"] == 0 else "decode_experts_mxfp4",
-                                           ex_per_launch)
     hits, misses = dec["hits"], dec["misses"]
     cfg = line_config(args, w, world)
     line = {
@@ -1333,7 +1345,7 @@ def run_v4_components(args, local):
             hid, lg = decode_inputs(wt, n_in)
             d = run_decode_leg(args, wt, 1, local, pool, hid, lg, with_e2e=False, seq=(T == 1))
             s = decode_summary(wt, d, peaks, link["whole_pool_gbs"])
-            tr, note = ncu_traffic("decode_experts_mxfp4", d["ex_bytes"] / max(1, d["ex_n"]))
+            _, tr, note = experts_traffic(wt, d)
             s["experts_traffic_per_launch"], s["experts_traffic_source"] = tr, note
             out[f"batch_{T}"] = s
             del hid, lg

@@ -1,5 +1,5 @@
-// Fused decode layer kernel (bf16 experts): the step's fill and all of its
-// routed SwiGLU experts in one cooperative launch, one CTA per SM.
+// Fused decode layer kernel (bf16 or MXFP4 experts): the step's fill and all
+// of its routed SwiGLU experts in one cooperative launch, one CTA per SM.
 //
 // FreeToken article, section "设计：三大机制" 1, Decode bullet: the q filled
 // experts are copied from the host pool into their cache slots and then run on
@@ -26,10 +26,19 @@
 // Each CTA's producer warp takes the next item when its ring has room and
 // passes the index to the consumers through shared memory, published by the
 // mbarrier of the item's first stage; the TMA ring (up to 12 16 KB stages)
-// runs across a CTA's items, two stages per consumer iteration.
+// runs across a CTA's items.  bf16: gate/up tiles of 32 rows x 256 columns,
+// down tiles of 256 rows x 32 columns, two stages per consumer iteration.
+// MXFP4 (e2m1 codes, one e8m0 scale per 32 elements of a row): per token
+// batch a first stage with the chunk's gate/up scale bytes (two bulk copies,
+// copied to shared memory by the consumers so the ring moves on), then
+// gate/up stages of two 32-row x 256-byte code boxes and down stages of four
+// 256-row x 16-byte boxes; the arithmetic is the split MXFP4 kernel's (f16
+// activations, HFMA2 within a scale group, fp32 across groups, h in f16), the
+// down scales read through L2 (the fill may have written them in this launch).
 #include <math.h>
 
 #include "decode_bf16.cuh"
+#include "decode_mxfp4.cuh"
 #include "ft_internal.h"
 #include "tma.h"
 
@@ -37,6 +46,7 @@ namespace ft {
 namespace {
 
 constexpr int FC = kDecodeChunk;           // 32 rows of f per item
+static_assert(kDecodeChunk == kDecodeChunkFp4, "both formats use 32-row items");
 constexpr int kConsumers = 512;            // 16 consumer warps
 constexpr int kThreads = kConsumers + 32;  // + 1 producer warp
 constexpr int kQueue = 16;                 // item indices in flight between producer and consumers (> stages)
@@ -63,19 +73,21 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
 __device__ __forceinline__ void proxy_fence_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 struct Layout {
-  size_t ring, full, empty, xs, gu, hs, queue, lists, total;
+  size_t ring, full, empty, xs, gu, hs, sc, queue, lists, total;
 };
 
 // TB: tokens per pass over the weights (1 for one-token steps, else 4).
+template <bool FP4>
 __host__ __device__ inline Layout smem_layout(int d, int ns, int max_groups, int TB) {
   Layout L{};
   L.ring = 0;
   L.full = L.ring + (size_t)ns * kTile;
   L.empty = L.full + 8 * (size_t)ns;
-  L.xs = (L.empty + 8 * (size_t)ns + 15) / 16 * 16;  // [TB][d] bf16 hidden rows
-  L.gu = L.xs + (size_t)TB * d * 2;                   // [2][FC][TB] row sums
-  L.hs = L.gu + sizeof(float) * 2 * FC * TB;          // [TB][FC] h of the chunk
-  L.queue = L.hs + sizeof(float) * TB * FC;           // [kQueue] items, producer -> consumers
+  L.xs = (L.empty + 8 * (size_t)ns + 15) / 16 * 16;  // [TB][d] bf16 hidden rows (MXFP4: [TB][d/2] f16 pairs)
+  L.gu = L.xs + (size_t)TB * d * 2;                   // [2][FC][TB] row sums (MXFP4: [2 halves][2][FC][TB])
+  L.hs = L.gu + sizeof(float) * (FP4 ? 4 : 2) * FC * TB;  // [TB][FC] h of the chunk (MXFP4: [TB][FC/2] f16 pairs)
+  L.sc = L.hs + (FP4 ? 4 * (size_t)TB * (FC / 2) : sizeof(float) * TB * FC);  // MXFP4: [2][FC][d/32] scale bytes
+  L.queue = (L.sc + (FP4 ? 2 * (size_t)FC * (d / 32) : 0) + 15) / 16 * 16;  // [kQueue] items, producer -> consumers
   L.lists = L.queue + sizeof(int) * kQueue;           // [2] counts, group lists, group slots, group offsets
   L.total = L.lists + sizeof(int) * (2 + 4 * (size_t)max_groups + 1);
   return L;
@@ -140,20 +152,21 @@ __device__ void fill_role(const LayerArgs& la) {
 
 // ---------------------------------------------------------------- the kernel
 
-template <int TB>
+template <int TB, bool FP4>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
-    decode_layer_bf16_kernel(const __grid_constant__ CUtensorMap tmap_gu, const __grid_constant__ CUtensorMap tmap_wd,
-                             const LayerArgs la) {
+    decode_layer_kernel(const __grid_constant__ CUtensorMap tmap_gu, const __grid_constant__ CUtensorMap tmap_wd,
+                        const LayerArgs la) {
   const DecodeArgs& a = la.d;
   extern __shared__ __align__(1024) unsigned char dyn[];
   const int d = a.d, f = a.f, ns = la.ns;
-  const Layout Ly = smem_layout(d, ns, a.max_groups, TB);
+  const Layout Ly = smem_layout<FP4>(d, ns, a.max_groups, TB);
   unsigned char* ring = dyn + Ly.ring;
   uint64_t* full = reinterpret_cast<uint64_t*>(dyn + Ly.full);
   uint64_t* empty = reinterpret_cast<uint64_t*>(dyn + Ly.empty);
   uint16_t* xs = reinterpret_cast<uint16_t*>(dyn + Ly.xs);  // [TB][d]
   float* gu = reinterpret_cast<float*>(dyn + Ly.gu);        // [2][FC][TB]
   float* hs = reinterpret_cast<float*>(dyn + Ly.hs);        // [TB][FC]
+  unsigned char* sc = dyn + Ly.sc;                          // MXFP4: the chunk's gate/up scale bytes
   volatile int* queue = reinterpret_cast<int*>(dyn + Ly.queue);
   int* nlist = reinterpret_cast<int*>(dyn + Ly.lists);  // [0] resident, [1] installed
   int* res = nlist + 2;                                 // resident groups, ascending
@@ -247,9 +260,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int total_items = (nr + ni) * n_chunks;
   const int q = a.counts[3];
   const uint32_t now = (uint32_t)a.counts[6];
-  const int cb_n = d / 256;   // column blocks of a gate (or up) row; down tiles per batch
-  const int P1 = 2 * cb_n;    // gate/up tiles per token batch
-  const int NTL = P1 + cb_n;  // + down tiles (256 rows each)
+  const int cb_n = d / 256;   // bf16: column blocks of a gate (or up) row; down tiles per batch
+  const int P1 = 2 * cb_n;    // bf16: gate/up tiles per token batch
+  // MXFP4: 256-byte column blocks of a gate (or up) row, two per stage; 256-row down boxes, four per stage
+  const int cb4 = d / 512, gst = (cb4 + 1) / 2, nbox = d / 256, dst4 = (nbox + 3) / 4, sc_row = d / 32;
+  const int NTL = FP4 ? 1 + 2 * gst + dst4 : P1 + cb_n;  // stages per token batch
 
   // item j -> group, chunk, fill index (-1 = resident before the step)
   auto item = [&](int j, int& g, int& c, int& fi) {
@@ -313,12 +328,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int t = 0, i = 0; t < n_batches * NTL; ++t) {
           if (t > 0 && n >= ns && !mbar_wait(&empty[s], ph ^ 1u, late)) late = true;
           unsigned char* dst = ring + s * kTile;
-          mbar_expect_tx(&full[s], kTile);
-          if (i < P1) {
-            const int mtx = i < cb_n ? 0 : 1, cb = i - mtx * cb_n;
-            tensor_g2s_4d(dst, &tmap_gu, cb * 256, c * FC, mtx, slot, &full[s]);
+          if constexpr (FP4) {
+            if (i == 0) {  // the chunk's gate and up scale rows (FC x d/32 bytes each, contiguous)
+              const uint32_t scb = (uint32_t)(FC * sc_row);
+              const size_t df = (size_t)d * f;
+              const unsigned char* scg = a.arena + (size_t)slot * a.Bx + 3 * (df / 2) + (size_t)c * scb;
+              mbar_expect_tx(&full[s], 2 * scb);
+              bulk_g2s(dst, scg, scb, &full[s]);
+              bulk_g2s(dst + scb, scg + df / 32, scb, &full[s]);
+            } else if (i <= 2 * gst) {
+              const int ii = i - 1, mtx = ii < gst ? 0 : 1, cb0 = 2 * (ii - mtx * gst), nb = min(2, cb4 - cb0);
+              mbar_expect_tx(&full[s], nb * (kTile / 2));
+              for (int b2 = 0; b2 < nb; ++b2)
+                tensor_g2s_4d(dst + b2 * (kTile / 2), &tmap_gu, (cb0 + b2) * 256, c * FC, mtx, slot, &full[s]);
+            } else {
+              const int box0 = 4 * (i - 1 - 2 * gst), nb = min(4, nbox - box0);
+              mbar_expect_tx(&full[s], nb * (kTile / 4));
+              for (int b2 = 0; b2 < nb; ++b2)
+                tensor_g2s_3d(dst + b2 * (kTile / 4), &tmap_wd, c * (FC / 2), (box0 + b2) * 256, slot, &full[s]);
+            }
           } else {
-            tensor_g2s_3d(dst, &tmap_wd, c * FC, (i - P1) * 256, slot, &full[s]);
+            mbar_expect_tx(&full[s], kTile);
+            if (i < P1) {
+              const int mtx = i < cb_n ? 0 : 1, cb = i - mtx * cb_n;
+              tensor_g2s_4d(dst, &tmap_gu, cb * 256, c * FC, mtx, slot, &full[s]);
+            } else {
+              tensor_g2s_3d(dst, &tmap_wd, c * FC, (i - P1) * 256, slot, &full[s]);
+            }
           }
           if (++i == NTL) i = 0;
           if (++s == ns) {
@@ -357,11 +393,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     advance();
   };
   if (TB == 1) {
-    uint4* dst = reinterpret_cast<uint4*>(xs);
+    if constexpr (FP4) {
+      unsigned* x4 = reinterpret_cast<unsigned*>(xs);
 #pragma unroll
-    for (int j = 0; j < kXPre; ++j) {
-      const int i = tid + j * kConsumers;
-      if (i < d / 8) dst[i] = xpre[j];
+      for (int j = 0; j < kXPre; ++j) {
+        const int i = tid + j * kConsumers;
+        if (i < d / 8) {
+          x4[xs_swz(4 * i + 0)] = bf2_to_h2(xpre[j].x);
+          x4[xs_swz(4 * i + 1)] = bf2_to_h2(xpre[j].y);
+          x4[xs_swz(4 * i + 2)] = bf2_to_h2(xpre[j].z);
+          x4[xs_swz(4 * i + 3)] = bf2_to_h2(xpre[j].w);
+        }
+      }
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(xs);
+#pragma unroll
+      for (int j = 0; j < kXPre; ++j) {
+        const int i = tid + j * kConsumers;
+        if (i < d / 8) dst[i] = xpre[j];
+      }
     }
   }
   // resident-phase meter: CTAs that ran resident items stamp the end of their
@@ -412,6 +462,122 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
       for (int t = 0; t < TB; ++t) rt[t] = t < nt ? __ldg(a.group_routes + tb + t) : 0;
       consumer_sync();  // the previous batch (or item) is done with xs / hs
+      if constexpr (FP4) {
+        unsigned* x4 = reinterpret_cast<unsigned*>(xs);  // [TB][d/2] f16 pairs, swizzled
+        unsigned* h4 = reinterpret_cast<unsigned*>(hs);  // [TB][FC/2] f16 pairs
+        if (TB > 1) {
+          for (int t = 0; t < nt; ++t) {
+            const unsigned* src = reinterpret_cast<const unsigned*>(a.hidden + (size_t)(rt[t] / a.k) * d);
+            for (int i = tid; i < d / 2; i += kConsumers) x4[(size_t)t * (d / 2) + xs_swz(i)] = bf2_to_h2(src[i]);
+          }
+        }
+        // the batch's first stage: the chunk's gate/up scales, copied out so the ring moves on
+        if (!mbar_wait(&full[s], ph, late)) late = true;
+        {
+          const uint4* src = reinterpret_cast<const uint4*>(ring + s * kTile);
+          uint4* dst = reinterpret_cast<uint4*>(sc);
+          for (int i = tid; i < 2 * FC * sc_row / 16; i += kConsumers) dst[i] = src[i];
+        }
+        release();
+        consumer_sync();  // xs and the scales are in place
+        // gate/up: thread = 16-byte column piece p of rows 2rp and 2rp + 1 of column block hb of a stage
+        const int p = tid & 15, rp = (tid >> 4) & 15, hb = tid >> 8;
+        float acc[2][2][TB];  // [gate/up][row 2rp + i][token]
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int t = 0; t < TB; ++t) acc[m][i][t] = 0.f;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+#pragma unroll 1
+          for (int k2 = 0; k2 < gst; ++k2) {
+            if (!mbar_wait(&full[s], ph, late)) late = true;
+            const int cb = 2 * k2 + hb;
+            uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+            if (cb < cb4) {
+              const unsigned char* buf = ring + s * kTile + hb * (kTile / 2) + (2 * rp) * 256 + p * 16;
+              w0 = *reinterpret_cast<const uint4*>(buf);
+              w1 = *reinterpret_cast<const uint4*>(buf + 256);
+            }
+            release();
+            if (cb < cb4) {
+              const int grp = cb * 16 + p;  // scale group (and global 16-word piece) of this thread
+              const float s0 = e8m0(sc[(m * FC + 2 * rp) * sc_row + grp]);
+              const float s1 = e8m0(sc[(m * FC + 2 * rp + 1) * sc_row + grp]);
+#pragma unroll
+              for (int t = 0; t < TB; ++t) {
+                if (t < nt) {
+                  const unsigned* xrow = x4 + (size_t)t * (d / 2) + grp * 16;
+                  uint4 xv[4];
+#pragma unroll
+                  for (int c4 = 0; c4 < 4; ++c4)
+                    xv[c4] = *reinterpret_cast<const uint4*>(xrow + (((c4 + (grp >> 1)) & 3) << 2));
+                  acc[m][0][t] = fmaf(group_dot(w0, xv), s0, acc[m][0][t]);
+                  acc[m][1][t] = fmaf(group_dot(w1, xv), s1, acc[m][1][t]);
+                }
+              }
+            }
+          }
+        }
+        // row sums: the 16 pieces of a row pair are 16 consecutive lanes; the two
+        // column-block halves are added in the SwiGLU step
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int t = 0; t < TB; ++t) {
+              float v = acc[m][i][t];
+              v += __shfl_xor_sync(0xffffffffu, v, 8);
+              v += __shfl_xor_sync(0xffffffffu, v, 4);
+              v += __shfl_xor_sync(0xffffffffu, v, 2);
+              v += __shfl_xor_sync(0xffffffffu, v, 1);
+              if (p == 0 && t < nt) gu[((hb * 2 + m) * FC + 2 * rp + i) * TB + t] = v;
+            }
+        consumer_sync();
+        if (tid < (FC / 2) * TB) {
+          const int pr = tid % (FC / 2), t = tid / (FC / 2);
+          if (t < nt) {
+            auto rsum = [&](int m, int row) { return gu[(m * FC + row) * TB + t] + gu[((2 + m) * FC + row) * TB + t]; };
+            const float g0 = rsum(0, 2 * pr), u0 = rsum(1, 2 * pr), g1 = rsum(0, 2 * pr + 1), u1 = rsum(1, 2 * pr + 1);
+            const __half2 hv = __floats2half2_rn(g0 / (1.f + expf(-g0)) * u0, g1 / (1.f + expf(-g1)) * u1);
+            h4[t * (FC / 2) + pr] = *reinterpret_cast<const unsigned*>(&hv);
+          }
+        }
+        consumer_sync();
+        // down: a stage holds rows 1024 j .. 1024 j + 1023 (16 bytes each, in order);
+        // thread = rows tid and tid + 512 of the stage, one scale group each
+        const size_t df = (size_t)d * f;
+        const size_t sc_step = (size_t)512 * (f / 32);  // 512 rows of scales
+        const unsigned char* scd =
+            a.arena + (size_t)gslot[g] * a.Bx + 3 * (df / 2) + 2 * (df / 32) + (size_t)tid * (f / 32) + c;
+        unsigned e0n = tid < d ? __ldcg(scd) : 0u, e1n = tid + 512 < d ? __ldcg(scd + sc_step) : 0u;
+#pragma unroll 1
+        for (int jd = 0; jd < dst4; ++jd) {
+          const int row0 = jd * 1024 + tid, row1 = row0 + 512;
+          const float s0 = e8m0(e0n), s1 = e8m0(e1n);
+          if (jd + 1 < dst4) {
+            e0n = row0 + 1024 < d ? __ldcg(scd + (size_t)(2 * jd + 2) * sc_step) : 0u;
+            e1n = row1 + 1024 < d ? __ldcg(scd + (size_t)(2 * jd + 3) * sc_step) : 0u;
+          }
+          if (!mbar_wait(&full[s], ph, late)) late = true;
+          const unsigned char* buf = ring + s * kTile + tid * 16;
+          const uint4 w0 = row0 < d ? *reinterpret_cast<const uint4*>(buf) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 w1 = row1 < d ? *reinterpret_cast<const uint4*>(buf + kTile / 2) : make_uint4(0u, 0u, 0u, 0u);
+          release();
+#pragma unroll
+          for (int t = 0; t < TB; ++t) {
+            if (t < nt) {
+              const uint4* hp = reinterpret_cast<const uint4*>(h4 + t * (FC / 2));
+              float* yp = a.ypart + ((size_t)rt[t] * n_chunks + c) * d;
+              if (row0 < d) yp[row0] = group_dot(w0, hp) * s0;
+              if (row1 < d) yp[row1] = group_dot(w1, hp) * s1;
+            }
+          }
+        }
+      } else {
       if (TB > 1) {
         for (int t = 0; t < nt; ++t) {
           const int tok = rt[t] / a.k;
@@ -526,6 +692,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           }
         }
       }
+      }
     }
     if (j < n_res_items) {  // stamp the end of a resident item (thread 0 stands for the CTA)
       ran_resident = true;
@@ -549,10 +716,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 }  // namespace
 
-int decode_layer_ring_stages(int d, int max_groups, int smem_optin, int ctas_per_sm) {
+int decode_layer_ring_stages(int d, int max_groups, int smem_optin, int ctas_per_sm, int dtype) {
   // the shared memory of an SM holds ctas_per_sm CTAs (1 KB of it reserved per CTA)
   const size_t per_cta = (size_t)(smem_optin + 1024) / ctas_per_sm - 1024;
-  const size_t fixed = smem_layout(d, 0, max_groups, 4).total + 16 * 16 + 1024;
+  const size_t fixed = (dtype == FT_DTYPE_MXFP4 ? smem_layout<true>(d, 0, max_groups, 4).total
+                                                : smem_layout<false>(d, 0, max_groups, 4).total) +
+                       16 * 16 + 1024;
   if (per_cta <= fixed) return 0;
   return (int)std::min<size_t>(12, (per_cta - fixed) / (kTile + 16));
 }
@@ -560,17 +729,17 @@ int decode_layer_ring_stages(int d, int max_groups, int smem_optin, int ctas_per
 int decode_layer_ctas_per_sm() { return kCtasPerSm; }
 
 namespace {
-template <int TB>
+template <int TB, bool FP4>
 cudaError_t launch_tb(const LayerArgs& la, int grid, cudaStream_t st) {
   const DecodeArgs& a = la.d;
-  const size_t smem = smem_layout(a.d, la.ns, a.max_groups, TB).total;
+  const size_t smem = smem_layout<FP4>(a.d, la.ns, a.max_groups, TB).total;
   static thread_local int configured_dev = -1;
   static thread_local size_t configured_smem = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev || configured_smem < smem) {
     cudaError_t e =
-        cudaFuncSetAttribute(decode_layer_bf16_kernel<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(decode_layer_kernel<TB, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
     configured_smem = smem;
@@ -585,33 +754,40 @@ cudaError_t launch_tb(const LayerArgs& la, int grid, cudaStream_t st) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_layer_bf16_kernel<TB>, *a.tmap_gu, *a.tmap_wd, la);
+  return cudaLaunchKernelEx(&cfg, decode_layer_kernel<TB, FP4>, *a.tmap_gu, *a.tmap_wd, la);
+}
+
+template <bool FP4>
+cudaError_t max_blocks(int d, int ns, int max_groups, int* out) {
+  const size_t smem4 = smem_layout<FP4>(d, ns, max_groups, 4).total;
+  cudaError_t e =
+      cudaFuncSetAttribute(decode_layer_kernel<4, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem4);
+  if (e != cudaSuccess) return e;
+  int b4 = 0, b1 = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b4, decode_layer_kernel<4, FP4>, kThreads, smem4);
+  if (e != cudaSuccess) return e;
+  const size_t smem1 = smem_layout<FP4>(d, ns, max_groups, 1).total;
+  e = cudaFuncSetAttribute(decode_layer_kernel<1, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, decode_layer_kernel<1, FP4>, kThreads, smem1);
+  *out = std::min(b1, b4);
+  return e;
 }
 }  // namespace
 
 cudaError_t launch_decode_layer(const LayerArgs& la, int grid, cudaStream_t st) {
   const DecodeArgs& a = la.d;
-  if (a.dtype != FT_DTYPE_BF16) return cudaErrorNotSupported;
-  if (a.d > 8192 || a.d % 256 || a.f % FC || !a.tmap_wd || !a.tmap_gu || la.ns < 2 || la.ns >= kQueue ||
-      la.n_fill < 1 || la.n_fill >= grid || !la.sched)
+  const bool fp4 = a.dtype == FT_DTYPE_MXFP4;
+  if (a.dtype != FT_DTYPE_BF16 && !fp4) return cudaErrorNotSupported;
+  if (a.d > 8192 || a.d % (fp4 ? 512 : 256) || a.f % FC || !a.tmap_wd || !a.tmap_gu || la.ns < 2 ||
+      la.ns >= kQueue || la.n_fill < 1 || la.n_fill >= grid || !la.sched)
     return cudaErrorInvalidValue;
-  return a.T == 1 ? launch_tb<1>(la, grid, st) : launch_tb<4>(la, grid, st);
+  if (fp4) return a.T == 1 ? launch_tb<1, true>(la, grid, st) : launch_tb<4, true>(la, grid, st);
+  return a.T == 1 ? launch_tb<1, false>(la, grid, st) : launch_tb<4, false>(la, grid, st);
 }
 
-cudaError_t decode_layer_max_blocks_per_sm(int d, int ns, int max_groups, int* out) {
-  const size_t smem = smem_layout(d, ns, max_groups, 4).total;
-  cudaError_t e =
-      cudaFuncSetAttribute(decode_layer_bf16_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int b4 = 0, b1 = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b4, decode_layer_bf16_kernel<4>, kThreads, smem);
-  if (e != cudaSuccess) return e;
-  const size_t smem1 = smem_layout(d, ns, max_groups, 1).total;
-  e = cudaFuncSetAttribute(decode_layer_bf16_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
-  if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, decode_layer_bf16_kernel<1>, kThreads, smem1);
-  *out = std::min(b1, b4);
-  return e;
+cudaError_t decode_layer_max_blocks_per_sm(int d, int ns, int max_groups, int* out, int dtype) {
+  return dtype == FT_DTYPE_MXFP4 ? max_blocks<true>(d, ns, max_groups, out) : max_blocks<false>(d, ns, max_groups, out);
 }
 
 }  // namespace ft

@@ -20,6 +20,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include "decode_bf16.cuh"
+#include "decode_mxfp4.cuh"
 #include "ft_internal.h"
 #include "tma.h"
 
@@ -36,57 +38,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
-
-// Exact 2^(E-127) for an e8m0 byte (E = 255 is NaN, E = 0 the subnormal 2^-127).
-__device__ __forceinline__ float e8m0(unsigned e) {
-  return e == 255u ? __int_as_float(0x7FC00000) : (e ? __int_as_float((int)(e << 23)) : __int_as_float(0x00400000));
-}
-
-// Four code bytes -> four f16x2 pairs (low nibble -> low half).
-__device__ __forceinline__ void e2m1x8(unsigned w, unsigned& p0, unsigned& p1, unsigned& p2, unsigned& p3) {
-  asm("{ .reg .b8 a0, a1, a2, a3; mov.b32 {a0, a1, a2, a3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, a0; cvt.rn.f16x2.e2m1x2 %1, a1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, a2; cvt.rn.f16x2.e2m1x2 %3, a3; }"
-      : "=r"(p0), "=r"(p1), "=r"(p2), "=r"(p3)
-      : "r"(w));
-}
-
-__device__ __forceinline__ __half2 h2(unsigned v) { return *reinterpret_cast<__half2*>(&v); }
-
-// Shared-memory position of activation word i (an f16 pair) of a token row:
-// the four 16-byte chunks of each 16-word piece are rotated by (piece / 2),
-// so the 16 pieces of a column block read chunk c from all 32 banks (two
-// wavefronts) instead of two bank groups.
-__device__ __forceinline__ int xs_swz(int i) {
-  const int piece = i >> 4, c = (i >> 2) & 3;
-  return (piece << 4) | (((c + (piece >> 1)) & 3) << 2) | (i & 3);
-}
-
-// Sum over one 32-element group: 16 code bytes (w) against 16 f16x2 activation
-// pairs (x[0..3] as four uint4), returned in fp32 (unscaled).
-__device__ __forceinline__ float group_dot(const uint4 w, const uint4* x) {
-  __half2 a0 = __float2half2_rn(0.f), a1 = __float2half2_rn(0.f);
-  const unsigned ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    unsigned p0, p1, p2, p3;
-    e2m1x8(ww[i], p0, p1, p2, p3);
-    const uint4 xv = x[i];
-    if (i < 2) {
-      a0 = __hfma2(h2(p0), h2(xv.x), a0);
-      a0 = __hfma2(h2(p1), h2(xv.y), a0);
-      a0 = __hfma2(h2(p2), h2(xv.z), a0);
-      a0 = __hfma2(h2(p3), h2(xv.w), a0);
-    } else {
-      a1 = __hfma2(h2(p0), h2(xv.x), a1);
-      a1 = __hfma2(h2(p1), h2(xv.y), a1);
-      a1 = __hfma2(h2(p2), h2(xv.z), a1);
-      a1 = __hfma2(h2(p3), h2(xv.w), a1);
-    }
-  }
-  const float2 f0 = __half22float2(a0), f1 = __half22float2(a1);
-  return (f0.x + f0.y) + (f1.x + f1.y);
-}
 
 struct Layout {
   size_t ring, full, empty, scbar, sc, xs, gu, hs, rs, total;
@@ -106,22 +57,6 @@ __host__ __device__ inline Layout smem_layout(int d) {
   L.rs = L.hs + (size_t)TB * (FC / 2) * 4;                  // [TB]
   L.total = L.rs + sizeof(int) * TB;
   return L;
-}
-
-// 16-byte read-only load kept where it is written (not sunk past the branches
-// that follow), so that it overlaps the loads issued after it.
-__device__ __forceinline__ uint4 ld_nc_early(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-// bf16 pair -> f16 pair (the activations' f16 copy)
-__device__ __forceinline__ unsigned bf2_to_h2(unsigned v) {
-  const __half2 hv = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-  return *reinterpret_cast<const unsigned*>(&hv);
 }
 
 template <int TB, int NS>

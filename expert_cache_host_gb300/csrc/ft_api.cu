@@ -447,20 +447,20 @@ int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx
   }
   // The fused decode path needs one CTA per SM with a ring of at least four
   // stages; where that does not fit, the split path serves the context.
-  if (cfg->dtype == FT_DTYPE_BF16 && cfg->fill_mode == FT_FILL_KERNEL && cfg->decode_path == FT_DECODE_FUSED &&
-      cfg->hidden <= 8192) {
+  if ((cfg->dtype == FT_DTYPE_BF16 || (cfg->dtype == FT_DTYPE_MXFP4 && cfg->hidden % 512 == 0)) &&
+      cfg->fill_mode == FT_FILL_KERNEL && cfg->decode_path == FT_DECODE_FUSED && cfg->hidden <= 8192) {
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
     const int mg = std::min(TK, E);
     // as many CTAs per SM as the kernel is built for, if each still gets a ring of four stages; else one
     int want_per_sm = decode_layer_ctas_per_sm();
-    int ns = decode_layer_ring_stages(cfg->hidden, mg, optin, want_per_sm);
+    int ns = decode_layer_ring_stages(cfg->hidden, mg, optin, want_per_sm, cfg->dtype);
     if (ns < 4) {
       want_per_sm = 1;
-      ns = decode_layer_ring_stages(cfg->hidden, mg, optin, 1);
+      ns = decode_layer_ring_stages(cfg->hidden, mg, optin, 1, cfg->dtype);
     }
     int per_sm = 0;
-    if (ns >= 4 && decode_layer_max_blocks_per_sm(cfg->hidden, ns, mg, &per_sm) == cudaSuccess &&
+    if (ns >= 4 && decode_layer_max_blocks_per_sm(cfg->hidden, ns, mg, &per_sm, cfg->dtype) == cudaSuccess &&
         per_sm >= want_per_sm) {
       c->fused = true;
       c->fused_ns = ns;

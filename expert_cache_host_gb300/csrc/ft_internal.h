@@ -130,7 +130,7 @@ cudaError_t launch_decode_experts(const DecodeArgs& a, cudaStream_t st);
 // MXFP4 experts; ypart is [T*k][f/kDecodeChunkFp4][d]; tokens = T of the step.
 cudaError_t launch_decode_experts_mxfp4(const DecodeArgs& a, int tokens, cudaStream_t st);
 
-// Fused decode layer (bf16): the step's fill and all of its experts in one
+// Fused decode layer (bf16 or MXFP4): the step's fill and all of its experts in one
 // cooperative launch (decode_layer.cu).  CTAs [0, n_fill) fill first, then
 // every CTA takes (expert, 32-row chunk) work items from a device-wide
 // counter; ready[i] receives the step's clock once fetch entry i is in its
@@ -152,9 +152,9 @@ struct LayerArgs {
 };
 // Ring stages that fit one CTA per SM at hidden size d (0: none).
 // Ring stages of a fused-kernel CTA when ctas_per_sm of them share an SM (0: none fit).
-int decode_layer_ring_stages(int d, int max_groups, int smem_optin, int ctas_per_sm);
+int decode_layer_ring_stages(int d, int max_groups, int smem_optin, int ctas_per_sm, int dtype);
 int decode_layer_ctas_per_sm();  // CTAs per SM the kernel is built for (its register bound)
-cudaError_t decode_layer_max_blocks_per_sm(int d, int ns, int max_groups, int* out);
+cudaError_t decode_layer_max_blocks_per_sm(int d, int ns, int max_groups, int* out, int dtype);
 cudaError_t launch_decode_layer(const LayerArgs& la, int grid, cudaStream_t st);
 
 // out[t] = partial[t] + sum_j [slot_ids >= 0] w[t,j] * sum_c ypart[t*k+j][c]

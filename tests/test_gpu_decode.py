@@ -102,7 +102,7 @@ def run_decode(ft, model, S, K_max, r, steps, T=1, fill_mode=0, check_every=1, o
                          decode_path=decode_path, fill_ctas=fill_ctas)
     ctx = ft.ft_moe_init(cfg, model.pool.ctypes.data, model.pool.nbytes)
     try:
-        if model.dtype == 0 and fill_mode == 0:
+        if fill_mode == 0 and (model.dtype == 0 or model.d % 512 == 0):
             assert ft.ft_decode_path(ctx) == decode_path
         if cpu_exec:
             ft.ft_cpu_executor(ctx, cpu_exec)
@@ -326,24 +326,36 @@ def test_forward_without_step_is_rejected(ft):
 
 # ------------------------------------------------------------------ MXFP4 experts
 
-def test_mxfp4_decode_small(ft):
+@pytest.mark.parametrize("path", PATHS)
+def test_mxfp4_decode_small(ft, path):
     """MXFP4 experts (e2m1 codes uniform over all 16 values, e8m0 scales 119..121)."""
     model = make_model(2, 16, 2, 512, 128, dtype=1, seed=21)
-    ctx, _, worst = run_decode(ft, model, S=6, K_max=16, r=(1, 1), steps=10)
+    ctx, _, worst = run_decode(ft, model, S=6, K_max=16, r=(1, 1), steps=10, decode_path=path)
     ft.ft_moe_destroy(ctx)
 
 
-def test_mxfp4_decode_batch16_groups(ft):
+@pytest.mark.parametrize("path", PATHS)
+def test_mxfp4_decode_batch16_groups(ft, path):
     """16 tokens per step, top-6: groups of several routes share one pass over the weights."""
     model = make_model(1, 32, 6, 1024, 256, dtype=1, seed=22)
-    ctx, _, worst = run_decode(ft, model, S=40, K_max=64, r=(1, 2), steps=4, T=16)
+    ctx, _, worst = run_decode(ft, model, S=40, K_max=64, r=(1, 2), steps=4, T=16, decode_path=path)
     ft.ft_moe_destroy(ctx)
 
 
-def test_mxfp4_decode_v4_expert_shape(ft):
+@pytest.mark.parametrize("path", PATHS)
+def test_mxfp4_decode_v4_expert_shape(ft, path):
     """d=4096, f=2048 (the V4-Flash-style expert), top-6 of 16 experts, 3 steps."""
     model = make_model(1, 16, 6, 4096, 2048, dtype=1, seed=23)
-    ctx, _, worst = run_decode(ft, model, S=8, K_max=16, r=(1, 1), steps=3)
+    ctx, _, worst = run_decode(ft, model, S=8, K_max=16, r=(1, 1), steps=3, decode_path=path)
+    ft.ft_moe_destroy(ctx)
+
+
+@pytest.mark.parametrize("fill_ctas", [1, 150])
+def test_mxfp4_decode_fused_fill_ctas(ft, fill_ctas):
+    """Fused MXFP4 path with one fill CTA (every installed item waits on a long
+    fill) and with all but two CTAs filling; steps that hit and fill."""
+    model = make_model(2, 32, 6, 1024, 512, dtype=1, seed=24)
+    ctx, _, worst = run_decode(ft, model, S=20, K_max=64, r=(1, 1), steps=6, fill_ctas=fill_ctas)
     ft.ft_moe_destroy(ctx)
 
 
