@@ -464,7 +464,7 @@ def run_decode_leg(args, w, world, local, pool, hid, lg, with_e2e=True, seq=True
 
     elapsed_max, units = replica_reduce(elapsed, K * T, world)
     res.update(value=units / elapsed_max, elapsed=elapsed_max, K=K, W=W, T=T, clocks=clocks, status=status,
-               t_init=t_init, hits=hits, misses=misses, fills=fills, cpu=cpu, P=P)
+               t_init=t_init, hits=hits, misses=misses, fills=fills, cpu=cpu, P=P, bx=bx)
     if B is None and e2e_elapsed is not None:
         res.update(e2e=K * T / e2e_elapsed, h2d=int(lg[0].nbytes + hid[0].nbytes), d2h=int(L * T * d * 4))
     if prof:
@@ -976,7 +976,14 @@ def experts_rate(dec):
     (device clock).  Split path: every executed expert over the expert
     launches' CUDA-event durations (profiled tokens)."""
     m = dec.get("meters")
-    if dec.get("path") == "fused" and m and m["resident_s"] > 0:
+    if dec.get("path") == "fused":
+        if not m or m["resident_s"] <= 0:
+            return 0.0, None
+        # a phase of less than one resident expert per layer on average (hit rate ~0: the step's experts
+        # are installed by its own fill and run behind it) measures start-up, not streaming
+        per_launch = m["resident_bytes"] / max(1, m.get("resident_launches", 0))
+        if per_launch < dec.get("bx", 0):
+            return 0.0, None
         return (m["resident_bytes"] / m["resident_s"] / 1e9,
                 "fused path: resident experts' bytes / resident phase span (first compute CTA start to last "
                 "resident item end), device clock, timed window")
