@@ -33,7 +33,8 @@
 // copied to shared memory by the consumers so the ring moves on), then
 // gate/up stages of two 32-row x 256-byte code boxes and down stages of four
 // 256-row x 16-byte boxes; the arithmetic is the split MXFP4 kernel's (f16
-// activations, HFMA2 within a scale group, fp32 across groups, h in f16), the
+// activations, HFMA2 within a scale group, fp32 across groups, h in f16 under a
+// per-chunk power-of-two range scale), the
 // down scales read through L2 (the fill may have written them in this launch).
 #include <math.h>
 
@@ -86,7 +87,9 @@ __host__ __device__ inline Layout smem_layout(int d, int ns, int max_groups, int
   L.xs = (L.empty + 8 * (size_t)ns + 15) / 16 * 16;  // [TB][d] bf16 hidden rows (MXFP4: [TB][d/2] f16 pairs)
   L.gu = L.xs + (size_t)TB * d * 2;                   // [2][FC][TB] row sums (MXFP4: [2 halves][2][FC][TB])
   L.hs = L.gu + sizeof(float) * (FP4 ? 4 : 2) * FC * TB;  // [TB][FC] h of the chunk (MXFP4: [TB][FC/2] f16 pairs)
-  L.sc = L.hs + (FP4 ? 4 * (size_t)TB * (FC / 2) : sizeof(float) * TB * FC);  // MXFP4: [2][FC][d/32] scale bytes
+  // MXFP4: + [TB] range scales of h; then [2][FC][d/32] gate/up scale bytes
+  // (16-byte aligned: the consumers copy the scale bytes in with 16-byte stores)
+  L.sc = (L.hs + (FP4 ? 4 * (size_t)TB * (FC / 2) + sizeof(float) * TB : sizeof(float) * TB * FC) + 15) / 16 * 16;
   L.queue = (L.sc + (FP4 ? 2 * (size_t)FC * (d / 32) : 0) + 15) / 16 * 16;  // [kQueue] items, producer -> consumers
   L.lists = L.queue + sizeof(int) * kQueue;           // [2] counts, group lists, group slots, group offsets
   L.total = L.lists + sizeof(int) * (2 + 4 * (size_t)max_groups + 1);
@@ -465,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if constexpr (FP4) {
         unsigned* x4 = reinterpret_cast<unsigned*>(xs);  // [TB][d/2] f16 pairs, swizzled
         unsigned* h4 = reinterpret_cast<unsigned*>(hs);  // [TB][FC/2] f16 pairs
+        float* hdown = hs + TB * (FC / 2);                // [TB] 2^(e-8) of each token's h range scale
         if (TB > 1) {
           for (int t = 0; t < nt; ++t) {
             const unsigned* src = reinterpret_cast<const unsigned*>(a.hidden + (size_t)(rt[t] / a.k) * d);
@@ -537,13 +541,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               if (p == 0 && t < nt) gu[((hb * 2 + m) * FC + 2 * rp + i) * TB + t] = v;
             }
         consumer_sync();
-        if (tid < (FC / 2) * TB) {
+        if (tid < 32 * ((FC / 2 * TB + 31) / 32)) {  // whole warps: 16 lanes per token
           const int pr = tid % (FC / 2), t = tid / (FC / 2);
+          float h0 = 0.f, h1 = 0.f;
           if (t < nt) {
             auto rsum = [&](int m, int row) { return gu[(m * FC + row) * TB + t] + gu[((2 + m) * FC + row) * TB + t]; };
             const float g0 = rsum(0, 2 * pr), u0 = rsum(1, 2 * pr), g1 = rsum(0, 2 * pr + 1), u1 = rsum(1, 2 * pr + 1);
-            const __half2 hv = __floats2half2_rn(g0 / (1.f + expf(-g0)) * u0, g1 / (1.f + expf(-g1)) * u1);
+            h0 = g0 / (1.f + expf(-g0)) * u0;
+            h1 = g1 / (1.f + expf(-g1)) * u1;
+          }
+          float mx = fmaxf(fabsf(h0), fabsf(h1));
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          float up, down;
+          h_range_scale(mx, up, down);
+          if (t < nt) {
+            const __half2 hv = __floats2half2_rn(h0 * up, h1 * up);
             h4[t * (FC / 2) + pr] = *reinterpret_cast<const unsigned*>(&hv);
+            if (pr == 0) hdown[t] = down;
           }
         }
         consumer_sync();
@@ -572,8 +587,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (t < nt) {
               const uint4* hp = reinterpret_cast<const uint4*>(h4 + t * (FC / 2));
               float* yp = a.ypart + ((size_t)rt[t] * n_chunks + c) * d;
-              if (row0 < d) yp[row0] = group_dot(w0, hp) * s0;
-              if (row1 < d) yp[row1] = group_dot(w1, hp) * s1;
+              if (row0 < d) yp[row0] = group_dot(w0, hp) * (s0 * hdown[t]);
+              if (row1 < d) yp[row1] = group_dot(w1, hp) * (s1 * hdown[t]);
             }
           }
         }

@@ -63,6 +63,29 @@ __device__ __forceinline__ float group_dot(const uint4 w, const uint4* x) {
   return (f0.x + f0.y) + (f1.x + f1.y);
 }
 
+// Power-of-two range scale for the f16 copy of h: for the largest |h| of a
+// chunk (one token, 32 rows of f), `up` = 2^(8-e) brings it into [2^8, 2^9)
+// (e its binary exponent), so that h*up keeps f16's full precision and the
+// down projection's products with e2m1 values (|v| <= 6), summed 16 at a time
+// in f16, stay far below the f16 range whatever the weight scales; `down` =
+// 2^(e-8) undoes it exactly on the fp32 partial sums.  Zero, subnormal or
+// non-finite maxima take 1.
+__device__ __forceinline__ void h_range_scale(float mx, float& up, float& down) {
+  const unsigned eb = (__float_as_uint(mx) >> 23) & 255u;  // biased exponent
+  if (!(mx > 0.f) || eb == 0u || eb == 255u) {
+    up = down = 1.f;
+    return;
+  }
+  const int e = (int)eb - 127;  // -126 .. 127
+  if (e >= -118) {
+    up = __int_as_float((127 + 8 - e) << 23);    // 2^(8-e), biased exponent 8 .. 253
+    down = __int_as_float((127 - 8 + e) << 23);  // 2^(e-8), biased exponent 1 .. 246
+  } else {  // 2^(8-e) would leave the fp32 range: scale by 2^126 only
+    up = __int_as_float(253 << 23);
+    down = __int_as_float(1 << 23);
+  }
+}
+
 // bf16 pair -> f16 pair (the activations' f16 copy)
 __device__ __forceinline__ unsigned bf2_to_h2(unsigned v) {
   const __half2 hv = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));

@@ -15,7 +15,10 @@
 // the group's products with the f16 activations accumulate in two chains of
 // eight HFMA2, the group sum is widened to fp32 and multiplied by the exact
 // power of two 2^(E-127), and groups accumulate in fp32.  The intermediate h
-// is held in f16 for the down projection.  (The page keeps DSV4's experts in
+// is held in f16 for the down projection, scaled per token and chunk by a
+// power of two that puts its largest value in [2^8, 2^9) (undone exactly on
+// the fp32 partial sums), so that its range never depends on the weights'
+// scales.  (The page keeps DSV4's experts in
 // native MXFP4, "bit-identical" to the checkpoint: section "评估结果".)
 #include <cuda_fp16.h>
 #include <math.h>
@@ -40,7 +43,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
 struct Layout {
-  size_t ring, full, empty, scbar, sc, xs, gu, hs, rs, total;
+  size_t ring, full, empty, scbar, sc, xs, gu, hs, rs, hd, total;
 };
 
 template <int TB, int NS>
@@ -55,7 +58,8 @@ __host__ __device__ inline Layout smem_layout(int d) {
   L.gu = L.xs + (size_t)TB * (d / 2) * 4;                   // [2 halves][2][FC][TB] fp32 row sums
   L.hs = L.gu + sizeof(float) * 4 * FC * TB;                // [TB][FC/2] f16x2
   L.rs = L.hs + (size_t)TB * (FC / 2) * 4;                  // [TB]
-  L.total = L.rs + sizeof(int) * TB;
+  L.hd = L.rs + sizeof(int) * TB;                           // [TB] 2^(e-8) of each token's h range scale
+  L.total = L.hd + sizeof(float) * TB;
   return L;
 }
 
@@ -74,6 +78,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   unsigned* xs = reinterpret_cast<unsigned*>(dyn + Ly.xs);
   float* gu = reinterpret_cast<float*>(dyn + Ly.gu);
   unsigned* hs = reinterpret_cast<unsigned*>(dyn + Ly.hs);
+  float* hdown = reinterpret_cast<float*>(dyn + Ly.hd);
   int* rs = reinterpret_cast<int*>(dyn + Ly.rs);
 
   const int c = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
@@ -273,13 +278,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     if (tid < nt) rs[tid] = my_route;
     consumer_sync();
-    if (tid < (FC / 2) * TB) {
+    if (tid < 32 * ((FC / 2 * TB + 31) / 32)) {  // whole warps: 16 lanes per token
       const int pr = tid % (FC / 2), t = tid / (FC / 2);
+      float h0 = 0.f, h1 = 0.f;
       if (t < nt) {
         auto rsum = [&](int m, int row) { return gu[((0 * 2 + m) * FC + row) * TB + t] + gu[((1 * 2 + m) * FC + row) * TB + t]; };
         const float g0 = rsum(0, 2 * pr), u0 = rsum(1, 2 * pr), g1 = rsum(0, 2 * pr + 1), u1 = rsum(1, 2 * pr + 1);
-        const __half2 hv = __floats2half2_rn(g0 / (1.f + expf(-g0)) * u0, g1 / (1.f + expf(-g1)) * u1);
+        h0 = g0 / (1.f + expf(-g0)) * u0;
+        h1 = g1 / (1.f + expf(-g1)) * u1;
+      }
+      float mx = fmaxf(fabsf(h0), fabsf(h1));
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      float up, down;
+      h_range_scale(mx, up, down);
+      if (t < nt) {
+        const __half2 hv = __floats2half2_rn(h0 * up, h1 * up);
         hs[t * (FC / 2) + pr] = *reinterpret_cast<const unsigned*>(&hv);
+        if (pr == 0) hdown[t] = down;
       }
     }
     consumer_sync();
@@ -307,8 +323,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (t < nt) {
           const uint4* hp = reinterpret_cast<const uint4*>(hs + t * (FC / 2));
           float* yp = a.ypart + ((size_t)rs[t] * n_chunks + c) * d;
-          if (row0 < d) yp[row0] = group_dot(w0, hp) * s0;
-          if (row1 < d) yp[row1] = group_dot(w1, hp) * s1;
+          if (row0 < d) yp[row0] = group_dot(w0, hp) * (s0 * hdown[t]);
+          if (row1 < d) yp[row1] = group_dot(w1, hp) * (s1 * hdown[t]);
         }
       }
     }

@@ -350,6 +350,53 @@ def test_mxfp4_decode_v4_expert_shape(ft, path):
     ft.ft_moe_destroy(ctx)
 
 
+@pytest.mark.parametrize("path", PATHS)
+def test_mxfp4_decode_cpu_split(ft, path):
+    """r = 1/2: half of the misses arrive as the oracle's CPU partial sum and
+    merge exactly; MXFP4 experts, several tokens per step."""
+    model = make_model(2, 16, 4, 512, 256, dtype=1, seed=25)
+    ctx, _, _ = run_decode(ft, model, S=8, K_max=16, r=(1, 2), steps=8, T=4, decode_path=path)
+    cnt = ft.ft_get_counters(ctx, 2)
+    assert cnt[:, 3].sum() > 0  # some routes did go to the CPU
+    ft.ft_moe_destroy(ctx)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("T", [1, 4])
+def test_mxfp4_decode_wide_scale_range(ft, path, T):
+    """Scale bytes drawn uniformly from [100, 140] for every (row, 32-element
+    group) of every matrix: the gate/up scales the kernels stage per chunk and
+    the down scales they read per row must pair with the right codes."""
+    model = make_model(2, 16, 2, 1024, 256, dtype=1, seed=26)
+    d, f, bx = model.d, model.f, model.bx
+    rng = np.random.default_rng(77)
+    for e in range(model.L * model.E):
+        base = e * bx + 3 * d * f // 2
+        model.pool[base:base + 3 * d * f // 32] = rng.integers(100, 141, 3 * d * f // 32, dtype=np.uint8)
+    ctx, _, _ = run_decode(ft, model, S=6, K_max=16, r=(1, 1), steps=5, T=T, decode_path=path)
+    ft.ft_moe_destroy(ctx)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("d,f,T", [(1536, 256, 1), (1536, 256, 16), (8192, 128, 2)])
+def test_mxfp4_decode_shapes(ft, path, d, f, T):
+    """An odd number of 256-byte column blocks per gate row (d = 1536: a
+    half-filled last gate/up stage and down stage) and the largest hidden size
+    of the fused kernel (d = 8192)."""
+    model = make_model(2, 16, 4, d, f, dtype=1, seed=27 + d)
+    ctx, _, _ = run_decode(ft, model, S=10, K_max=16, r=(1, 1), steps=4, T=T, decode_path=path)
+    ft.ft_moe_destroy(ctx)
+
+
+def test_mxfp4_rebuild_retain_fused(ft):
+    """A retaining rebuild mid-run on the fused MXFP4 path: the kept experts'
+    bytes move to new slots and the steps after it hit on them."""
+    model = make_model(2, 16, 2, 512, 128, dtype=1, seed=28)
+    ctx, _, _ = run_decode(ft, model, S=8, K_max=16, r=(1, 1), steps=10, rebuild_at=(5, 6, "retain"))
+    assert ft.ft_get_epoch(ctx) == 1 and ft.ft_num_slots(ctx) == 6
+    ft.ft_moe_destroy(ctx)
+
+
 @pytest.mark.parametrize("fill_ctas", [1, 150])
 def test_mxfp4_decode_fused_fill_ctas(ft, fill_ctas):
     """Fused MXFP4 path with one fill CTA (every installed item waits on a long
