@@ -43,18 +43,26 @@ namespace {
 constexpr int BM = 128, BK = 64, kEpiWarps = 4, kConvWarps = 8;
 constexpr int kBaseThreads = 192;  // producer, MMA issuer, 4 epilogue warps
 
+// bf16: a tile is one 128-row M tile x 256 B rows (mode 1: 128 gate + 128 up
+// rows; mode 2: 256 rows of W_down).  MXFP4: two M tiles of the same expert
+// (256 activation rows) x 128 B rows (64 gate + 64 up; 128 of W_down), so
+// that every dequantised B tile feeds two MMAs; the two accumulators of a
+// tile (128 columns each) still leave room for a second buffer.
 template <int MODE, bool FP4>
 struct Cfg {
-  static constexpr int BN = MODE == 1 ? 128 : 256;   // output columns of a tile
-  static constexpr int B_ROWS = 256;                  // B operand rows (mode 1: BN gate + BN up rows)
-  static constexpr int NSTAGE = FP4 ? 3 : 4;
+  static constexpr int MT = FP4 ? 2 : 1;                                  // 128-row M tiles per tile
+  static constexpr int B_ROWS = FP4 ? 128 : 256;                           // B operand rows
+  static constexpr int BN = MODE == 1 ? B_ROWS / 2 : B_ROWS;               // output columns of a tile
+  static constexpr int NSTAGE = FP4 && MODE == 2 ? 3 : 4;  // MXFP4 down: room for the epilogue staging
   static constexpr int kThreads = kBaseThreads + (FP4 ? 32 * kConvWarps : 0);
-  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int A_TILE = BM * BK * 2;
+  static constexpr int A_BYTES = MT * A_TILE;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int RAW_CODES = FP4 ? B_ROWS * BK / 2 : 0;  // 32 code bytes per row per K step
   static constexpr int RAW_SC = FP4 ? B_ROWS * 16 : 0;          // scale bytes of 8 K steps per row
   static constexpr int STAGE = A_BYTES + B_BYTES + RAW_CODES + RAW_SC;  // a multiple of 1024
-  static constexpr uint32_t ACC_COLS = 256;            // fp32 columns of one accumulator buffer
+  static constexpr uint32_t ACC_COLS = 256;            // fp32 columns of one accumulator buffer (MT x B_ROWS)
+  static_assert(MT * B_ROWS == (int)ACC_COLS, "a tile's accumulators fill one buffer");
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // double buffer: all 512 columns
   // epilogue staging (mode 2): per epilogue warp, two 32-row x 128-byte boxes (4 KB each)
   static constexpr int OUT_COLS = MODE == 1 ? 64 : 32;  // output columns per 128-byte row piece (bf16 / fp32)
@@ -147,8 +155,8 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
           uint8_t* sa = smem + s * C::STAGE;
           uint8_t* sb = sa + C::A_BYTES;
           if (FP4) {
-            uint8_t* rc = sb + C::B_BYTES;  // [256 rows][32 code bytes]
-            uint8_t* rs = rc + C::RAW_CODES;  // [256 rows][16 scale bytes]
+            uint8_t* rc = sb + C::B_BYTES;    // [B_ROWS][32 code bytes]
+            uint8_t* rs = rc + C::RAW_CODES;  // [B_ROWS][16 scale bytes]
             const int xs = (kb >> 3) * 16;  // the 16 scale bytes that cover K steps 8*(kb/8) .. +7
             mbar_expect_tx(&rawf[s], C::RAW_CODES + C::RAW_SC);
             if (MODE == 1) {
@@ -161,7 +169,7 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
               tensor_g2s_3d(rs, &map_s, xs, n0, e, &rawf[s]);
             }
             mbar_expect_tx(&full[s], C::A_BYTES);
-            tensor_g2s_2d(sa, &map_a, kb * BK, r0, &full[s]);
+            for (int h = 0; h < C::MT; ++h) tensor_g2s_2d(sa + h * C::A_TILE, &map_a, kb * BK, r0 + BM * h, &full[s]);
           } else {
             mbar_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
             tensor_g2s_2d(sa, &map_a, kb * BK, r0, &full[s]);
@@ -193,8 +201,10 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
           const uint32_t sa = smem_u32(smem + s * C::STAGE), sb = sa + C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            umma_bf16(acc_tm, umma_desc_sw128(sa + kk * 32), umma_desc_sw128(sb + kk * 32), idesc,
-                      (kb | kk) ? 1u : 0u);
+#pragma unroll
+            for (int h = 0; h < C::MT; ++h)
+              umma_bf16(acc_tm + (uint32_t)(h * C::B_ROWS), umma_desc_sw128(sa + h * C::A_TILE + kk * 32),
+                        umma_desc_sw128(sb + kk * 32), idesc, (kb | kk) ? 1u : 0u);
           umma_commit(&empty[s]);
         }
         umma_commit(&accf[b]);
@@ -215,61 +225,66 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
       const int b = i & 1;
       const int mt = t / n_ntiles, n0 = (t - mt * n_ntiles) * C::BN;
-      const int e = a.tile_expert[mt], r0 = a.tile_row0[mt], r_end = a.seg_start[e + 1];
-      const int grow = r0 + row;
-      const bool valid = grow < r_end;
-      // every row of this warp is valid (warp-uniform); the bf16 H rows of
-      // mode 1 are small and go out directly, the fp32 Y rows through TMA
-      const bool whole = MODE == 2 && r0 + q * 32 + 31 < r_end;
+      const int e = a.tile_expert[mt], r_end = a.seg_start[e + 1];
       if (!mbar_wait(&accf[b], (uint32_t)((i >> 1) & 1), late)) late = true;
       tc_fence_after();
-      const uint32_t lane_addr = tmem + (uint32_t)b * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int c0 = 0; c0 < C::BN; c0 += C::OUT_COLS) {
-        uint4 packed[8];  // 128 bytes of this row's output columns c0 .. c0 + OUT_COLS
-        if (MODE == 1) {
-          uint32_t* pw = reinterpret_cast<uint32_t*>(packed);
+      for (int h = 0; h < C::MT; ++h) {  // the tile's M tiles, one accumulator each
+        const int r0 = a.tile_row0[mt] + BM * h;
+        const int grow = r0 + row;
+        const bool valid = grow < r_end;
+        // every row of this warp is valid (warp-uniform); the bf16 H rows of
+        // mode 1 are small and go out directly, the fp32 Y rows through TMA
+        const bool whole = MODE == 2 && r0 + q * 32 + 31 < r_end;
+        const uint32_t lane_addr =
+            tmem + (uint32_t)b * C::ACC_COLS + (uint32_t)(h * C::B_ROWS) + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+        for (int c0 = 0; c0 < C::BN; c0 += C::OUT_COLS) {
+          uint4 packed[8];  // 128 bytes of this row's output columns c0 .. c0 + OUT_COLS
+          if (MODE == 1) {
+            uint32_t* pw = reinterpret_cast<uint32_t*>(packed);
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float gv[32], uv[32];
-            tmem_ld32(lane_addr + c0 + 32 * half, gv);
-            tmem_ld32(lane_addr + C::BN + c0 + 32 * half, uv);
+            for (int half = 0; half < 2; ++half) {
+              float gv[32], uv[32];
+              tmem_ld32(lane_addr + c0 + 32 * half, gv);
+              tmem_ld32(lane_addr + C::BN + c0 + 32 * half, uv);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float g0 = gv[2 * j], g1 = gv[2 * j + 1];
-              // H is rounded to bf16 (8-bit mantissa) right after: the fast exp and
-              // divide (relative error ~1e-6) cannot change it beyond that rounding
-              const float h0 = __fdividef(g0, 1.f + __expf(-g0)) * uv[2 * j];
-              const float h1 = __fdividef(g1, 1.f + __expf(-g1)) * uv[2 * j + 1];
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
-              pw[16 * half + j] = *reinterpret_cast<uint32_t*>(&b2);
+              for (int j = 0; j < 16; ++j) {
+                const float g0 = gv[2 * j], g1 = gv[2 * j + 1];
+                // H is rounded to bf16 (8-bit mantissa) right after: the fast exp and
+                // divide (relative error ~1e-6) cannot change it beyond that rounding
+                const float h0 = __fdividef(g0, 1.f + __expf(-g0)) * uv[2 * j];
+                const float h1 = __fdividef(g1, 1.f + __expf(-g1)) * uv[2 * j + 1];
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
+                pw[16 * half + j] = *reinterpret_cast<uint32_t*>(&b2);
+              }
             }
+          } else {
+            float yv[32];
+            tmem_ld32(lane_addr + c0, yv);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              packed[j] = make_uint4(__float_as_uint(yv[4 * j]), __float_as_uint(yv[4 * j + 1]),
+                                     __float_as_uint(yv[4 * j + 2]), __float_as_uint(yv[4 * j + 3]));
           }
-        } else {
-          float yv[32];
-          tmem_ld32(lane_addr + c0, yv);
+          if (whole) {
+            uint8_t* buf = my_stg + nbuf * 4096;
+            if (lane == 0) bulk_wait_read<1>();  // the store issued from this buffer two boxes ago has read it
+            __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            packed[j] = make_uint4(__float_as_uint(yv[4 * j]), __float_as_uint(yv[4 * j + 1]),
-                                   __float_as_uint(yv[4 * j + 2]), __float_as_uint(yv[4 * j + 3]));
-        }
-        if (whole) {
-          uint8_t* buf = my_stg + nbuf * 4096;
-          if (lane == 0) bulk_wait_read<1>();  // the store issued from this buffer two boxes ago has read it
-          __syncwarp();
+            for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(buf + stg_off(lane, j)) = packed[j];
+            proxy_fence_writes();
+            __syncwarp();
+            if (lane == 0) {
+              tensor_s2g_2d(&map_out, n0 + c0, r0 + q * 32, buf);
+              bulk_commit();
+            }
+            nbuf ^= 1;
+          } else if (valid) {
+            uint8_t* dst = reinterpret_cast<uint8_t*>(a.out) + ((size_t)grow * a.out_ld + n0 + c0) * (MODE == 1 ? 2 : 4);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(buf + stg_off(lane, j)) = packed[j];
-          proxy_fence_writes();
-          __syncwarp();
-          if (lane == 0) {
-            tensor_s2g_2d(&map_out, n0 + c0, r0 + q * 32, buf);
-            bulk_commit();
+            for (int j = 0; j < 8; ++j) reinterpret_cast<uint4*>(dst)[j] = packed[j];
           }
-          nbuf ^= 1;
-        } else if (valid) {
-          uint8_t* dst = reinterpret_cast<uint8_t*>(a.out) + ((size_t)grow * a.out_ld + n0 + c0) * (MODE == 1 ? 2 : 4);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) reinterpret_cast<uint4*>(dst)[j] = packed[j];
         }
       }
       // this warp's reads of the buffer are done: hand it back to the MMA issuer
@@ -279,9 +294,10 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
     }
     if (lane == 0) bulk_wait_all();  // every store of this warp has landed before the CTA exits
   } else if (FP4) {
-    // converters: 256 threads, two (row, 32-element group) units each per K
-    // step; a warp covers 16 rows, so its 16-byte code reads are contiguous
-    // and each quarter-warp's four 16-byte chunk stores hit distinct banks.
+    // converters: 256 threads, B_ROWS * 2 / 256 (row, 32-element group) units
+    // each per K step; a warp covers 16 rows, so its 16-byte code reads are
+    // contiguous and each quarter-warp's four 16-byte chunk stores hit
+    // distinct banks.
     const int ct = threadIdx.x - kBaseThreads;
     uint32_t it = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
@@ -292,7 +308,7 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
         const uint8_t* rc = sb + C::B_BYTES;
         const uint8_t* rs = rc + C::RAW_CODES;
 #pragma unroll
-        for (int u2 = 0; u2 < 2; ++u2) {
+        for (int u2 = 0; u2 < C::B_ROWS * 2 / 256; ++u2) {
           const int u = ct + 256 * u2, r = u >> 1, h = u & 1;
           const uint4 cw = *reinterpret_cast<const uint4*>(rc + r * 32 + h * 16);
           const float sc = e8m0_scale(rs[r * 16 + (kb & 7) * 2 + h]);

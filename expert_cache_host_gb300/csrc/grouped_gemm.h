@@ -10,9 +10,9 @@
 namespace ft {
 
 struct GemmArgs {
-  const int32_t* n_mtiles;     // device: number of valid M tiles
-  const int32_t* tile_expert;  // [max_mtiles] expert of each M tile
-  const int32_t* tile_row0;    // [max_mtiles] first sorted row of each M tile
+  const int32_t* n_mtiles;     // device: number of valid tiles (bf16: 128 rows; MXFP4: 256 rows)
+  const int32_t* tile_expert;  // [max_mtiles] expert of each tile
+  const int32_t* tile_row0;    // [max_mtiles] first sorted row of each tile
   const int32_t* seg_start;    // [E + 1] first sorted row of each expert's segment
   void* out;                   // mode 1: H bf16 [rows, f]; mode 2: Y fp32 [rows, d]
   int out_ld;                  // elements per output row
@@ -34,14 +34,15 @@ cudaError_t launch_gemm_down(const CUtensorMap* map_h, const CUtensorMap* map_w2
                              const GemmArgs& a, int max_mtiles, int d, cudaStream_t st);
 
 // MXFP4 weights (e2m1 codes + e8m0 scales, the canonical expert layout),
-// dequantised to bf16 in shared memory; d and f multiples of 512.
-// map_c1: 4-D uint8 (d/2, f, {gate, up}, expert), box 32 x 128 x 1 x 1;
-// map_s1: 4-D uint8 (d/32, f, {gate, up}, expert), box 16 x 128 x 1 x 1.
+// dequantised to bf16 in shared memory; d and f multiples of 512.  The tile
+// list (GemmArgs n_mtiles / tile_expert / tile_row0) holds 256-row tiles.
+// map_c1: 4-D uint8 (d/2, f, {gate, up}, expert), box 32 x 64 x 1 x 1;
+// map_s1: 4-D uint8 (d/32, f, {gate, up}, expert), box 16 x 64 x 1 x 1.
 cudaError_t launch_gemm_gateup_mxfp4(const CUtensorMap* map_x, const CUtensorMap* map_c1, const CUtensorMap* map_s1,
                                      const CUtensorMap* map_h_out, const GemmArgs& a, int max_mtiles, int f,
                                      cudaStream_t st);
 
-// map_c2: 3-D uint8 (f/2, d, expert), box 32 x 256 x 1; map_s2: 3-D uint8 (f/32, d, expert), box 16 x 256 x 1.
+// map_c2: 3-D uint8 (f/2, d, expert), box 32 x 128 x 1; map_s2: 3-D uint8 (f/32, d, expert), box 16 x 128 x 1.
 cudaError_t launch_gemm_down_mxfp4(const CUtensorMap* map_h, const CUtensorMap* map_c2, const CUtensorMap* map_s2,
                                    const CUtensorMap* map_y_out, const GemmArgs& a, int max_mtiles, int d,
                                    cudaStream_t st);

@@ -45,6 +45,11 @@ struct PrefillState {
   int32_t* n_mtiles = nullptr;
   int32_t* tile_expert = nullptr;
   int32_t* tile_row0 = nullptr;
+  // MXFP4 GEMMs: tiles of two 128-row M tiles (256 rows) of one expert
+  int32_t* n_mtiles2 = nullptr;
+  int32_t* tile2_expert = nullptr;
+  int32_t* tile2_row0 = nullptr;
+  int max_mtiles2 = 0;
   int32_t* perm = nullptr;
   int32_t* inv = nullptr;
   uint16_t* xs = nullptr;
@@ -56,17 +61,19 @@ namespace {
 
 constexpr int kScanThreads = 1024;
 
-// Segment offsets of the counting sort and the list of 128-row M tiles.
+// Segment offsets of the counting sort, the list of 128-row M tiles and the
+// list of 256-row tiles (pairs of M tiles, the last one ragged).
 __global__ void __launch_bounds__(kScanThreads)
     scan_kernel(const int32_t* __restrict__ hist, int E, int32_t* __restrict__ seg_start, int32_t* __restrict__ cursor,
-                int32_t* __restrict__ n_mtiles, int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row0) {
+                int32_t* __restrict__ n_mtiles, int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row0,
+                int32_t* __restrict__ n_mtiles2, int32_t* __restrict__ tile2_expert, int32_t* __restrict__ tile2_row0) {
   __shared__ int wsum[32];
   const int e = threadIdx.x, lane = e & 31, wid = e >> 5;
   const int c = e < E ? hist[e] : 0;
-  const int mt = (c + 127) / 128;
-  int res[2];
-  const int v[2] = {c, mt};
-  for (int p = 0; p < 2; ++p) {
+  const int mt = (c + 127) / 128, mt2 = (c + 255) / 256;
+  int res[3];
+  const int v[3] = {c, mt, mt2};
+  for (int p = 0; p < 3; ++p) {
     int x = v[p];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -88,7 +95,8 @@ __global__ void __launch_bounds__(kScanThreads)
     res[p] = (wid ? wsum[wid - 1] : 0) + x - v[p];
     if (e == kScanThreads - 1) {
       if (p == 0) seg_start[E] = wsum[31];
-      else *n_mtiles = wsum[31];
+      else if (p == 1) *n_mtiles = wsum[31];
+      else *n_mtiles2 = wsum[31];
     }
     __syncthreads();
   }
@@ -98,6 +106,10 @@ __global__ void __launch_bounds__(kScanThreads)
     for (int i = 0; i < mt; ++i) {
       tile_expert[res[1] + i] = e;
       tile_row0[res[1] + i] = res[0] + 128 * i;
+    }
+    for (int i = 0; i < mt2; ++i) {
+      tile2_expert[res[2] + i] = e;
+      tile2_row0[res[2] + i] = res[0] + 256 * i;
     }
   }
 }
@@ -148,14 +160,15 @@ bool make_weight_maps(PrefillState* p, int b, char* msg, size_t n) {
     // canonical MXFP4 expert: [codes gate | up | down | scales gate | up | down]
     const uint64_t df = d * f;
     const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    // boxes: 64 gate (up) rows per gate/up tile, 128 W_down rows per down tile
     const uint64_t c1_dims[4] = {d / 2, f, 2, E}, c1_str[3] = {d / 2, df / 2, Bx};
-    const uint32_t c1_box[4] = {32, 128, 1, 1};
+    const uint32_t c1_box[4] = {32, 64, 1, 1};
     const uint64_t s1_dims[4] = {d / 32, f, 2, E}, s1_str[3] = {d / 32, df / 32, Bx};
-    const uint32_t s1_box[4] = {16, 128, 1, 1};
+    const uint32_t s1_box[4] = {16, 64, 1, 1};
     const uint64_t c2_dims[3] = {f / 2, d, E}, c2_str[2] = {f / 2, Bx};
-    const uint32_t c2_box[3] = {32, 256, 1};
+    const uint32_t c2_box[3] = {32, 128, 1};
     const uint64_t s2_dims[3] = {f / 32, d, E}, s2_str[2] = {f / 32, Bx};
-    const uint32_t s2_box[3] = {16, 256, 1};
+    const uint32_t s2_box[3] = {16, 128, 1};
     return encode_tensor_map(&p->map_w1[b], u8, 4, lb, c1_dims, c1_str, c1_box, msg, n) &&
            encode_tensor_map(&p->map_s1[b], u8, 4, lb + 3 * df / 2, s1_dims, s1_str, s1_box, msg, n) &&
            encode_tensor_map(&p->map_w2[b], u8, 3, lb + df, c2_dims, c2_str, c2_box, msg, n) &&
@@ -219,6 +232,9 @@ void prefill_destroy(PrefillState* p) {
   cudaFree(p->n_mtiles);
   cudaFree(p->tile_expert);
   cudaFree(p->tile_row0);
+  cudaFree(p->n_mtiles2);
+  cudaFree(p->tile2_expert);
+  cudaFree(p->tile2_row0);
   cudaFree(p->perm);
   cudaFree(p->inv);
   cudaFree(p->xs);
@@ -238,12 +254,14 @@ PrefillState* prefill_create(const PrefillConfig& cfg, char* msg, size_t msg_len
   p->cfg = cfg;
   p->rows_cap = cfg.t_max * cfg.k;
   p->max_mtiles = (p->rows_cap + 127) / 128 + cfg.E;
+  p->max_mtiles2 = (p->rows_cap + 255) / 256 + cfg.E;
   const size_t layer_bytes = (size_t)cfg.E * cfg.Bx;
   bool ok = true;
   for (int b = 0; b < cfg.buffers; ++b) ok = ok && dalloc(&p->lbuf[b], layer_bytes);
   ok = ok && dalloc(&p->ids, p->rows_cap) && dalloc(&p->w, p->rows_cap) && dalloc(&p->hist, cfg.E) &&
        dalloc(&p->seg_start, cfg.E + 1) && dalloc(&p->cursor, cfg.E) && dalloc(&p->n_mtiles, 1) &&
        dalloc(&p->tile_expert, p->max_mtiles) && dalloc(&p->tile_row0, p->max_mtiles) &&
+       dalloc(&p->n_mtiles2, 1) && dalloc(&p->tile2_expert, p->max_mtiles2) && dalloc(&p->tile2_row0, p->max_mtiles2) &&
        dalloc(&p->perm, p->rows_cap) && dalloc(&p->inv, p->rows_cap) &&
        dalloc(&p->xs, (size_t)p->rows_cap * cfg.d) && dalloc(&p->hbuf, (size_t)p->rows_cap * cfg.f) &&
        dalloc(&p->ybuf, (size_t)p->rows_cap * cfg.d);
@@ -319,7 +337,7 @@ int prefill_forward(PrefillState* p, int layer, const float* logits, const uint1
   if (e == cudaSuccess) e = launch_route(logits, T, c.E, c.k, p->ids, p->w, c.status, p->hist, st);
   if (e == cudaSuccess) {
     scan_kernel<<<1, kScanThreads, 0, st>>>(p->hist, c.E, p->seg_start, p->cursor, p->n_mtiles, p->tile_expert,
-                                            p->tile_row0);
+                                            p->tile_row0, p->n_mtiles2, p->tile2_expert, p->tile2_row0);
     scatter_kernel<<<(n_routes + 255) / 256, 256, 0, st>>>(p->ids, n_routes, p->seg_start, p->cursor, p->perm, p->inv);
     gather_kernel<<<(n_routes + 7) / 8, 256, 0, st>>>(reinterpret_cast<const uint4*>(hidden), p->perm, n_routes, c.k,
                                                       c.d / 8, reinterpret_cast<uint4*>(p->xs));
@@ -331,23 +349,27 @@ int prefill_forward(PrefillState* p, int layer, const float* logits, const uint1
   ga.tile_row0 = p->tile_row0;
   ga.seg_start = p->seg_start;
   ga.status = c.status;
-  const int max_mt = (n_routes + 127) / 128 + c.E;
+  const bool fp4 = c.dtype == FT_DTYPE_MXFP4;
+  if (fp4) {  // the MXFP4 GEMMs walk 256-row tiles
+    ga.n_mtiles = p->n_mtiles2;
+    ga.tile_expert = p->tile2_expert;
+    ga.tile_row0 = p->tile2_row0;
+  }
+  const int max_mt = fp4 ? (n_routes + 255) / 256 + c.E : (n_routes + 127) / 128 + c.E;
   if (prof) prof->end(st, FT_K_PREFILL, pb);
   pb = prof ? prof->begin(st) : nullptr;
   if (e == cudaSuccess) {
     ga.out = p->hbuf;
     ga.out_ld = c.f;
     ga.K = c.d;
-    e = c.dtype == FT_DTYPE_MXFP4
-            ? launch_gemm_gateup_mxfp4(&p->map_x, &p->map_w1[b], &p->map_s1[b], &p->map_h_out, ga, max_mt, c.f, st)
+    e = fp4 ? launch_gemm_gateup_mxfp4(&p->map_x, &p->map_w1[b], &p->map_s1[b], &p->map_h_out, ga, max_mt, c.f, st)
             : launch_gemm_gateup(&p->map_x, &p->map_w1[b], &p->map_h_out, ga, max_mt, c.f, st);
   }
   if (e == cudaSuccess) {
     ga.out = p->ybuf;
     ga.out_ld = c.d;
     ga.K = c.f;
-    e = c.dtype == FT_DTYPE_MXFP4
-            ? launch_gemm_down_mxfp4(&p->map_h, &p->map_w2[b], &p->map_s2[b], &p->map_y_out, ga, max_mt, c.d, st)
+    e = fp4 ? launch_gemm_down_mxfp4(&p->map_h, &p->map_w2[b], &p->map_s2[b], &p->map_y_out, ga, max_mt, c.d, st)
             : launch_gemm_down(&p->map_h, &p->map_w2[b], &p->map_y_out, ga, max_mt, c.d, st);
   }
   if (prof) prof->end(st, FT_K_GEMM, pb);
