@@ -40,35 +40,41 @@
 namespace ft {
 namespace {
 
-constexpr int BM = 128, BK = 64, kEpiWarps = 4, kConvWarps = 8;
-constexpr int kBaseThreads = 192;  // producer, MMA issuer, 4 epilogue warps
+constexpr int BM = 128, BK = 64, kConvWarps = 8;
 
-// bf16: a tile is one 128-row M tile x 256 B rows (mode 1: 128 gate + 128 up
-// rows; mode 2: 256 rows of W_down).  MXFP4: two M tiles of the same expert
-// (256 activation rows) x 128 B rows (64 gate + 64 up; 128 of W_down), so
-// that every dequantised B tile feeds two MMAs; the two accumulators of a
-// tile (128 columns each) still leave room for a second buffer.
+// A tile is up to MT 128-row M tiles of one expert (the tile list says how
+// many) x B_ROWS rows of the B operand:
+//   bf16: 1 M tile x 256 B rows (gate/up: 128 gate + 128 up; down: 256 rows
+//     of W_down), accumulators double-buffered;
+//   MXFP4: 2 M tiles x 128 B rows (64 gate + 64 up; 128 rows of W_down): every
+//     dequantised B tile feeds two MMAs, accumulators double-buffered.
+// (A single accumulator buffer -- MT x B_ROWS = 512 columns -- gets 8
+// epilogue warps, so that its drain, which the MMAs then wait for, is short.)
 template <int MODE, bool FP4>
 struct Cfg {
-  static constexpr int MT = FP4 ? 2 : 1;                                  // 128-row M tiles per tile
+  static constexpr int MT = FP4 ? 2 : 1;                                   // max 128-row M tiles per tile
   static constexpr int B_ROWS = FP4 ? 128 : 256;                           // B operand rows
   static constexpr int BN = MODE == 1 ? B_ROWS / 2 : B_ROWS;               // output columns of a tile
-  static constexpr int NSTAGE = FP4 && MODE == 2 ? 3 : 4;  // MXFP4 down: room for the epilogue staging
-  static constexpr int kThreads = kBaseThreads + (FP4 ? 32 * kConvWarps : 0);
+  static constexpr uint32_t ACC_COLS = MT * B_ROWS;                        // fp32 columns of one buffer
+  static constexpr int NBUF = 512 / ACC_COLS;                              // accumulator buffers
+  static constexpr uint32_t TMEM_COLS = NBUF * ACC_COLS;                   // all 512 columns
+  static constexpr int EPI = NBUF == 1 ? 8 : 4;                            // epilogue warps
+  static constexpr int kThreads = 64 + 32 * EPI + (FP4 ? 32 * kConvWarps : 0);
+  static constexpr int CONV0 = 2 + EPI;                                    // first converter warp
   static constexpr int A_TILE = BM * BK * 2;
   static constexpr int A_BYTES = MT * A_TILE;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int RAW_CODES = FP4 ? B_ROWS * BK / 2 : 0;  // 32 code bytes per row per K step
   static constexpr int RAW_SC = FP4 ? B_ROWS * 16 : 0;          // scale bytes of 8 K steps per row
   static constexpr int STAGE = A_BYTES + B_BYTES + RAW_CODES + RAW_SC;  // a multiple of 1024
-  static constexpr uint32_t ACC_COLS = 256;            // fp32 columns of one accumulator buffer (MT x B_ROWS)
-  static_assert(MT * B_ROWS == (int)ACC_COLS, "a tile's accumulators fill one buffer");
-  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // double buffer: all 512 columns
+  static constexpr int NSTAGE = FP4 && MODE == 2 ? 3 : 4;  // MXFP4 down: room for the epilogue staging
   // epilogue staging (mode 2): per epilogue warp, two 32-row x 128-byte boxes (4 KB each)
   static constexpr int OUT_COLS = MODE == 1 ? 64 : 32;  // output columns per 128-byte row piece (bf16 / fp32)
-  static constexpr int STG_BYTES = MODE == 2 ? kEpiWarps * 2 * 4096 : 0;
+  static constexpr int STG_BYTES = MODE == 2 ? EPI * 2 * 4096 : 0;
   static constexpr size_t SMEM = (size_t)NSTAGE * STAGE + STG_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(STAGE % 1024 == 0, "stage tiles must stay 1024-byte aligned for the 128-byte swizzle");
+  static_assert(NBUF * ACC_COLS == 512 && (NBUF == 1 || NBUF == 2), "accumulators fill the tensor memory");
+  static_assert(BN % ((EPI / 4) * OUT_COLS) == 0, "epilogue warps split the columns evenly");
 };
 
 // Exact 2^(s-127) for an e8m0 byte (s = 255 is NaN, s = 0 the fp32 subnormal 2^-127).
@@ -130,9 +136,9 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
       mbar_init(&empty[s], 1);
       mbar_init(&rawf[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NBUF; ++b) {
       mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], kEpiWarps);
+      mbar_init(&acce[b], C::EPI);
     }
     mbar_init_fence();
   }
@@ -149,6 +155,7 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
       for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
         const int mt = t / n_ntiles, n0 = (t - mt * n_ntiles) * C::BN;
         const int e = a.tile_expert[mt], r0 = a.tile_row0[mt];
+        const int mc = C::MT == 1 ? 1 : (a.tile_mcnt ? a.tile_mcnt[mt] : C::MT);  // M tiles of this tile (1 .. MT)
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % NSTAGE;
           if (it >= NSTAGE && !mbar_wait(&empty[s], (uint32_t)(((it / NSTAGE) - 1) & 1), late)) late = true;
@@ -168,11 +175,11 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
               tensor_g2s_3d(rc, &map_b, kb * (BK / 2), n0, e, &rawf[s]);
               tensor_g2s_3d(rs, &map_s, xs, n0, e, &rawf[s]);
             }
-            mbar_expect_tx(&full[s], C::A_BYTES);
-            for (int h = 0; h < C::MT; ++h) tensor_g2s_2d(sa + h * C::A_TILE, &map_a, kb * BK, r0 + BM * h, &full[s]);
+            mbar_expect_tx(&full[s], mc * C::A_TILE);
+            for (int h = 0; h < mc; ++h) tensor_g2s_2d(sa + h * C::A_TILE, &map_a, kb * BK, r0 + BM * h, &full[s]);
           } else {
-            mbar_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
-            tensor_g2s_2d(sa, &map_a, kb * BK, r0, &full[s]);
+            mbar_expect_tx(&full[s], mc * C::A_TILE + C::B_BYTES);
+            for (int h = 0; h < mc; ++h) tensor_g2s_2d(sa + h * C::A_TILE, &map_a, kb * BK, r0 + BM * h, &full[s]);
             if (MODE == 1) {
               tensor_g2s_4d(sb, &map_b, kb * BK, n0, 0, e, &full[s]);
               tensor_g2s_4d(sb + C::B_BYTES / 2, &map_b, kb * BK, n0, 1, e, &full[s]);
@@ -189,9 +196,10 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
       uint32_t it = 0;
       int i = 0;  // tiles of this CTA so far
       for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
-        const int b = i & 1;
-        // the epilogue must have drained this buffer (tile i - 2)
-        if (i >= 2 && !mbar_wait(&acce[b], (uint32_t)(((i >> 1) - 1) & 1), late)) late = true;
+        const int b = i % C::NBUF;
+        const int mc = C::MT == 1 ? 1 : (a.tile_mcnt ? a.tile_mcnt[t / n_ntiles] : C::MT);
+        // the epilogue must have drained this buffer (tile i - NBUF)
+        if (i >= C::NBUF && !mbar_wait(&acce[b], (uint32_t)(((i / C::NBUF) - 1) & 1), late)) late = true;
         tc_fence_after();
         const uint32_t acc_tm = tmem + (uint32_t)b * C::ACC_COLS;
         for (int kb = 0; kb < KB; ++kb, ++it) {
@@ -203,33 +211,38 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
           for (int kk = 0; kk < BK / 16; ++kk)
 #pragma unroll
             for (int h = 0; h < C::MT; ++h)
-              umma_bf16(acc_tm + (uint32_t)(h * C::B_ROWS), umma_desc_sw128(sa + h * C::A_TILE + kk * 32),
-                        umma_desc_sw128(sb + kk * 32), idesc, (kb | kk) ? 1u : 0u);
+              if (h < mc)
+                umma_bf16(acc_tm + (uint32_t)(h * C::B_ROWS), umma_desc_sw128(sa + h * C::A_TILE + kk * 32),
+                          umma_desc_sw128(sb + kk * 32), idesc, (kb | kk) ? 1u : 0u);
           umma_commit(&empty[s]);
         }
         umma_commit(&accf[b]);
       }
     }
-  } else if (warp < 2 + kEpiWarps) {
+  } else if (warp < C::CONV0) {
     // epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 (one row each).
     // Mode 2: a warp whose 32 rows all belong to the segment stages them in
     // shared memory (128-byte swizzle) and writes each 32-row x 128-byte box
     // with one TMA store (32 scattered 16-byte row pieces per store
     // instruction were bound by L2 write requests); otherwise valid rows are
     // stored directly.
-    const int q = warp & 3;
+    // A warp reads the tensor-memory lane quarter warp % 4; with 8 epilogue
+    // warps, warps w and w + 4 share a quarter and split its columns.
+    const int ew = warp - 2, q = warp & 3, cs = ew >> 2;
+    constexpr int CSTEP = (C::EPI / 4) * C::OUT_COLS;
     const int row = q * 32 + lane;
-    uint8_t* my_stg = stg + q * 2 * 4096;
+    uint8_t* my_stg = stg + ew * 2 * 4096;
     int nbuf = 0;  // staging buffer to fill next (0/1)
     int i = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
-      const int b = i & 1;
+      const int b = i % C::NBUF;
       const int mt = t / n_ntiles, n0 = (t - mt * n_ntiles) * C::BN;
       const int e = a.tile_expert[mt], r_end = a.seg_start[e + 1];
-      if (!mbar_wait(&accf[b], (uint32_t)((i >> 1) & 1), late)) late = true;
+      const int mc = C::MT == 1 ? 1 : (a.tile_mcnt ? a.tile_mcnt[mt] : C::MT);
+      if (!mbar_wait(&accf[b], (uint32_t)((i / C::NBUF) & 1), late)) late = true;
       tc_fence_after();
 #pragma unroll 1
-      for (int h = 0; h < C::MT; ++h) {  // the tile's M tiles, one accumulator each
+      for (int h = 0; h < mc; ++h) {  // the tile's M tiles, one accumulator each
         const int r0 = a.tile_row0[mt] + BM * h;
         const int grow = r0 + row;
         const bool valid = grow < r_end;
@@ -239,7 +252,7 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
         const uint32_t lane_addr =
             tmem + (uint32_t)b * C::ACC_COLS + (uint32_t)(h * C::B_ROWS) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-        for (int c0 = 0; c0 < C::BN; c0 += C::OUT_COLS) {
+        for (int c0 = cs * C::OUT_COLS; c0 < C::BN; c0 += CSTEP) {
           uint4 packed[8];  // 128 bytes of this row's output columns c0 .. c0 + OUT_COLS
           if (MODE == 1) {
             uint32_t* pw = reinterpret_cast<uint32_t*>(packed);
@@ -298,7 +311,7 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
     // each per K step; a warp covers 16 rows, so its 16-byte code reads are
     // contiguous and each quarter-warp's four 16-byte chunk stores hit
     // distinct banks.
-    const int ct = threadIdx.x - kBaseThreads;
+    const int ct = threadIdx.x - 32 * C::CONV0;
     uint32_t it = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
       for (int kb = 0; kb < KB; ++kb, ++it) {

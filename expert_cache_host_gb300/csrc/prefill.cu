@@ -45,10 +45,12 @@ struct PrefillState {
   int32_t* n_mtiles = nullptr;
   int32_t* tile_expert = nullptr;
   int32_t* tile_row0 = nullptr;
-  // MXFP4 GEMMs: tiles of two 128-row M tiles (256 rows) of one expert
+  // tiles of two 128-row M tiles of one expert (an expert's last tile holds
+  // one when its M-tile count is odd): the MXFP4 GEMMs
   int32_t* n_mtiles2 = nullptr;
   int32_t* tile2_expert = nullptr;
   int32_t* tile2_row0 = nullptr;
+  int32_t* tile2_mcnt = nullptr;
   int max_mtiles2 = 0;
   int32_t* perm = nullptr;
   int32_t* inv = nullptr;
@@ -62,11 +64,13 @@ namespace {
 constexpr int kScanThreads = 1024;
 
 // Segment offsets of the counting sort, the list of 128-row M tiles and the
-// list of 256-row tiles (pairs of M tiles, the last one ragged).
+// list of tiles of two M tiles (an expert's last one holds one when its
+// M-tile count is odd).
 __global__ void __launch_bounds__(kScanThreads)
     scan_kernel(const int32_t* __restrict__ hist, int E, int32_t* __restrict__ seg_start, int32_t* __restrict__ cursor,
                 int32_t* __restrict__ n_mtiles, int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row0,
-                int32_t* __restrict__ n_mtiles2, int32_t* __restrict__ tile2_expert, int32_t* __restrict__ tile2_row0) {
+                int32_t* __restrict__ n_mtiles2, int32_t* __restrict__ tile2_expert, int32_t* __restrict__ tile2_row0,
+                int32_t* __restrict__ tile2_mcnt) {
   __shared__ int wsum[32];
   const int e = threadIdx.x, lane = e & 31, wid = e >> 5;
   const int c = e < E ? hist[e] : 0;
@@ -110,6 +114,7 @@ __global__ void __launch_bounds__(kScanThreads)
     for (int i = 0; i < mt2; ++i) {
       tile2_expert[res[2] + i] = e;
       tile2_row0[res[2] + i] = res[0] + 256 * i;
+      tile2_mcnt[res[2] + i] = mt - 2 * i >= 2 ? 2 : 1;
     }
   }
 }
@@ -235,6 +240,7 @@ void prefill_destroy(PrefillState* p) {
   cudaFree(p->n_mtiles2);
   cudaFree(p->tile2_expert);
   cudaFree(p->tile2_row0);
+  cudaFree(p->tile2_mcnt);
   cudaFree(p->perm);
   cudaFree(p->inv);
   cudaFree(p->xs);
@@ -262,6 +268,7 @@ PrefillState* prefill_create(const PrefillConfig& cfg, char* msg, size_t msg_len
        dalloc(&p->seg_start, cfg.E + 1) && dalloc(&p->cursor, cfg.E) && dalloc(&p->n_mtiles, 1) &&
        dalloc(&p->tile_expert, p->max_mtiles) && dalloc(&p->tile_row0, p->max_mtiles) &&
        dalloc(&p->n_mtiles2, 1) && dalloc(&p->tile2_expert, p->max_mtiles2) && dalloc(&p->tile2_row0, p->max_mtiles2) &&
+       dalloc(&p->tile2_mcnt, p->max_mtiles2) &&
        dalloc(&p->perm, p->rows_cap) && dalloc(&p->inv, p->rows_cap) &&
        dalloc(&p->xs, (size_t)p->rows_cap * cfg.d) && dalloc(&p->hbuf, (size_t)p->rows_cap * cfg.f) &&
        dalloc(&p->ybuf, (size_t)p->rows_cap * cfg.d);
@@ -337,40 +344,42 @@ int prefill_forward(PrefillState* p, int layer, const float* logits, const uint1
   if (e == cudaSuccess) e = launch_route(logits, T, c.E, c.k, p->ids, p->w, c.status, p->hist, st);
   if (e == cudaSuccess) {
     scan_kernel<<<1, kScanThreads, 0, st>>>(p->hist, c.E, p->seg_start, p->cursor, p->n_mtiles, p->tile_expert,
-                                            p->tile_row0, p->n_mtiles2, p->tile2_expert, p->tile2_row0);
+                                            p->tile_row0, p->n_mtiles2, p->tile2_expert, p->tile2_row0, p->tile2_mcnt);
     scatter_kernel<<<(n_routes + 255) / 256, 256, 0, st>>>(p->ids, n_routes, p->seg_start, p->cursor, p->perm, p->inv);
     gather_kernel<<<(n_routes + 7) / 8, 256, 0, st>>>(reinterpret_cast<const uint4*>(hidden), p->perm, n_routes, c.k,
                                                       c.d / 8, reinterpret_cast<uint4*>(p->xs));
     e = cudaGetLastError();
   }
-  GemmArgs ga{};
+  GemmArgs ga{};  // 128-row tiles (bf16)
   ga.n_mtiles = p->n_mtiles;
   ga.tile_expert = p->tile_expert;
   ga.tile_row0 = p->tile_row0;
   ga.seg_start = p->seg_start;
   ga.status = c.status;
+  GemmArgs ga2 = ga;  // tiles of two M tiles (MXFP4)
+  ga2.n_mtiles = p->n_mtiles2;
+  ga2.tile_expert = p->tile2_expert;
+  ga2.tile_row0 = p->tile2_row0;
+  ga2.tile_mcnt = p->tile2_mcnt;
   const bool fp4 = c.dtype == FT_DTYPE_MXFP4;
-  if (fp4) {  // the MXFP4 GEMMs walk 256-row tiles
-    ga.n_mtiles = p->n_mtiles2;
-    ga.tile_expert = p->tile2_expert;
-    ga.tile_row0 = p->tile2_row0;
-  }
-  const int max_mt = fp4 ? (n_routes + 255) / 256 + c.E : (n_routes + 127) / 128 + c.E;
+  const int max_mt = (n_routes + 127) / 128 + c.E, max_mt2 = (n_routes + 255) / 256 + c.E;
   if (prof) prof->end(st, FT_K_PREFILL, pb);
   pb = prof ? prof->begin(st) : nullptr;
   if (e == cudaSuccess) {
-    ga.out = p->hbuf;
-    ga.out_ld = c.f;
-    ga.K = c.d;
-    e = fp4 ? launch_gemm_gateup_mxfp4(&p->map_x, &p->map_w1[b], &p->map_s1[b], &p->map_h_out, ga, max_mt, c.f, st)
-            : launch_gemm_gateup(&p->map_x, &p->map_w1[b], &p->map_h_out, ga, max_mt, c.f, st);
+    GemmArgs& gu = fp4 ? ga2 : ga;
+    gu.out = p->hbuf;
+    gu.out_ld = c.f;
+    gu.K = c.d;
+    e = fp4 ? launch_gemm_gateup_mxfp4(&p->map_x, &p->map_w1[b], &p->map_s1[b], &p->map_h_out, gu, max_mt2, c.f, st)
+            : launch_gemm_gateup(&p->map_x, &p->map_w1[b], &p->map_h_out, gu, max_mt, c.f, st);
   }
   if (e == cudaSuccess) {
-    ga.out = p->ybuf;
-    ga.out_ld = c.d;
-    ga.K = c.f;
-    e = fp4 ? launch_gemm_down_mxfp4(&p->map_h, &p->map_w2[b], &p->map_s2[b], &p->map_y_out, ga, max_mt, c.d, st)
-            : launch_gemm_down(&p->map_h, &p->map_w2[b], &p->map_y_out, ga, max_mt, c.d, st);
+    GemmArgs& gd = fp4 ? ga2 : ga;
+    gd.out = p->ybuf;
+    gd.out_ld = c.d;
+    gd.K = c.f;
+    e = fp4 ? launch_gemm_down_mxfp4(&p->map_h, &p->map_w2[b], &p->map_s2[b], &p->map_y_out, gd, max_mt2, c.d, st)
+            : launch_gemm_down(&p->map_h, &p->map_w2[b], &p->map_y_out, gd, max_mt, c.d, st);
   }
   if (prof) prof->end(st, FT_K_GEMM, pb);
   pb = prof ? prof->begin(st) : nullptr;
