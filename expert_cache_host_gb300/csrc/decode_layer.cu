@@ -55,6 +55,7 @@ constexpr int kMaxGroupsWarp = 64;         // groups whose values warp 0 fetches
 constexpr int kTile = 16384;               // bytes per ring stage
 constexpr int kXPre = 2;                   // uint4 of a hidden row per consumer (d <= 8192)
 constexpr int kFillUnroll = 16;            // 16-byte host loads in flight per fill thread
+constexpr int kFillTail = 4;               // the same for the last pieces of an expert (predicated)
 constexpr int kCtasPerSm = 1;              // CTAs of the grid on each SM (two measured no faster, with spills)
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
@@ -122,7 +123,17 @@ __device__ void fill_role(const LayerArgs& la) {
 #pragma unroll
         for (int j = 0; j < kFillUnroll; ++j) dst[v + j * nth] = r[j];
       }
-      for (; v < bx16; v += nth) dst[v] = src[v];
+      // the rest in predicated batches of kFillTail loads in flight: copying it
+      // one piece after the other would cost a host round trip per piece
+      for (; v < bx16; v += kFillTail * nth) {
+        int4 r[kFillTail];
+#pragma unroll
+        for (int j = 0; j < kFillTail; ++j)
+          if (v + j * nth < bx16) r[j] = src[v + j * nth];
+#pragma unroll
+        for (int j = 0; j < kFillTail; ++j)
+          if (v + j * nth < bx16) dst[v + j * nth] = r[j];
+      }
     } else if (blockIdx.x == 0 && threadIdx.x == 0) {
       atomicOr(a.status, FT_ST_BAD_SLOT);
     }

@@ -40,15 +40,17 @@ __global__ void __launch_bounds__(kFillThreads)
     }
     const int4* src = pool + (size_t)u * bx16;
     int4* dst = arena + (size_t)s * bx16;
-    size_t v = tid;
-    for (; v + (kUnroll - 1) * nthreads < bx16; v += kUnroll * nthreads) {
+    // batches of kUnroll loads in flight, the last one predicated: a
+    // copy-one-then-the-next tail would cost a host round trip per piece
+    for (size_t v = tid; v < bx16; v += kUnroll * nthreads) {
       int4 r[kUnroll];
 #pragma unroll
-      for (int j = 0; j < kUnroll; ++j) r[j] = src[v + j * nthreads];
+      for (int j = 0; j < kUnroll; ++j)
+        if (v + j * nthreads < bx16) r[j] = src[v + j * nthreads];
 #pragma unroll
-      for (int j = 0; j < kUnroll; ++j) dst[v + j * nthreads] = r[j];
+      for (int j = 0; j < kUnroll; ++j)
+        if (v + j * nthreads < bx16) dst[v + j * nthreads] = r[j];
     }
-    for (; v < bx16; v += nthreads) dst[v] = src[v];
   }
   __syncthreads();
   if (threadIdx.x == 0) {

@@ -27,12 +27,15 @@ def ft():
     return lib
 
 
-def test_adaptive_ratio_follows_oracle_with_the_same_r_sequence(ft):
-    L, E, k, d, f, T, S, K_max = 2, 16, 2, 256, 128, 1, 5, 16
-    model = make_model(L, E, k, d, f, seed=31)
+@pytest.mark.parametrize("dtype,d", [(0, 256), (1, 512)])
+def test_adaptive_ratio_follows_oracle_with_the_same_r_sequence(ft, dtype, d):
+    """bf16 and MXFP4 experts (the fused decode path, the CPU expert executor
+    and a graph captured before r changes)."""
+    L, E, k, f, T, S, K_max = 2, 16, 2, 128, 1, 5, 16
+    model = make_model(L, E, k, d, f, dtype=dtype, seed=31)
     steps, r = 16, (1, 2)
-    cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, num_slots=S, k_max=K_max, t_max=T,
-                         r_num=r[0], r_den=r[1])
+    cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, dtype=dtype, num_slots=S,
+                         k_max=K_max, t_max=T, r_num=r[0], r_den=r[1])
     ctx = ft.ft_moe_init(cfg, model.pool.ctypes.data, model.pool.nbytes)
     try:
         ft.ft_cpu_executor(ctx, 2)
@@ -65,7 +68,7 @@ def test_adaptive_ratio_follows_oracle_with_the_same_r_sequence(ft):
                 for l in range(L):
                     ids, w = oracle.route(logits[s, l], k)
                     ref = cache.step(l, E, ids, r[0], r[1], K_max)
-                    full, _, _ = oracle.moe_forward(model.layer_pool(l), model.bx, 0, d, f, ids, w, hid[s, l],
+                    full, _, _ = oracle.moe_forward(model.layer_pool(l), model.bx, dtype, d, f, ids, w, hid[s, l],
                                                     slot_ids=ref.slot_ids.reshape(T, k))
                     refs.append((ids, ref))
                     fulls.append(full)
