@@ -70,11 +70,11 @@ NCU_TRAFFIC = {
     "decode_experts_mxfp4": dict(ratio=80_432_896 / 80_216_064, src="expert_cache_host_gb300/csrc/expert_decode_mxfp4.cu",
                                  sha16="c69e88ed9f44398c", profile="profiles/decode_experts_mxfp4_v4.md"),
     # two all-hit launches of the fused decode layer kernel (8 resident experts each)
-    "decode_layer": dict(ratio=154_293_248 / 150_994_944, src="expert_cache_host_gb300/csrc/decode_layer.cu",
-                         sha16="220c09e07d559334", profile="profiles/decode_layer_a3b.md"),
+    "decode_layer": dict(ratio=154_340_864 / 150_994_944, src="expert_cache_host_gb300/csrc/decode_layer.cu",
+                         sha16="21f6d1d1675fdf2c", profile="profiles/decode_layer_a3b.md"),
     # four all-hit launches of the fused kernel's MXFP4 instantiation (6 resident V4 experts each)
-    "decode_layer_mxfp4": dict(ratio=332_339_456 / 320_864_256, src="expert_cache_host_gb300/csrc/decode_layer.cu",
-                               sha16="220c09e07d559334", profile="profiles/decode_layer_mxfp4_v4.md"),
+    "decode_layer_mxfp4": dict(ratio=331_816_960 / 320_864_256, src="expert_cache_host_gb300/csrc/decode_layer.cu",
+                               sha16="21f6d1d1675fdf2c", profile="profiles/decode_layer_mxfp4_v4.md"),
 }
 
 
