@@ -48,17 +48,17 @@ constexpr int BM = 128, BK = 64, kConvWarps = 8;
 //     of W_down), accumulators double-buffered;
 //   MXFP4: 2 M tiles x 128 B rows (64 gate + 64 up; 128 rows of W_down): every
 //     dequantised B tile feeds two MMAs, accumulators double-buffered.
-// (A single accumulator buffer -- MT x B_ROWS = 512 columns -- gets 8
-// epilogue warps, so that its drain, which the MMAs then wait for, is short.)
+// Either way a tile's accumulators take 256 tensor-memory columns, so two
+// buffers fill the 512 and the epilogue of a tile overlaps the next tile's MMAs.
 template <int MODE, bool FP4>
 struct Cfg {
   static constexpr int MT = FP4 ? 2 : 1;                                   // max 128-row M tiles per tile
   static constexpr int B_ROWS = FP4 ? 128 : 256;                           // B operand rows
   static constexpr int BN = MODE == 1 ? B_ROWS / 2 : B_ROWS;               // output columns of a tile
   static constexpr uint32_t ACC_COLS = MT * B_ROWS;                        // fp32 columns of one buffer
-  static constexpr int NBUF = 512 / ACC_COLS;                              // accumulator buffers
+  static constexpr int NBUF = 2;                                           // accumulator buffers
   static constexpr uint32_t TMEM_COLS = NBUF * ACC_COLS;                   // all 512 columns
-  static constexpr int EPI = NBUF == 1 ? 8 : 4;                            // epilogue warps
+  static constexpr int EPI = 4;                                            // epilogue warps, one per lane quarter
   static constexpr int kThreads = 64 + 32 * EPI + (FP4 ? 32 * kConvWarps : 0);
   static constexpr int CONV0 = 2 + EPI;                                    // first converter warp
   static constexpr int A_TILE = BM * BK * 2;
@@ -73,8 +73,7 @@ struct Cfg {
   static constexpr int STG_BYTES = MODE == 2 ? EPI * 2 * 4096 : 0;
   static constexpr size_t SMEM = (size_t)NSTAGE * STAGE + STG_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(STAGE % 1024 == 0, "stage tiles must stay 1024-byte aligned for the 128-byte swizzle");
-  static_assert(NBUF * ACC_COLS == 512 && (NBUF == 1 || NBUF == 2), "accumulators fill the tensor memory");
-  static_assert(BN % ((EPI / 4) * OUT_COLS) == 0, "epilogue warps split the columns evenly");
+  static_assert(TMEM_COLS == 512, "two accumulator buffers fill the tensor memory");
 };
 
 // Exact 2^(s-127) for an e8m0 byte (s = 255 is NaN, s = 0 the fp32 subnormal 2^-127).
@@ -226,12 +225,9 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
     // with one TMA store (32 scattered 16-byte row pieces per store
     // instruction were bound by L2 write requests); otherwise valid rows are
     // stored directly.
-    // A warp reads the tensor-memory lane quarter warp % 4; with 8 epilogue
-    // warps, warps w and w + 4 share a quarter and split its columns.
-    const int ew = warp - 2, q = warp & 3, cs = ew >> 2;
-    constexpr int CSTEP = (C::EPI / 4) * C::OUT_COLS;
+    const int q = warp & 3;  // the tensor-memory lane quarter this warp may read
     const int row = q * 32 + lane;
-    uint8_t* my_stg = stg + ew * 2 * 4096;
+    uint8_t* my_stg = stg + q * 2 * 4096;
     int nbuf = 0;  // staging buffer to fill next (0/1)
     int i = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
@@ -252,7 +248,7 @@ __global__ void __launch_bounds__(Cfg<MODE, FP4>::kThreads, 1)
         const uint32_t lane_addr =
             tmem + (uint32_t)b * C::ACC_COLS + (uint32_t)(h * C::B_ROWS) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-        for (int c0 = cs * C::OUT_COLS; c0 < C::BN; c0 += CSTEP) {
+        for (int c0 = 0; c0 < C::BN; c0 += C::OUT_COLS) {
           uint4 packed[8];  // 128 bytes of this row's output columns c0 .. c0 + OUT_COLS
           if (MODE == 1) {
             uint32_t* pw = reinterpret_cast<uint32_t*>(packed);
