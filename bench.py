@@ -73,6 +73,12 @@ NCU_TRAFFIC = {
     "decode_layer": dict(ratio=154_340_864 / 150_994_944, src="expert_cache_host_gb300/csrc/decode_layer.cu",
                          sha16="21f6d1d1675fdf2c", profile="profiles/decode_layer_a3b.md"),
     # four all-hit launches of the fused kernel's MXFP4 instantiation (6 resident V4 experts each)
+    # both prefill GEMMs of one layer (gate/up + down): the A3B 8192-token chunk, and the V4 shape with 64
+    # experts and 2048 tokens (192 rows per expert, as in its 8192-token chunk)
+    "grouped_gemm": dict(ratio=2_153_847_296 / 2_214_592_512, src="expert_cache_host_gb300/csrc/grouped_gemm.cu",
+                         sha16="5f68d3782a496771", profile="profiles/grouped_gemm_prefill_a3b.md"),
+    "grouped_gemm_mxfp4": dict(ratio=1_215_293_952 / 1_258_291_200, src="expert_cache_host_gb300/csrc/grouped_gemm.cu",
+                               sha16="5f68d3782a496771", profile="profiles/grouped_gemm_prefill_mxfp4_v4.md"),
     "decode_layer_mxfp4": dict(ratio=331_816_960 / 320_864_256, src="expert_cache_host_gb300/csrc/decode_layer.cu",
                                sha16="21f6d1d1675fdf2c", profile="profiles/decode_layer_mxfp4_v4.md"),
 }
@@ -656,6 +662,9 @@ def run_prefill_leg(args, w, pool):
         finally:
             ft.ft_moe_destroy(ctx)
     pool_bytes = L * E * bx
+    # algorithmic bytes of one layer's two GEMMs: X in, the layer's experts, H out and back in, Y out
+    gemm_bytes = T * k * d * 2 + E * bx + 2 * T * k * f * 2 + T * k * d * 4
+    gemm_traffic, gemm_traffic_note = ncu_traffic("grouped_gemm" if dt == 0 else "grouped_gemm_mxfp4", gemm_bytes)
     up_ms, up_n = prof_chunk["upload"]
     gemm_ms, gemm_n = prof_res["gemm"]
     flops_layer = T * k * 3 * d * f * 2  # 3 matrices of d*f MACs per (token, expert), 2 flops per MAC
@@ -663,7 +672,8 @@ def run_prefill_leg(args, w, pool):
     upload_gbs = up_n * E * bx / (up_ms / 1e3) / 1e9 if up_n else 0.0
     return dict(L=L, T=T, chunk_s=res[2], chunk_s_single_buffer=res[1], pool_bytes=pool_bytes,
                 link_gbs=pool_bytes / res[2] / 1e9, upload_gbs=upload_gbs, gemm_tflops=gemm_tflops,
-                gemm_ms_per_layer=gemm_ms / max(1, gemm_n), status=status,
+                gemm_ms_per_layer=gemm_ms / max(1, gemm_n), status=status, gemm_bytes_per_layer=gemm_bytes,
+                gemm_traffic_per_layer=gemm_traffic, gemm_traffic_source=gemm_traffic_note,
                 overlap_loss_without_double_buffer=1.0 - res[2] / res[1])
 
 
@@ -1113,7 +1123,10 @@ def build_line(args, w, world, dec, link, pre, ctl, peaks, comps=None):
             "roofline_gemm": {"bound": "tensor", "kernel": "grouped SwiGLU GEMMs (tcgen05), weights resident",
                               "achieved": round(pre["gemm_tflops"], 1), "peak": peaks["bf16_tflops"],
                               "unit": "TFLOP/s", "frac": round(pre["gemm_tflops"] / peaks["bf16_tflops"], 4),
-                              "ms_per_layer": round(pre["gemm_ms_per_layer"], 3), "traffic": None,
+                              "ms_per_layer": round(pre["gemm_ms_per_layer"], 3),
+                              "traffic": pre["gemm_traffic_per_layer"], "traffic_unit": "bytes per layer (both GEMMs)",
+                              "algorithmic_bytes_per_layer": pre["gemm_bytes_per_layer"],
+                              "traffic_source": pre["gemm_traffic_source"],
                               "peak_source": peaks["source"] + " (burst bf16)"},
         }
     if ctl:
@@ -1371,6 +1384,10 @@ def run_v4_components(args, local):
                                   "achieved": round(pre["gemm_tflops"], 1), "peak": bf16_peak, "unit": "TFLOP/s",
                                   "frac": round(pre["gemm_tflops"] / bf16_peak, 4),
                                   "ms_per_layer": round(pre["gemm_ms_per_layer"], 3),
+                                  "traffic": pre["gemm_traffic_per_layer"],
+                                  "traffic_unit": "bytes per layer (both GEMMs)",
+                                  "algorithmic_bytes_per_layer": pre["gemm_bytes_per_layer"],
+                                  "traffic_source": pre["gemm_traffic_source"],
                                   "peak_source": peaks["source"] + " (burst bf16)"},
             }
     finally:
