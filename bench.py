@@ -1012,6 +1012,8 @@ def experts_traffic(w, dec):
     else:
         per = dec.get("ex_bytes", 0.0) / max(1, dec.get("ex_n", 0))
         key = "decode_experts" if w["dtype"] == 0 else "decode_experts_mxfp4"
+    if per <= 0:
+        return per, None, "no resident experts in the timed window"
     tr, note = ncu_traffic(key, per)
     return per, tr, note
 
@@ -1068,6 +1070,8 @@ def build_line(args, w, world, dec, link, pre, ctl, peaks, comps=None):
                                                                      if fused else ""),
                      "achieved": round(fill_gbs, 1), "peak": link_gbs, "unit": "GB/s",
                      "frac": round(fill_gbs / link_gbs, 4) if link_gbs else None, "traffic": None,
+                     "traffic_note": "DRAM counters do not see the host link; its bytes per fill launch equal q x B_x "
+                                     "to 0.001 % (system-memory read sectors, profiles/fill_host_link_a3b.md)",
                      "achieved_how": "bytes filled / summed fill spans (first fill CTA start to last fill CTA end, "
                                      "device clock) over the timed window",
                      "peak_source": "measured in this run: the whole pool streamed host -> device once in 1 GiB "
