@@ -95,3 +95,21 @@ def test_reference_arm_prints_the_same_config_and_integer_steps():
     assert ref["warmup"] == 3 and ref["config"] == bench.line_config(args, w, 1)
     assert ref["metric"] == bench.metric_name(args, w) and ref["unit"] == "tok/s" and ref["value"] > 0
     assert set(ref["e2e"]) == {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
+
+
+def test_fused_resident_phase_needs_resident_experts():
+    """Fused path: the experts' HBM rate is the resident phase's bytes over its
+    span, and is not reported when the window held less than one resident
+    expert per launch (hit rate ~0), nor is a traffic figure."""
+    bx = 9_437_184
+    dec = dict(_dec(), path="fused", bx=bx,
+               meters={"resident_bytes": 8 * bx * 10.0, "resident_s": 10 * 20e-6, "resident_launches": 10})
+    gbs, how = bench.experts_rate(dec)
+    assert gbs == pytest.approx(8 * bx / 20e-6 / 1e9) and "resident" in how
+    per, tr, note = bench.experts_traffic(dict(bench.A3B), dec)
+    assert per == pytest.approx(8 * bx)
+    dec_none = dict(dec, meters={"resident_bytes": 0.3 * bx * 10, "resident_s": 10 * 2e-6, "resident_launches": 10})
+    assert bench.experts_rate(dec_none) == (0.0, None)
+    dec_zero = dict(dec, meters={"resident_bytes": 0.0, "resident_s": 0.0, "resident_launches": 0})
+    per, tr, note = bench.experts_traffic(dict(bench.A3B), dec_zero)
+    assert tr is None and "no resident" in note
