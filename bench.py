@@ -371,11 +371,13 @@ def _window(c0, c1):
 
 
 def run_decode_leg(args, w, world, local, pool, hid, lg, with_e2e=True, seq=True, profile=True):
-    """Headline decode measurement.  Context A times tokens W..W+K-1 (device
-    inputs, graph replays); context B, which stepped through the same W warm-up
-    tokens, times the same K tokens end to end (pinned host inputs in, every
-    layer's output out).  A then runs P profiled tokens eagerly (per-kernel
-    CUDA events) and, from a cold rebuild, the whole decode sequence."""
+    """Headline decode measurement.  Context A times K tokens after W warm-up
+    tokens (device inputs, graph replays).  With the end-to-end twin B (stepped through the
+    same W warm-up tokens; pinned host inputs in, every layer's output out) the
+    two contexts step tokens W..W+2K-1 and take turns to lead: A is timed on
+    the K tokens it leads, B on the other K.  A then runs P profiled tokens
+    eagerly (per-kernel CUDA events) and, from a cold rebuild, the whole decode
+    sequence."""
     import torch
 
     import expert_cache_host_gb300 as ft
@@ -408,38 +410,67 @@ def run_decode_leg(args, w, world, local, pool, hid, lg, with_e2e=True, seq=True
             torch.distributed.barrier()
         c0 = A.counters()
         ft.ft_decode_meters(A.ctx, reset=True)
-        it = iter(range(W, W + K))
-        with torch.cuda.stream(A.stream):
-            with ClockSampler(local) as clk:
-                elapsed = timed(A.stream, lambda: A.step(next(it)), K)
-        if world > 1:
-            torch.distributed.barrier()
-        c1 = A.counters()
-        res["meters"] = ft.ft_decode_meters(A.ctx, reset=True)  # fill and resident-expert phases of the window
-        res["path"] = "fused" if ft.ft_decode_path(A.ctx) == ft.FT_DECODE_FUSED else "split"
-        clocks = clk.summary()
-        hits, misses, fills, cpu = _window(c0, c1)
-
         e2e_elapsed = None
         if B:
             h_hid = torch.from_numpy(hid.view(np.int16)).pin_memory()
             h_lg = torch.from_numpy(lg).pin_memory()
             h_out = torch.empty((L, T, d), dtype=torch.float32).pin_memory()
             cb0 = B.counters()
-            it2 = iter(range(W, W + K))
+            e2e_elapsed = 0.0
 
-            def e2e_step():
-                i = next(it2)
+            def e2e_step(i):
                 B.cur_hid.copy_(h_hid[i], non_blocking=True)
                 B.cur_lg.copy_(h_lg[i], non_blocking=True)
                 B.graph.replay()
                 h_out.copy_(B.out, non_blocking=True)
 
-            with torch.cuda.stream(B.stream):
-                e2e_elapsed = timed(B.stream, e2e_step, K)
-            cb1 = B.counters()
+        with ClockSampler(local) as clk:
+            if not B:
+                it = iter(range(W, W + K))
+                with torch.cuda.stream(A.stream):
+                    elapsed = timed(A.stream, lambda: A.step(next(it)), K)
+                dA = A.counters() - c0
+                meters = ft.ft_decode_meters(A.ctx, reset=True)
+            else:
+                # The two contexts step the same 2K tokens and take turns to go
+                # first: A leads the even tokens, B (end to end) the odd ones,
+                # and each is timed only on the tokens it leads.  The context
+                # that follows reads the pool pages the leader has just read
+                # and runs a few per cent faster, so no follower token is
+                # timed, and both sums see the same host-link conditions.
+                elapsed = 0.0
+                dA = np.zeros_like(c0)
+                meters = None
+                for j in range(2 * K):
+                    i = W + j
+                    if j % 2 == 0:
+                        ca = A.counters()
+                        ft.ft_decode_meters(A.ctx, reset=True)
+                        with torch.cuda.stream(A.stream):
+                            elapsed += timed(A.stream, lambda: A.step(i))
+                        m = ft.ft_decode_meters(A.ctx, reset=True)
+                        meters = m if meters is None else {n: meters[n] + m[n] for n in m}
+                        dA += A.counters() - ca
+                        with torch.cuda.stream(B.stream):
+                            e2e_step(i)
+                        B.stream.synchronize()
+                    else:
+                        with torch.cuda.stream(B.stream):
+                            e2e_elapsed += timed(B.stream, lambda: e2e_step(i))
+                        with torch.cuda.stream(A.stream):
+                            A.step(i)
+                        A.stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        res["meters"] = meters  # fill and resident-expert phases of the timed tokens
+        res["path"] = "fused" if ft.ft_decode_path(A.ctx) == ft.FT_DECODE_FUSED else "split"
+        clocks = clk.summary()
+        hits, misses, fills, cpu = _window(np.zeros_like(dA), dA)
+        end = W + K
+        if B:
+            end = W + 2 * K
             # same tokens from the same cache state: the control streams agree
-            res["e2e_same_window"] = bool(np.array_equal(cb1 - cb0, c1 - c0))
+            res["e2e_same_window"] = bool(np.array_equal(B.counters() - cb0, A.counters() - c0))
             B.destroy()
             B = None
 
@@ -449,7 +480,7 @@ def run_decode_leg(args, w, world, local, pool, hid, lg, with_e2e=True, seq=True
             ft.ft_profile_read(A.ctx, reset=True)
             cp0 = A.counters()
             with torch.cuda.stream(A.stream):
-                for i in range(W + K, W + K + P):
+                for i in range(end, end + P):
                     A.cur_hid.copy_(d_hid[i])
                     A.cur_lg.copy_(d_lg[i])
                     A.token(A.stream.cuda_stream)
@@ -1105,8 +1136,9 @@ def build_line(args, w, world, dec, link, pre, ctl, peaks, comps=None):
     if "e2e" in dec:
         line["e2e"] = {"value": round(dec["e2e"], 3), "unit": "tok/s", "h2d_bytes_per_step": dec["h2d"],
                        "d2h_bytes_per_step": dec["d2h"]}
-        line["components"]["e2e_how"] = ("a twin context stepped through the same warm-up tokens times the same K "
-                                         "tokens with host copies; control streams identical: %s"
+        line["components"]["e2e_how"] = ("a twin context (host copies in and out) and the device-timed context step the "
+                                         "same 2K tokens and take turns to go first; each is timed on the K "
+                                         "tokens it leads; control streams identical: %s"
                                          % dec.get("e2e_same_window"))
     if "sequence" in dec:
         line["components"]["sequence"] = dec["sequence"]
@@ -1252,7 +1284,7 @@ def main():
         run_sweep(args, w, world, local)
         return
     hp, pool, t_pool = make_host_pool(args, w)
-    n_in = max(args.warmup + args.steps + min(args.steps, args.profile_steps), w["seq"])
+    n_in = max(args.warmup + 2 * args.steps + min(args.steps, args.profile_steps), w["seq"])
     hid, lg = decode_inputs(w, n_in)
     if args.repeat_tokens:
         hid = np.ascontiguousarray(np.repeat(hid[:(n_in + 1) // 2], 2, axis=0)[:n_in])
