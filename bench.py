@@ -659,39 +659,46 @@ def run_prefill_leg(args, w, pool):
     del hid, lg
     out = torch.empty((T, d), dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
-    res = {}
-    for buffers in (2, 1):
-        cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, dtype=dt, num_slots=1, k_max=1,
-                             t_max=1, prefill_buffers=buffers, prefill_t_max=T)
-        ctx = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
-        try:
-            with torch.cuda.stream(stream):
-                st = stream.cuda_stream
+    # The double- and the single-buffer context take turns, three timed chunks
+    # each, and each reports its median: the host link has slow spells of
+    # seconds, which would otherwise land on one setting only.
+    ctxs, times = {}, {2: [], 1: []}
+    try:
+        for buffers in (2, 1):
+            cfg = ft.make_config(num_layers=L, num_experts=E, top_k=k, hidden=d, inter=f, dtype=dt, num_slots=1,
+                                 k_max=1, t_max=1, prefill_buffers=buffers, prefill_t_max=T)
+            ctxs[buffers] = ft.ft_moe_init(cfg, pool.ctypes.data, pool.nbytes)
+        with torch.cuda.stream(stream):
+            st = stream.cuda_stream
 
-                def chunk():
-                    for l in range(L):
-                        ft.ft_moe_forward(ctx, l, ft.FT_PREFILL_LAYER, d_lg[l].data_ptr(), d_hid[l].data_ptr(), T, 0,
-                                          out.data_ptr(), st)
-
-                chunk()  # warm-up chunk (each chunk re-uploads the whole pool: layer 0 is not resident)
-                times = [timed(stream, chunk) for _ in range(2)]
-                res[buffers] = min(times)
-                if buffers == 2:
-                    # upload rate and grouped-GEMM throughput, weights resident (layer 0 twice in a row)
-                    ft.ft_profile_enable(ctx, True)
-                    ft.ft_profile_read(ctx, reset=True)
-                    chunk()
-                    prof_chunk = ft.ft_profile_read(ctx, reset=True)
-                    for _ in range(3):
-                        ft.ft_moe_forward(ctx, 0, ft.FT_PREFILL_LAYER, d_lg[0].data_ptr(), d_hid[0].data_ptr(), T, 0,
-                                          out.data_ptr(), st)
-                    ft.ft_moe_forward(ctx, 0, ft.FT_PREFILL_LAYER, d_lg[0].data_ptr(), d_hid[0].data_ptr(), T, 0,
+            def chunk(ctx):
+                for l in range(L):
+                    ft.ft_moe_forward(ctx, l, ft.FT_PREFILL_LAYER, d_lg[l].data_ptr(), d_hid[l].data_ptr(), T, 0,
                                       out.data_ptr(), st)
-                    prof_res = ft.ft_profile_read(ctx, reset=True)
-                    ft.ft_profile_enable(ctx, False)
-            status = ft.ft_get_status(ctx)
-        finally:
-            ft.ft_moe_destroy(ctx)
+
+            for buffers in (2, 1):
+                chunk(ctxs[buffers])  # warm-up chunk (each chunk re-uploads the whole pool)
+            for _ in range(3):
+                for buffers in (2, 1):
+                    times[buffers].append(timed(stream, lambda: chunk(ctxs[buffers])))
+            # upload rate and grouped-GEMM throughput, weights resident (layer 0 twice in a row)
+            ctx = ctxs[2]
+            ft.ft_profile_enable(ctx, True)
+            ft.ft_profile_read(ctx, reset=True)
+            chunk(ctx)
+            prof_chunk = ft.ft_profile_read(ctx, reset=True)
+            for _ in range(3):
+                ft.ft_moe_forward(ctx, 0, ft.FT_PREFILL_LAYER, d_lg[0].data_ptr(), d_hid[0].data_ptr(), T, 0,
+                                  out.data_ptr(), st)
+            ft.ft_moe_forward(ctx, 0, ft.FT_PREFILL_LAYER, d_lg[0].data_ptr(), d_hid[0].data_ptr(), T, 0,
+                              out.data_ptr(), st)
+            prof_res = ft.ft_profile_read(ctx, reset=True)
+            ft.ft_profile_enable(ctx, False)
+        status = max(ft.ft_get_status(c) for c in ctxs.values())
+    finally:
+        for c in ctxs.values():
+            ft.ft_moe_destroy(c)
+    res = {b_: statistics.median(v) for b_, v in times.items()}
     pool_bytes = L * E * bx
     # algorithmic bytes of one layer's two GEMMs: X in, the layer's experts, H out and back in, Y out
     gemm_bytes = T * k * d * 2 + E * bx + 2 * T * k * f * 2 + T * k * d * 4
@@ -705,6 +712,7 @@ def run_prefill_leg(args, w, pool):
                 link_gbs=pool_bytes / res[2] / 1e9, upload_gbs=upload_gbs, gemm_tflops=gemm_tflops,
                 gemm_ms_per_layer=gemm_ms / max(1, gemm_n), status=status, gemm_bytes_per_layer=gemm_bytes,
                 gemm_traffic_per_layer=gemm_traffic, gemm_traffic_source=gemm_traffic_note,
+                chunk_s_runs={"double": [round(t, 4) for t in times[2]], "single": [round(t, 4) for t in times[1]]},
                 overlap_loss_without_double_buffer=1.0 - res[2] / res[1])
 
 
@@ -1071,10 +1079,18 @@ def decode_summary(w, dec, peaks, link_gbs):
     return r
 
 
+def fill_link_peak(link):
+    """The host-link peak of the decode fill fractions: the median rate of the
+    pool's 1 GiB chunks (a fill reads experts scattered over the pool; a
+    few slow regions pull the whole-pool rate down but not the median)."""
+    return link["chunk_gbs_median"] if link else 0.0
+
+
 def build_line(args, w, world, dec, link, pre, ctl, peaks, comps=None):
     """The bench line.  `link` is the host-link record (host_link_profile);
-    its whole-pool rate is the peak of the host-link fractions."""
-    link_gbs = link["whole_pool_gbs"] if link else 0.0
+    its median 1 GiB chunk rate is the peak of the fill's host-link fraction,
+    its whole-pool rate that of the prefill's."""
+    link_gbs = fill_link_peak(link)
     ex_gbs, ex_how = experts_rate(dec)
     fill_gbs = fill_rate(dec)
     fused = dec.get("path") == "fused"
@@ -1105,8 +1121,8 @@ def build_line(args, w, world, dec, link, pre, ctl, peaks, comps=None):
                                      "to 0.001 % (system-memory read sectors, profiles/fill_host_link_a3b.md)",
                      "achieved_how": "bytes filled / summed fill spans (first fill CTA start to last fill CTA end, "
                                      "device clock) over the timed window",
-                     "peak_source": "measured in this run: the whole pool streamed host -> device once in 1 GiB "
-                                    "copy-engine chunks",
+                     "peak_source": "measured in this run: the median rate of the pool's 1 GiB chunks, each "
+                                    "streamed host -> device once by the copy engine (whole-pool rate: host_link)",
                      "share": dec.get("shares", {}).get("experts" if fused else "fill")},
         "roofline_experts": {"bound": "hbm",
                              "kernel": ("decode experts resident before the step (fused decode layer kernel, compute "
@@ -1149,6 +1165,8 @@ def build_line(args, w, world, dec, link, pre, ctl, peaks, comps=None):
         line["prefill"] = {
             "workload": f"{pre['T']}-token chunk, A3B-style, {pre['L']} layers, full-layer double buffer",
             "chunk_s": round(pre["chunk_s"], 4), "chunk_s_single_buffer": round(pre["chunk_s_single_buffer"], 4),
+            "chunk_s_runs": pre["chunk_s_runs"],
+            "chunk_timing": "median of three chunks per setting, double and single buffer taking turns",
             "loss_without_double_buffer": round(pre["overlap_loss_without_double_buffer"], 4),
             "tok_s": round(pre["T"] / pre["chunk_s"], 1), "pool_gb": round(pre["pool_bytes"] / 1e9, 2),
             "link_gbs_effective": round(pre["link_gbs"], 1), "upload_gbs": round(pre["upload_gbs"], 1),
@@ -1314,7 +1332,7 @@ def main():
             for rr in ((1, 2), (2, 1)):
                 wr_ = dict(w, r=rr, desc=w["desc"].replace("BP/BH=1", f"BP/BH={rr[0]}/{rr[1]}"))
                 d_r = run_decode_leg(cargs, wr_, 1, local, pool, hid, lg, with_e2e=False, seq=False)
-                comps[f"decode_r_{rr[0]}_{rr[1]}"] = decode_summary(wr_, d_r, measured_peaks(), link["whole_pool_gbs"])
+                comps[f"decode_r_{rr[0]}_{rr[1]}"] = decode_summary(wr_, d_r, measured_peaks(), fill_link_peak(link))
             comps["decode_adaptive_r"] = run_adaptive_leg(cargs, w, pool, hid, lg)
             comps["route_control_graph"] = run_route_control_leg(w)
             comps["tiny"] = run_tiny_leg()
@@ -1400,7 +1418,7 @@ def run_v4_components(args, local):
             n_in = max(args.warmup + args.steps + min(args.steps, args.profile_steps), w["seq"] if T == 1 else 0)
             hid, lg = decode_inputs(wt, n_in)
             d = run_decode_leg(args, wt, 1, local, pool, hid, lg, with_e2e=False, seq=(T == 1))
-            s = decode_summary(wt, d, peaks, link["whole_pool_gbs"])
+            s = decode_summary(wt, d, peaks, fill_link_peak(link))
             _, tr, note = experts_traffic(wt, d)
             s["experts_traffic_per_launch"], s["experts_traffic_source"] = tr, note
             out[f"batch_{T}"] = s
@@ -1412,6 +1430,8 @@ def run_v4_components(args, local):
                 "workload": f"{pre['T']}-token chunk, V4-Flash-style MXFP4, {pre['L']} layers, full-layer double "
                             "buffer",
                 "chunk_s": round(pre["chunk_s"], 4), "chunk_s_single_buffer": round(pre["chunk_s_single_buffer"], 4),
+                "chunk_s_runs": pre["chunk_s_runs"],
+                "chunk_timing": "median of three chunks per setting, double and single buffer taking turns",
                 "tok_s": round(pre["T"] / pre["chunk_s"], 1), "pool_gb": round(pre["pool_bytes"] / 1e9, 2),
                 "link_gbs_effective": round(pre["link_gbs"], 1), "upload_gbs": round(pre["upload_gbs"], 1),
                 "link_frac": round(pre["link_gbs"] / link["whole_pool_gbs"], 4), "device_status": pre["status"],

@@ -44,7 +44,8 @@ def test_line_has_the_contract_keys():
     assert set(r) >= {"bound", "achieved", "peak", "unit", "frac", "traffic"}
     # achieved = fill bytes / fill time; frac = achieved / peak
     assert r["achieved"] == pytest.approx(1.0e9 / 6.0e-3 / 1e9, abs=0.05)
-    assert r["frac"] == pytest.approx(r["achieved"] / 211.0, abs=1e-3)
+    # the link peak of the fill is the median 1 GiB chunk rate, not the whole-pool rate
+    assert r["peak"] == 210.0 and r["frac"] == pytest.approx(r["achieved"] / 210.0, abs=1e-3)
     e = line["e2e"]
     assert set(e) == {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
     assert line["ms_per_step"] == pytest.approx(0.5 / 100 * 1e3)
@@ -73,7 +74,7 @@ def test_timed_window_and_host_link_are_reported():
     line = bench.build_line(_args(), w, 1, _dec(), LINK, None, None, PEAKS)
     tw = line["timed_window"]
     assert tw["tokens"] == [8, 108] and tw["hit_rate"] == pytest.approx(0.8)
-    assert line["host_link"]["whole_pool_gbs"] == 211.0 and line["roofline"]["peak"] == 211.0
+    assert line["host_link"]["whole_pool_gbs"] == 211.0 and line["roofline"]["peak"] == 210.0
     # the config object is the workload alone (the reference arm prints the same one)
     assert line["config"] == bench.line_config(_args(), w, 1)
 
