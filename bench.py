@@ -440,6 +440,7 @@ def run_decode_leg(args, w, world, local, pool, hid, lg, with_e2e=True, seq=True
                 # timed, and both sums see the same host-link conditions.
                 elapsed = 0.0
                 dA = np.zeros_like(c0)
+                dB = np.zeros_like(c0)  # the control counters of the tokens B leads
                 meters = None
                 for j in range(2 * K):
                     i = W + j
@@ -455,8 +456,10 @@ def run_decode_leg(args, w, world, local, pool, hid, lg, with_e2e=True, seq=True
                             e2e_step(i)
                         B.stream.synchronize()
                     else:
+                        cb = B.counters()
                         with torch.cuda.stream(B.stream):
                             e2e_elapsed += timed(B.stream, lambda: e2e_step(i))
+                        dB += B.counters() - cb
                         with torch.cuda.stream(A.stream):
                             A.step(i)
                         A.stream.synchronize()
@@ -471,6 +474,8 @@ def run_decode_leg(args, w, world, local, pool, hid, lg, with_e2e=True, seq=True
             end = W + 2 * K
             # same tokens from the same cache state: the control streams agree
             res["e2e_same_window"] = bool(np.array_equal(B.counters() - cb0, A.counters() - c0))
+            # the two timed token sets differ: their fills per token, side by side
+            res["e2e_fills"] = (_window(np.zeros_like(dB), dB)[2], fills)
             B.destroy()
             B = None
 
@@ -1152,6 +1157,10 @@ def build_line(args, w, world, dec, link, pre, ctl, peaks, comps=None):
     if "e2e" in dec:
         line["e2e"] = {"value": round(dec["e2e"], 3), "unit": "tok/s", "h2d_bytes_per_step": dec["h2d"],
                        "d2h_bytes_per_step": dec["d2h"]}
+        if dec.get("e2e_fills"):
+            fb, fa = dec["e2e_fills"]
+            line["components"]["e2e_fills_per_token"] = {"e2e_tokens": round(fb / (dec["K"] * dec["T"]), 3),
+                                                          "value_tokens": round(fa / (dec["K"] * dec["T"]), 3)}
         line["components"]["e2e_how"] = ("a twin context (host copies in and out) and the device-timed context step the "
                                          "same 2K tokens and take turns to go first; each is timed on the K "
                                          "tokens it leads; control streams identical: %s"

@@ -114,3 +114,12 @@ def test_fused_resident_phase_needs_resident_experts():
     dec_zero = dict(dec, meters={"resident_bytes": 0.0, "resident_s": 0.0, "resident_launches": 0})
     per, tr, note = bench.experts_traffic(dict(bench.A3B), dec_zero)
     assert tr is None and "no resident" in note
+
+
+def test_e2e_token_sets_report_their_fills():
+    """The device-timed and the end-to-end contexts are timed on different
+    halves of the same 2K tokens: the line shows each half's fills per token."""
+    w = dict(bench.A3B)
+    line = bench.build_line(_args(), w, 1, dict(_dec(), e2e_fills=(140.0, 150.0)), LINK, None, None, PEAKS)
+    f = line["components"]["e2e_fills_per_token"]
+    assert f == {"e2e_tokens": 1.4, "value_tokens": 1.5}
