@@ -1417,6 +1417,7 @@ def run_v4_components(args, local):
             passes = [host_link_profile(pool) for _ in range(2)]
             link = dict(max(passes, key=lambda p: p["whole_pool_gbs"]))
             link["passes_whole_pool_gbs"] = [p["whole_pool_gbs"] for p in passes]
+            link["placement"] = pool_placement(pool)
         finally:
             ft.ft_moe_destroy(ctx)
         out["host_link"] = link
