@@ -65,20 +65,21 @@ L2_BYTES = 129 * 2 ** 20
 # it.  A launch's traffic is reported as ratio x its algorithmic bytes only
 # while the source is unchanged; otherwise traffic is null.
 NCU_TRAFFIC = {
-    "decode_experts": dict(ratio=123_111_424 / 122_683_392, src="expert_cache_host_gb300/csrc/expert_decode.cu",
-                           sha16="e5a4dc8ca19734a8", profile="profiles/decode_experts_a3b.md"),
-    "decode_experts_mxfp4": dict(ratio=80_432_896 / 80_216_064, src="expert_cache_host_gb300/csrc/expert_decode_mxfp4.cu",
-                                 sha16="c69e88ed9f44398c", profile="profiles/decode_experts_mxfp4_v4.md"),
+    # split decode path: three bf16 expert launches (11 experts), two MXFP4 launches (6 experts)
+    "decode_experts": dict(ratio=105_966_592 / 103_809_024, src="expert_cache_host_gb300/csrc/expert_decode.cu",
+                           sha16="8b886874d489e037", profile="profiles/decode_experts_a3b.md"),
+    "decode_experts_mxfp4": dict(ratio=81_504_000 / 80_216_064, src="expert_cache_host_gb300/csrc/expert_decode_mxfp4.cu",
+                                 sha16="e7d6809da31fca43", profile="profiles/decode_experts_mxfp4_v4.md"),
     # two all-hit launches of the fused decode layer kernel (8 resident experts each)
     "decode_layer": dict(ratio=154_340_864 / 150_994_944, src="expert_cache_host_gb300/csrc/decode_layer.cu",
                          sha16="21f6d1d1675fdf2c", profile="profiles/decode_layer_a3b.md"),
-    # four all-hit launches of the fused kernel's MXFP4 instantiation (6 resident V4 experts each)
     # both prefill GEMMs of one layer (gate/up + down): the A3B 8192-token chunk, and the V4 shape with 64
     # experts and 2048 tokens (192 rows per expert, as in its 8192-token chunk)
     "grouped_gemm": dict(ratio=2_153_847_296 / 2_214_592_512, src="expert_cache_host_gb300/csrc/grouped_gemm.cu",
                          sha16="5f68d3782a496771", profile="profiles/grouped_gemm_prefill_a3b.md"),
     "grouped_gemm_mxfp4": dict(ratio=1_215_293_952 / 1_258_291_200, src="expert_cache_host_gb300/csrc/grouped_gemm.cu",
                                sha16="5f68d3782a496771", profile="profiles/grouped_gemm_prefill_mxfp4_v4.md"),
+    # four all-hit launches of the fused kernel's MXFP4 instantiation (6 resident V4 experts each)
     "decode_layer_mxfp4": dict(ratio=331_816_960 / 320_864_256, src="expert_cache_host_gb300/csrc/decode_layer.cu",
                                sha16="21f6d1d1675fdf2c", profile="profiles/decode_layer_mxfp4_v4.md"),
 }
