@@ -466,9 +466,12 @@ int ft_moe_init(const ft_config* cfg, void* host_pool, size_t pool_bytes, ft_ctx
       c->fused_ns = ns;
       c->fused_groups = mg;
       c->fused_grid = want_per_sm * c->sm_count;
-      // default: 3/8 of the SMs fill (A3B decode, measured: 57 of 152 fill at 0.90-0.92 of the link,
-      // and the other 95 still finish the resident experts well before the fill)
-      const int want = cfg->fill_ctas ? cfg->fill_ctas : std::max(4, c->fused_grid * 3 / 8);
+      // default: bf16 experts, 3/8 of the SMs fill (A3B decode, measured: 57 of 152 fill at 0.90-0.92
+      // of the link, and the other 95 still finish the resident experts well before the fill; 38
+      // lost 1 % tok/s); MXFP4 experts, 1/4 (V4 decode: 38 fill at the same ~200 GB/s and tok/s as
+      // 57, and the issue-bound MXFP4 items stream 1.13x faster on the other 114)
+      const int share = cfg->dtype == FT_DTYPE_MXFP4 ? c->fused_grid / 4 : c->fused_grid * 3 / 8;
+      const int want = cfg->fill_ctas ? cfg->fill_ctas : std::max(4, share);
       c->fused_fill = std::min(want, c->fused_grid - 1);
     }
     cudaGetLastError();

@@ -94,8 +94,9 @@ extern "C" {
 #define FT_FILL_KERNEL 0      /* SM copy from the mapped pool; graph capturable */
 #define FT_FILL_COPY_ENGINE 1 /* cudaMemcpyAsync per expert; reads the fetch list back (host sync) */
 
-/* How a decode step's fill and experts are launched (bf16 experts with
- * FT_FILL_KERNEL; other configurations always take the split path):
+/* How a decode step's fill and experts are launched (FT_FILL_KERNEL, bf16
+ * experts or MXFP4 experts with hidden a multiple of 512; other
+ * configurations always take the split path):
  *  FUSED  one cooperative kernel per layer, one CTA per SM: fill_ctas CTAs copy
  *         the fetched experts from the host pool, the others run the experts
  *         resident before the step and then each installed expert as soon as
@@ -123,7 +124,8 @@ typedef struct ft_config {
   int32_t fill_mode;     /* FT_FILL_KERNEL or FT_FILL_COPY_ENGINE */
   int32_t fill_order;    /* FT_FILL_ORDER_ID or FT_FILL_ORDER_MOST_ROUTED: which q of the m misses are filled */
   int32_t decode_path;   /* FT_DECODE_FUSED (default) or FT_DECODE_SPLIT */
-  int32_t fill_ctas;     /* CTAs that fill, on either decode path (0 = the library's choice) */
+  int32_t fill_ctas;     /* CTAs that fill, on either decode path (0 = the library's choice: fused path
+                            3/8 of the SMs for bf16 experts, 1/4 for MXFP4) */
   int32_t reserved[1];   /* must be zero */
 } ft_config;
 
