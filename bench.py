@@ -383,7 +383,7 @@ def run_decode_leg(args, w, world, local, pool, hid, lg, with_e2e=True, seq=True
 
     import expert_cache_host_gb300 as ft
 
-    L, E, k, d, f, T = w["L"], w["E"], w["k"], w["d"], w["f"], w["T"]
+    L, d, f, T = w["L"], w["d"], w["f"], w["T"]
     bx = ftsynth.expert_bytes(d, f, w["dtype"])
     W, K = args.warmup, args.steps
     P = min(K, args.profile_steps) if profile else 0
@@ -607,7 +607,7 @@ def run_route_control_leg(w, batches=(1, 16), n=128):
     import torch
 
     import expert_cache_host_gb300 as ft
-    L, E, k, d, f = w["L"], w["E"], w["k"], w["d"], w["f"]
+    L, E, k = w["L"], w["E"], w["k"]
     pool = np.zeros(L * E * ftsynth.expert_bytes(256, 128, 0), dtype=np.uint8)  # never read by the control path
     out = []
     for T in batches:
@@ -909,7 +909,7 @@ def run_reference(args, w, world):
     oracle.moe_forward(pool[:w["E"] * bx], bx, w["dtype"], w["d"], w["f"], ids, wt, hid[0, 0])
     per_layer = time.time() - t0
     Ls = max(1, min(w["L"], int(args.ref_budget_s / max(1e-9, (W + K) * per_layer))))
-    rate, n, t, threads = oracle_decode_rate(w, pool, hid, lg, args.ref_budget_s, warmup_tokens=W, steps=K,
+    rate, _, t, threads = oracle_decode_rate(w, pool, hid, lg, args.ref_budget_s, warmup_tokens=W, steps=K,
                                               layers_per_step=Ls)
     what = "decode tokens" if Ls == w["L"] else f"steps of the first {Ls} of {w['L']} layers of a decode token"
     sample = f"{K} timed {what} after {W} warm-up steps from a cold cache ({t:.1f} s of oracle work)"
@@ -1065,7 +1065,6 @@ def experts_traffic(w, dec):
 
 def decode_summary(w, dec, peaks, link_gbs):
     """Per-workload decode figures (component form)."""
-    bx = ftsynth.expert_bytes(w["d"], w["f"], w["dtype"])
     r = dict(workload=w["desc"], tok_s=round(dec["value"], 3), timed_tokens=dec["K"], warmup_tokens=dec["W"],
              hit_rate=round(dec["hits"] / max(1.0, dec["hits"] + dec["misses"]), 4),
              fills_per_token=round(dec["fills"] / (dec["K"] * dec["T"]), 3),
