@@ -506,7 +506,8 @@ def run_decode_leg(args, w, world, local, pool, hid, lg, with_e2e=True, seq=True
             B.destroy()
 
     elapsed_max, units = replica_reduce(elapsed, K * T, world)
-    res.update(value=units / elapsed_max, elapsed=elapsed_max, K=K, W=W, T=T, clocks=clocks, status=status,
+    res.update(value=units / elapsed_max, elapsed=elapsed_max, K=K, W=W, T=T, stride=2 if with_e2e else 1,
+               clocks=clocks, status=status,
                t_init=t_init, hits=hits, misses=misses, fills=fills, cpu=cpu, P=P, bx=bx)
     if B is None and e2e_elapsed is not None:
         res.update(e2e=K * T / e2e_elapsed, h2d=int(lg[0].nbytes + hid[0].nbytes), d2h=int(L * T * d * 4))
@@ -1113,7 +1114,9 @@ def build_line(args, w, world, dec, link, pre, ctl, peaks, comps=None):
         "warmup": dec["W"], "ms_per_step": round(dec["elapsed"] / dec["K"] * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w["dtype"] == 0 else "e2m1*e8m0 x bf16 -> f16/f32",
         "data": "synthetic", "config": cfg,
-        "timed_window": {"tokens": [dec["W"], dec["W"] + dec["K"]], "of_sequence": w["seq"],
+        # with the end-to-end twin, value's K tokens are every second token of a 2K-token range
+        "timed_window": {"tokens": [dec["W"], dec["W"] + dec.get("stride", 1) * dec["K"]],
+                         "every": dec.get("stride", 1), "of_sequence": w["seq"],
                          "hit_rate": round(hits / max(1.0, hits + misses), 4),
                          "fills_per_token": round(dec["fills"] / (dec["K"] * dec["T"]), 3)},
         # the dominant kernel by time is the fill: host-link bound

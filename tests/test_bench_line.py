@@ -73,7 +73,10 @@ def test_timed_window_and_host_link_are_reported():
     w = dict(bench.A3B)
     line = bench.build_line(_args(), w, 1, _dec(), LINK, None, None, PEAKS)
     tw = line["timed_window"]
-    assert tw["tokens"] == [8, 108] and tw["hit_rate"] == pytest.approx(0.8)
+    assert tw["tokens"] == [8, 108] and tw["every"] == 1 and tw["hit_rate"] == pytest.approx(0.8)
+    # beside the end-to-end twin, value's tokens are every second one of 2K
+    tw2 = bench.build_line(_args(), w, 1, dict(_dec(), stride=2), LINK, None, None, PEAKS)["timed_window"]
+    assert tw2["tokens"] == [8, 208] and tw2["every"] == 2
     assert line["host_link"]["whole_pool_gbs"] == 211.0 and line["roofline"]["peak"] == 210.0
     # the config object is the workload alone (the reference arm prints the same one)
     assert line["config"] == bench.line_config(_args(), w, 1)
